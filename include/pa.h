@@ -1,0 +1,155 @@
+/*
+ * pa.h - C ABI of the GB300 (sm_103a) windowed prefill attention over a paged
+ * int8 KV pool.
+ *
+ * The operation ("int8 tensor-core prefill attention", sections "Summary" and
+ * "Why the attention, and why tensor cores"; window-off case in "Relation to
+ * open PRs"; pool layout and StreamingLLM window in "fp16 shared-memory tiles
+ * for windowed prefill attention", "Summary"):
+ *
+ *   for every sequence, query token t (absolute position) and q head h, with
+ *   kv head g = h / (n_q_heads / n_kv_heads):
+ *     key j is visible iff j <= t and, when n_win_blk > 0,
+ *       j/16 < n_sink_blk  or  j/16 >= max(0, t/16 + 1 - n_win_blk)
+ *     K_j = k_pool code * k_scale,  V_j = v_pool code * v_scale   (per token, per kv head)
+ *     out[t][h] = softmax_j(sm_scale * <q[t][h], K_j>) . V_j     over visible j
+ *
+ * computed with the pages' method: the query quantised per row in a fused
+ * prologue, per-row Q / per-token K / softmax scales applied to the integer-
+ * valued scores, an online softmax over key tiles that skips masked blocks,
+ * and the per-token V scale folded into P before P is quantised per row.
+ *
+ * Layouts (all row-major, C order):
+ *   q, out        bf16  [total_q][n_q_heads][256]          16-byte aligned
+ *   k_pool,v_pool int8  [n_pool_pages][16][n_kv_heads][256] 16-byte aligned
+ *   k_scale,
+ *   v_scale       fp32  [n_pool_pages][16][n_kv_heads]      4-byte aligned
+ *   block_table   int32 [n_seq][max_pages_per_seq]: logical page -> pool page
+ *
+ * Ownership: every tensor argument is caller-owned memory; device entry points
+ * take device pointers, pa_prefill_host takes host pointers.  The handle owns
+ * only its workspace (widened K/V copies of the visible pages, work list,
+ * error word), grown on demand and freed by pa_destroy.
+ *
+ * Asynchrony: pa_prefill / pa_prefill_batch only enqueue work on `stream`
+ * (a cudaStream_t; NULL = legacy default stream) and return; device-side
+ * failures (a bounded wait that ran out, a block-table entry outside the pool)
+ * are reported by the next pa_last_error.  A handle serialises its own calls:
+ * use one handle per concurrently running stream.
+ *
+ * Return codes: PA_OK (0) or a negative PA_E* code; pa_strerror names it.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_OK 0
+#define PA_EINVAL (-1)    /* bad argument: shape, null pointer, alignment, range */
+#define PA_EARCH (-2)     /* current device is not an sm_103 GPU */
+#define PA_ECUDA (-3)     /* a CUDA runtime call or kernel launch failed */
+#define PA_ETIMEOUT (-4)  /* a device-side wait ran out (see pa_options.wait_timeout_ms) */
+#define PA_EBADPAGE (-5)  /* a block-table entry read was outside [0, n_pool_pages) */
+#define PA_ENOMEM (-6)    /* workspace allocation failed */
+
+/* Query container (step "Q per-row quantise", fused into the kernel prologue). */
+#define PA_Q_F16 0   /* default: per-row power-of-two scale into fp16 (lossless for bf16 input) */
+#define PA_Q_INT8 1  /* the pages' grid: scale absmax/127, codes rint(q*127/absmax) in [-127,127] */
+/* P container (step "V scale folded into P, P quantised per row"). */
+#define PA_P_F16 0   /* default: P' = p * v_scale rounded to fp16 (11-bit significand) */
+#define PA_P_U8 1    /* the pages' grid per row and 64-key tile: scale max/255, codes in [0,255] */
+
+typedef struct pa_ctx* pa_handle;
+
+typedef struct {
+  int q_mode;           /* PA_Q_F16 | PA_Q_INT8 */
+  int p_mode;           /* PA_P_F16 | PA_P_U8 */
+  int wait_timeout_ms;  /* bound on every device-side wait (default 2000) */
+  int record_timing;    /* nonzero: time each launch with CUDA events (pa_timing) */
+} pa_options;
+
+typedef struct {
+  int q_off;    /* first row of this sequence in q and out */
+  int q_start;  /* absolute position of that row (tokens already cached) */
+  int n_q;      /* query tokens of this sequence (>= 1) */
+  int n_ctx;    /* context tokens in the pool; q_start + n_q <= n_ctx */
+} pa_seq;
+
+/* Fill *opt with the defaults (fp16 containers, 2000 ms waits, no timing). */
+void pa_default_options(pa_options* opt);
+
+/* Create a handle bound to the current CUDA device.  head_dim must be 256 and
+ * page_size 16; n_q_heads % n_kv_heads == 0 and 128 % (n_q_heads/n_kv_heads)
+ * == 0; n_kv_heads <= 8.  opt may be NULL (defaults).  PA_EARCH unless the
+ * device is sm_103. */
+int pa_create(pa_handle* h, int n_q_heads, int n_kv_heads, int head_dim, int page_size, int n_pool_pages,
+              int max_pages_per_seq, const pa_options* opt);
+
+/* Release the handle and its workspace (synchronises the device). */
+void pa_destroy(pa_handle h);
+
+/* One sequence: queries are tokens [q_start, q_start + n_q) of a context of
+ * n_ctx tokens whose pages block_table[0 .. ceil(n_ctx/16)) lists.  q and out
+ * hold n_q rows.  n_win_blk <= 0 turns the window off (plain causal). */
+int pa_prefill(pa_handle h, const void* q, const int8_t* k_pool, const int8_t* v_pool, const float* k_scale,
+               const float* v_scale, const int32_t* block_table, int q_start, int n_q, int n_ctx, int n_sink_blk,
+               int n_win_blk, float sm_scale, void* out, void* stream);
+
+/* Several sequences in one launch.  seqs is a HOST array of n_seq entries;
+ * block_table row s belongs to seqs[s]; all sequences share the pool. */
+int pa_prefill_batch(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* k_pool,
+                     const int8_t* v_pool, const float* k_scale, const float* v_scale, const int32_t* block_table,
+                     int n_sink_blk, int n_win_blk, float sm_scale, void* out, void* stream);
+
+/* pa_prefill_batch on HOST buffers: copies the inputs to handle-owned device
+ * memory on `stream`, runs, copies out back and synchronises the stream; the
+ * return value includes device-side errors.  Pinned host memory is fastest. */
+int pa_prefill_host(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* k_pool,
+                    const int8_t* v_pool, const float* k_scale, const float* v_scale, const int32_t* block_table,
+                    int n_sink_blk, int n_win_blk, float sm_scale, void* out, void* stream);
+
+/* Synchronise `stream`, then report and clear the first device-side error
+ * recorded since the last call (PA_ETIMEOUT, PA_EBADPAGE) or PA_ECUDA. */
+int pa_last_error(pa_handle h, void* stream);
+
+/* Launch times recorded since the last reset (needs record_timing): sums of
+ * the widening pass and the attention kernel in milliseconds, and the number
+ * of calls.  Waits for the recorded events. */
+int pa_timing(pa_handle h, int reset, double* widen_ms, double* attention_ms, int* n_calls);
+
+const char* pa_strerror(int code);
+
+/* Host-only planning, no GPU needed: the work units of a call in launch order
+ * (longest first).  units_out (may be NULL) receives up to cap entries of
+ * int32[4] = {sequence, kv head, first token, key tiles}.  Outputs: unit
+ * count, total key tiles, widened rows. */
+int pa_plan(int n_q_heads, int n_kv_heads, int n_seq, const pa_seq* seqs, int n_sink_blk, int n_win_blk,
+            int32_t* units_out, int cap, int* n_units, long long* n_tiles, int* n_widened_rows);
+
+/* Debug (tests): run the widening pass, then export sequence `seq`'s widened
+ * rows: k_out/v_out int8 [n_kv_heads][n_rows][256], ks_out/vs_out fp32
+ * [n_kv_heads][n_rows], tok_out int32 [n_rows] (logical token of each row, -1
+ * past n_ctx); all device pointers with room for `cap` rows.  *n_rows (host)
+ * receives the row count.  Synchronous. */
+int pa_debug_gather(pa_handle h, int n_seq, const pa_seq* seqs, const int8_t* k_pool, const int8_t* v_pool,
+                    const float* k_scale, const float* v_scale, const int32_t* block_table, int n_sink_blk,
+                    int n_win_blk, int seq, int8_t* k_out, int8_t* v_out, float* ks_out, float* vs_out,
+                    int32_t* tok_out, int cap, int* n_rows, void* stream);
+
+/* Debug (tests): for every work unit, the key blocks its tiles visit
+ * (unit_blocks int32 [n_units][cap], -1 padded) and per row the number of keys
+ * the kernel's mask admits (row_counts int32 [n_units][128]); device pointers.
+ * units_out (host int32 [n_units][4], as pa_plan) names each unit.  Synchronous. */
+int pa_debug_maskset(pa_handle h, int n_seq, const pa_seq* seqs, int n_sink_blk, int n_win_blk,
+                     int32_t* row_counts, int32_t* unit_blocks, int cap, int32_t* units_out, int units_cap,
+                     int* n_units, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

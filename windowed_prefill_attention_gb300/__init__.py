@@ -1,0 +1,251 @@
+"""GB300 (sm_103a) windowed prefill attention over a paged int8 KV pool.
+
+A thin ctypes binding over ``libpa.so`` (C ABI in ``include/pa.h``).  The
+functions keep the C names; they only marshal arguments (torch tensors for
+device memory, the current torch stream) and raise on a non-zero status.
+Every step of the computation runs in the library's CUDA kernels; there is no
+CPU or PyTorch fallback: if the library is missing this module fails to import.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libpa.so")
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError("libpa.so is not built; run `python -c \"import __graft_entry__ as g; g.build()\"` "
+                      "or `python windowed_prefill_attention_gb300/build.py`")
+
+_lib = C.CDLL(_LIB_PATH)
+
+PA_OK, PA_EINVAL, PA_EARCH, PA_ECUDA, PA_ETIMEOUT, PA_EBADPAGE, PA_ENOMEM = 0, -1, -2, -3, -4, -5, -6
+PA_Q_F16, PA_Q_INT8 = 0, 1
+PA_P_F16, PA_P_U8 = 0, 1
+
+EXPORTED = ("pa_default_options", "pa_create", "pa_destroy", "pa_prefill", "pa_prefill_batch", "pa_prefill_host",
+            "pa_last_error", "pa_timing", "pa_strerror", "pa_plan", "pa_debug_gather", "pa_debug_maskset")
+
+
+class pa_options(C.Structure):
+    _fields_ = [("q_mode", C.c_int), ("p_mode", C.c_int), ("wait_timeout_ms", C.c_int), ("record_timing", C.c_int)]
+
+
+class pa_seq(C.Structure):
+    _fields_ = [("q_off", C.c_int), ("q_start", C.c_int), ("n_q", C.c_int), ("n_ctx", C.c_int)]
+
+
+_vp, _i, _f = C.c_void_p, C.c_int, C.c_float
+_lib.pa_default_options.argtypes = [C.POINTER(pa_options)]
+_lib.pa_default_options.restype = None
+_lib.pa_create.argtypes = [C.POINTER(_vp), _i, _i, _i, _i, _i, _i, C.POINTER(pa_options)]
+_lib.pa_destroy.argtypes = [_vp]
+_lib.pa_destroy.restype = None
+_lib.pa_prefill.argtypes = [_vp] + [_vp] * 6 + [_i] * 5 + [_f, _vp, _vp]
+_lib.pa_prefill_batch.argtypes = [_vp, _i, C.POINTER(pa_seq)] + [_vp] * 6 + [_i, _i, _f, _vp, _vp]
+_lib.pa_prefill_host.argtypes = _lib.pa_prefill_batch.argtypes
+_lib.pa_last_error.argtypes = [_vp, _vp]
+_lib.pa_timing.argtypes = [_vp, _i, C.POINTER(C.c_double), C.POINTER(C.c_double), C.POINTER(_i)]
+_lib.pa_strerror.argtypes = [_i]
+_lib.pa_strerror.restype = C.c_char_p
+_lib.pa_plan.argtypes = [_i, _i, _i, C.POINTER(pa_seq), _i, _i, _vp, _i, C.POINTER(_i), C.POINTER(C.c_longlong),
+                         C.POINTER(_i)]
+_lib.pa_debug_gather.argtypes = ([_vp, _i, C.POINTER(pa_seq)] + [_vp] * 5 + [_i, _i, _i] + [_vp] * 5
+                                 + [_i, C.POINTER(_i), _vp])
+_lib.pa_debug_maskset.argtypes = [_vp, _i, C.POINTER(pa_seq), _i, _i, _vp, _vp, _i, _vp, _i, C.POINTER(_i), _vp]
+
+
+class PAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__("%s: %s (%d)" % (where, pa_strerror(code), code))
+        self.code = code
+
+
+def pa_strerror(code: int) -> str:
+    return _lib.pa_strerror(code).decode()
+
+
+def _check(code: int, where: str) -> int:
+    if code != PA_OK:
+        raise PAError(code, where)
+    return code
+
+
+def _seqs(seqs):
+    """[(q_off, q_start, n_q, n_ctx), ...] or an int array [n, 4] -> ctypes array."""
+    arr = np.asarray(seqs, dtype=np.int64).reshape(-1, 4)
+    out = (pa_seq * arr.shape[0])()
+    for i, (a, b, c, d) in enumerate(arr.tolist()):
+        out[i] = pa_seq(a, b, c, d)
+    return out
+
+
+def _dev(t, dtype, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return C.c_void_p(t.data_ptr())
+
+
+def _host(a, name):
+    import torch
+    if isinstance(a, torch.Tensor):
+        if a.is_cuda or not a.is_contiguous():
+            raise TypeError("%s must be a contiguous host tensor" % name)
+        return C.c_void_p(a.data_ptr())
+    a = np.asarray(a)
+    if not a.flags["C_CONTIGUOUS"]:
+        raise ValueError("%s must be contiguous" % name)
+    return a.ctypes.data_as(C.c_void_p)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def pa_default_options() -> pa_options:
+    o = pa_options()
+    _lib.pa_default_options(C.byref(o))
+    return o
+
+
+def pa_create(n_q_heads, n_kv_heads, n_pool_pages, max_pages_per_seq, head_dim=256, page_size=16,
+              q_mode=PA_Q_F16, p_mode=PA_P_F16, wait_timeout_ms=2000, record_timing=False):
+    o = pa_options(q_mode, p_mode, wait_timeout_ms, 1 if record_timing else 0)
+    h = C.c_void_p()
+    _check(_lib.pa_create(C.byref(h), n_q_heads, n_kv_heads, head_dim, page_size, n_pool_pages, max_pages_per_seq,
+                          C.byref(o)), "pa_create")
+    return h
+
+
+def pa_destroy(h) -> None:
+    _lib.pa_destroy(h)
+
+
+def _dev_inputs(q, k_pool, v_pool, k_scale, v_scale, block_table):
+    import torch
+    return [_dev(q, torch.bfloat16, "q"), _dev(k_pool, torch.int8, "k_pool"), _dev(v_pool, torch.int8, "v_pool"),
+            _dev(k_scale, torch.float32, "k_scale"), _dev(v_scale, torch.float32, "v_scale"),
+            _dev(block_table, torch.int32, "block_table")]
+
+
+def pa_prefill(h, q, k_pool, v_pool, k_scale, v_scale, block_table, q_start, n_q, n_ctx, n_sink_blk, n_win_blk,
+               sm_scale, out, stream=None) -> None:
+    import torch
+    args = _dev_inputs(q, k_pool, v_pool, k_scale, v_scale, block_table)
+    _check(_lib.pa_prefill(h, *args, q_start, n_q, n_ctx, n_sink_blk, n_win_blk, float(sm_scale),
+                           _dev(out, torch.bfloat16, "out"), _stream(stream)), "pa_prefill")
+
+
+def pa_prefill_batch(h, seqs, q, k_pool, v_pool, k_scale, v_scale, block_table, n_sink_blk, n_win_blk, sm_scale,
+                     out, stream=None) -> None:
+    import torch
+    s = _seqs(seqs)
+    args = _dev_inputs(q, k_pool, v_pool, k_scale, v_scale, block_table)
+    _check(_lib.pa_prefill_batch(h, len(s), s, *args, n_sink_blk, n_win_blk, float(sm_scale),
+                                 _dev(out, torch.bfloat16, "out"), _stream(stream)), "pa_prefill_batch")
+
+
+def pa_prefill_host(h, seqs, q, k_pool, v_pool, k_scale, v_scale, block_table, n_sink_blk, n_win_blk, sm_scale,
+                    out, stream=None) -> None:
+    """Host buffers (numpy arrays or CPU tensors; pinned is fastest); synchronous."""
+    s = _seqs(seqs)
+    args = [_host(a, n) for a, n in ((q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"), (k_scale, "k_scale"),
+                                     (v_scale, "v_scale"), (block_table, "block_table"))]
+    _check(_lib.pa_prefill_host(h, len(s), s, *args, n_sink_blk, n_win_blk, float(sm_scale), _host(out, "out"),
+                                _stream(stream)), "pa_prefill_host")
+
+
+def pa_last_error(h, stream=None) -> int:
+    """Synchronise and return the first device-side status since the last call (0 = fine)."""
+    return _lib.pa_last_error(h, _stream(stream))
+
+
+def pa_timing(h, reset=False):
+    w, a, n = C.c_double(), C.c_double(), C.c_int()
+    _check(_lib.pa_timing(h, 1 if reset else 0, C.byref(w), C.byref(a), C.byref(n)), "pa_timing")
+    return w.value, a.value, n.value
+
+
+def pa_plan(n_q_heads, n_kv_heads, seqs, n_sink_blk, n_win_blk):
+    """Host-only work plan: (units int32 [n, 4] = seq, kv head, first token, tiles; total tiles; widened rows)."""
+    s = _seqs(seqs)
+    n_units, n_tiles, n_rows = C.c_int(), C.c_longlong(), C.c_int()
+    _check(_lib.pa_plan(n_q_heads, n_kv_heads, len(s), s, n_sink_blk, n_win_blk, None, 0, C.byref(n_units),
+                        C.byref(n_tiles), C.byref(n_rows)), "pa_plan")
+    units = np.zeros((n_units.value, 4), dtype=np.int32)
+    _check(_lib.pa_plan(n_q_heads, n_kv_heads, len(s), s, n_sink_blk, n_win_blk, units.ctypes.data_as(C.c_void_p),
+                        n_units.value, C.byref(n_units), C.byref(n_tiles), C.byref(n_rows)), "pa_plan")
+    return units, n_tiles.value, n_rows.value
+
+
+def pa_debug_gather(h, seqs, k_pool, v_pool, k_scale, v_scale, block_table, n_sink_blk, n_win_blk, seq, cap,
+                    stream=None):
+    """Widened rows of sequence `seq` as the kernels see them (int8 codes, scales, logical token of each row)."""
+    import torch
+    s = _seqs(seqs)
+    dev = k_pool.device
+    hkv = k_pool.shape[2]
+    k_out = torch.empty((hkv, cap, 256), dtype=torch.int8, device=dev)
+    v_out = torch.empty_like(k_out)
+    ks_out = torch.empty((hkv, cap), dtype=torch.float32, device=dev)
+    vs_out = torch.empty_like(ks_out)
+    tok = torch.empty((cap,), dtype=torch.int32, device=dev)
+    n = C.c_int()
+    _check(_lib.pa_debug_gather(h, len(s), s, _dev(k_pool, torch.int8, "k_pool"), _dev(v_pool, torch.int8, "v_pool"),
+                                _dev(k_scale, torch.float32, "k_scale"), _dev(v_scale, torch.float32, "v_scale"),
+                                _dev(block_table, torch.int32, "block_table"), n_sink_blk, n_win_blk, seq,
+                                C.c_void_p(k_out.data_ptr()), C.c_void_p(v_out.data_ptr()),
+                                C.c_void_p(ks_out.data_ptr()), C.c_void_p(vs_out.data_ptr()),
+                                C.c_void_p(tok.data_ptr()), cap, C.byref(n), _stream(stream)), "pa_debug_gather")
+    r = n.value
+    # the export packs rows densely as [HKV][n_rows]
+    k_flat = k_out.reshape(-1)[: hkv * r * 256].reshape(hkv, r, 256)
+    v_flat = v_out.reshape(-1)[: hkv * r * 256].reshape(hkv, r, 256)
+    ks = ks_out.reshape(-1)[: hkv * r].reshape(hkv, r)
+    vs = vs_out.reshape(-1)[: hkv * r].reshape(hkv, r)
+    return k_flat, v_flat, ks, vs, tok[:r]
+
+
+def pa_debug_maskset(h, seqs, n_sink_blk, n_win_blk, units_cap, cap, stream=None):
+    """Per unit: visited key blocks and per-row admitted key counts (see include/pa.h)."""
+    import torch
+    s = _seqs(seqs)
+    counts = torch.empty((units_cap, 128), dtype=torch.int32, device="cuda")
+    blocks = torch.empty((units_cap, cap), dtype=torch.int32, device="cuda")
+    units = np.zeros((units_cap, 4), dtype=np.int32)
+    n = C.c_int()
+    _check(_lib.pa_debug_maskset(h, len(s), s, n_sink_blk, n_win_blk, C.c_void_p(counts.data_ptr()),
+                                 C.c_void_p(blocks.data_ptr()), cap, units.ctypes.data_as(C.c_void_p), units_cap,
+                                 C.byref(n), _stream(stream)), "pa_debug_maskset")
+    k = n.value
+    return units[:k], counts[:k], blocks[:k]
+
+
+class Handle:
+    """Owns a pa_handle; ``close()`` (or garbage collection) destroys it."""
+
+    def __init__(self, n_q_heads, n_kv_heads, n_pool_pages, max_pages_per_seq, **opts):
+        self.h = pa_create(n_q_heads, n_kv_heads, n_pool_pages, max_pages_per_seq, **opts)
+        self.n_q_heads, self.n_kv_heads = n_q_heads, n_kv_heads
+
+    def close(self):
+        if self.h is not None:
+            pa_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,604 @@
+// C-ABI host side: handle, argument checks, the window-aware work planner
+// (longest-first unit order), workspace, tensor maps and launches.
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+#include "pa_ptx.cuh"
+
+using namespace pa;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+struct Plan {
+  std::vector<SeqGeom> seqs;
+  std::vector<Unit> units;
+  int n_stored_blocks = 0;
+  int n_tok_total = 0;
+  int total_q = 0;
+  long long n_tiles = 0;
+};
+
+// Host planner: per-sequence widened geometry and the work units sorted by
+// decreasing cost (tiles), so the longest units start first.
+int build_plan(int HQ, int HKV, int n_seq, const pa_seq* seqs, int S, int W, int max_pages, Plan& P) {
+  if (HQ <= 0 || HKV <= 0 || HQ % HKV != 0) return PA_EINVAL;
+  const int G = HQ / HKV;
+  if (G > kRows || kRows % G != 0) return PA_EINVAL;
+  if (n_seq <= 0 || seqs == nullptr || S < 0) return PA_EINVAL;
+  const int TQ = kRows / G;
+  P = Plan();
+  int tok_off = 0;
+  for (int s = 0; s < n_seq; ++s) {
+    const pa_seq& q = seqs[s];
+    if (q.n_q < 1 || q.q_start < 0 || q.q_off < 0 || q.n_ctx < q.q_start + q.n_q) return PA_EINVAL;
+    if (max_pages > 0 && (long long)q.n_ctx > (long long)max_pages * kPage) return PA_EINVAL;
+    if ((long long)q.q_off + q.n_q > (1LL << 30) || (long long)q.n_ctx > (1LL << 30)) return PA_EINVAL;
+    SeqGeom g{};
+    g.q_off = q.q_off;
+    g.q_start = q.q_start;
+    g.n_q = q.n_q;
+    g.n_ctx = q.n_ctx;
+    g.tok_off = tok_off;
+    g.bt_row = s;
+    seq_geom_fill(g, S, W);
+    tok_off += g.n_blocks * kPage;
+    if (tok_off > (1 << 30)) return PA_EINVAL;
+    P.seqs.push_back(g);
+    P.total_q = std::max(P.total_q, q.q_off + q.n_q);
+    const int t_first = (q.q_start / TQ) * TQ;
+    for (int t0 = t_first; t0 < q.q_start + q.n_q; t0 += TQ) {
+      const UnitGeom ug = unit_geom(t0, TQ, g, S, W);
+      for (int kv = 0; kv < HKV; ++kv) {
+        P.units.push_back(Unit{s, kv, t0, ug.n_tiles});
+        P.n_tiles += ug.n_tiles;
+      }
+    }
+  }
+  std::stable_sort(P.units.begin(), P.units.end(), [](const Unit& a, const Unit& b) { return a.n_tiles > b.n_tiles; });
+  P.n_stored_blocks = tok_off / kPage;
+  P.n_tok_total = tok_off;
+  return PA_OK;
+}
+
+bool same_plan_key(const std::vector<int>& a, const std::vector<int>& b) { return a == b; }
+
+}  // namespace
+
+struct pa_ctx {
+  int HQ = 0, HKV = 0, G = 0, TQ = 0, n_pool = 0, max_pages = 0;
+  pa_options opt{};
+  int device = 0, n_sm = 0;
+
+  // workspace
+  __half* kw = nullptr;
+  __half* vt = nullptr;
+  float* ks = nullptr;
+  float* vs = nullptr;
+  int n_tok_cap = 0;
+  unsigned int* vsmax = nullptr;
+  int vsmax_cap = 0;
+  SeqGeom* d_seqs = nullptr;
+  int seqs_cap = 0;
+  Unit* d_units = nullptr;
+  int units_cap = 0;
+  int* d_err = nullptr;
+  int* d_counter = nullptr;
+
+  // plan upload through pinned staging
+  void* h_stage = nullptr;
+  size_t h_stage_cap = 0;
+  cudaEvent_t upload_done = nullptr;
+  bool upload_recorded = false;
+  std::vector<int> plan_key;
+  Plan plan;
+
+  // tensor maps
+  AttnMaps maps{};
+  const void* q_ptr = nullptr;
+  int q_rows = -1;
+  const void* kv_ptr = nullptr;
+  int kv_rows = -1;
+  int kv_cap = -1;
+
+  // host-buffer path staging
+  void* hb[7] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  size_t hb_cap[7] = {0, 0, 0, 0, 0, 0, 0};
+
+  // timing
+  std::vector<cudaEvent_t> ev_free;
+  std::vector<cudaEvent_t> ev_pending;  // triples (before widen, after widen, after attention)
+  double t_widen = 0.0, t_attn = 0.0;
+  int t_calls = 0;
+};
+
+namespace {
+
+int cuda_fail(cudaError_t e) {
+  if (e == cudaErrorMemoryAllocation) return PA_ENOMEM;
+  return PA_ECUDA;
+}
+
+#define PA_CUDA(x)                              \
+  do {                                          \
+    cudaError_t e_ = (x);                       \
+    if (e_ != cudaSuccess) return cuda_fail(e_); \
+  } while (0)
+
+template <typename T>
+int grow(T*& p, int& cap, size_t need) {
+  if ((size_t)cap >= need) return PA_OK;
+  size_t n = std::max(need, (size_t)cap + (size_t)cap / 2);
+  if (p) PA_CUDA(cudaFree(p));
+  p = nullptr;
+  cap = 0;
+  PA_CUDA(cudaMalloc(reinterpret_cast<void**>(&p), n * sizeof(T)));
+  cap = (int)n;
+  return PA_OK;
+}
+
+int grow_bytes(void*& p, size_t& cap, size_t need) {
+  if (cap >= need) return PA_OK;
+  size_t n = std::max(need, cap + cap / 2);
+  if (p) PA_CUDA(cudaFree(p));
+  p = nullptr;
+  cap = 0;
+  PA_CUDA(cudaMalloc(&p, n));
+  cap = n;
+  return PA_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+           const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return PA_ECUDA;
+  cuuint64_t d[5], s[4];
+  cuuint32_t b[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
+  CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void*>(base), d, s, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ECUDA;
+}
+
+// Plan (cached by its inputs), workspace sizing and the upload of the plan.
+int prepare(pa_handle h, int n_seq, const pa_seq* seqs, int S, int W, cudaStream_t st) {
+  std::vector<int> key;
+  key.reserve(4 + 4 * n_seq);
+  key.push_back(n_seq);
+  key.push_back(S);
+  key.push_back(W);
+  for (int s = 0; s < n_seq; ++s) {
+    key.push_back(seqs[s].q_off);
+    key.push_back(seqs[s].q_start);
+    key.push_back(seqs[s].n_q);
+    key.push_back(seqs[s].n_ctx);
+  }
+  if (!h->plan_key.empty() && same_plan_key(key, h->plan_key)) return PA_OK;
+  Plan P;
+  int rc = build_plan(h->HQ, h->HKV, n_seq, seqs, S, W, h->max_pages, P);
+  if (rc) return rc;
+  // workspace
+  const size_t need_tok = ((size_t)P.n_tok_total + 63) / 64 * 64;
+  if ((size_t)h->n_tok_cap < need_tok) {
+    size_t cap = std::max(need_tok, (size_t)h->n_tok_cap + (size_t)h->n_tok_cap / 2);
+    cap = (cap + 63) / 64 * 64;
+    if (h->kw) cudaFree(h->kw);
+    if (h->vt) cudaFree(h->vt);
+    if (h->ks) cudaFree(h->ks);
+    if (h->vs) cudaFree(h->vs);
+    h->kw = nullptr;
+    h->vt = nullptr;
+    h->ks = nullptr;
+    h->vs = nullptr;
+    h->n_tok_cap = 0;
+    h->kv_ptr = nullptr;
+    PA_CUDA(cudaMalloc(&h->kw, cap * h->HKV * kHeadDim * sizeof(__half)));
+    PA_CUDA(cudaMalloc(&h->vt, cap * h->HKV * kHeadDim * sizeof(__half)));
+    PA_CUDA(cudaMalloc(&h->ks, cap * h->HKV * sizeof(float)));
+    PA_CUDA(cudaMalloc(&h->vs, cap * h->HKV * sizeof(float)));
+    h->n_tok_cap = (int)cap;
+  }
+  if ((rc = grow(h->vsmax, h->vsmax_cap, (size_t)n_seq * h->HKV))) return rc;
+  if ((rc = grow(h->d_seqs, h->seqs_cap, P.seqs.size()))) return rc;
+  if ((rc = grow(h->d_units, h->units_cap, P.units.size()))) return rc;
+  // upload through pinned staging; never overwrite staging a copy may still read
+  const size_t bytes_s = P.seqs.size() * sizeof(SeqGeom), bytes_u = P.units.size() * sizeof(Unit);
+  if (h->upload_recorded) PA_CUDA(cudaEventSynchronize(h->upload_done));
+  if (h->h_stage_cap < bytes_s + bytes_u) {
+    if (h->h_stage) cudaFreeHost(h->h_stage);
+    h->h_stage = nullptr;
+    h->h_stage_cap = 0;
+    PA_CUDA(cudaMallocHost(&h->h_stage, bytes_s + bytes_u));
+    h->h_stage_cap = bytes_s + bytes_u;
+  }
+  std::memcpy(h->h_stage, P.seqs.data(), bytes_s);
+  std::memcpy(static_cast<char*>(h->h_stage) + bytes_s, P.units.data(), bytes_u);
+  PA_CUDA(cudaMemcpyAsync(h->d_seqs, h->h_stage, bytes_s, cudaMemcpyHostToDevice, st));
+  PA_CUDA(cudaMemcpyAsync(h->d_units, static_cast<char*>(h->h_stage) + bytes_s, bytes_u, cudaMemcpyHostToDevice, st));
+  PA_CUDA(cudaEventRecord(h->upload_done, st));
+  h->upload_recorded = true;
+  h->plan = std::move(P);
+  h->plan_key = std::move(key);
+  return PA_OK;
+}
+
+int check_inputs(pa_handle h, const void* q, const int8_t* kp, const int8_t* vp, const float* ksc, const float* vsc,
+                 const int32_t* bt, const void* out) {
+  if (!h) return PA_EINVAL;
+  if (!q || !kp || !vp || !ksc || !vsc || !bt || !out) return PA_EINVAL;
+  if (!aligned(q, 16) || !aligned(kp, 16) || !aligned(vp, 16) || !aligned(out, 16)) return PA_EINVAL;
+  if (!aligned(ksc, 4) || !aligned(vsc, 4) || !aligned(bt, 4)) return PA_EINVAL;
+  return PA_OK;
+}
+
+WidenParams widen_params(pa_handle h, const int8_t* kp, const int8_t* vp, const float* ksc, const float* vsc,
+                         const int32_t* bt, int n_seq) {
+  WidenParams w{};
+  w.k_pool = kp;
+  w.v_pool = vp;
+  w.k_scale = ksc;
+  w.v_scale = vsc;
+  w.block_table = bt;
+  w.bt_stride = h->max_pages;
+  w.n_pool = h->n_pool;
+  w.HKV = h->HKV;
+  w.seqs = h->d_seqs;
+  w.n_seq = n_seq;
+  w.n_stored_blocks = h->plan.n_stored_blocks;
+  w.n_tok_cap = h->n_tok_cap;
+  w.kw = h->kw;
+  w.vt = h->vt;
+  w.ks = h->ks;
+  w.vs = h->vs;
+  w.vsmax = h->vsmax;
+  w.err = h->d_err;
+  return w;
+}
+
+cudaEvent_t take_event(pa_handle h) {
+  if (!h->ev_free.empty()) {
+    cudaEvent_t e = h->ev_free.back();
+    h->ev_free.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+int run(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* kp, const int8_t* vp,
+        const float* ksc, const float* vsc, const int32_t* bt, int S, int W, float sm_scale, void* out,
+        cudaStream_t st) {
+  int rc = check_inputs(h, q, kp, vp, ksc, vsc, bt, out);
+  if (rc) return rc;
+  if (!(sm_scale == sm_scale) || sm_scale < 0.f) return PA_EINVAL;
+  if ((rc = prepare(h, n_seq, seqs, S, W, st))) return rc;
+  const Plan& P = h->plan;
+  // tensor maps
+  if (q != h->q_ptr || P.total_q != h->q_rows) {
+    const uint64_t dims[3] = {(uint64_t)kHeadDim, (uint64_t)h->HQ, (uint64_t)P.total_q};
+    const uint64_t strides[2] = {(uint64_t)kHeadDim * 2, (uint64_t)h->HQ * kHeadDim * 2};
+    const uint32_t box[3] = {64, (uint32_t)h->G, (uint32_t)h->TQ};
+    if ((rc = encode(&h->maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B)))
+      return rc;
+    h->q_ptr = q;
+    h->q_rows = P.total_q;
+  }
+  if (h->kw != h->kv_ptr || P.n_tok_total != h->kv_rows || h->n_tok_cap != h->kv_cap) {
+    const uint64_t kd[3] = {(uint64_t)kHeadDim, (uint64_t)P.n_tok_total, (uint64_t)h->HKV};
+    const uint64_t kst[2] = {(uint64_t)kHeadDim * 2, (uint64_t)h->n_tok_cap * kHeadDim * 2};
+    const uint32_t kbox[3] = {64, (uint32_t)kTileKeys, 1};
+    if ((rc = encode(&h->maps.k, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, h->kw, kd, kst, kbox,
+                     CU_TENSOR_MAP_SWIZZLE_128B)))
+      return rc;
+    const uint64_t vd[3] = {(uint64_t)P.n_tok_total, (uint64_t)kHeadDim, (uint64_t)h->HKV};
+    const uint64_t vst[2] = {(uint64_t)h->n_tok_cap * 2, (uint64_t)h->n_tok_cap * kHeadDim * 2};
+    const uint32_t vbox[3] = {(uint32_t)kTileKeys, (uint32_t)kHeadDim, 1};
+    if ((rc = encode(&h->maps.v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, h->vt, vd, vst, vbox,
+                     CU_TENSOR_MAP_SWIZZLE_128B)))
+      return rc;
+    h->kv_ptr = h->kw;
+    h->kv_rows = P.n_tok_total;
+    h->kv_cap = h->n_tok_cap;
+  }
+  cudaEvent_t e0 = nullptr, e1 = nullptr, e2 = nullptr;
+  if (h->opt.record_timing) {
+    e0 = take_event(h);
+    e1 = take_event(h);
+    e2 = take_event(h);
+    if (!e0 || !e1 || !e2) return PA_ECUDA;
+    PA_CUDA(cudaEventRecord(e0, st));
+  }
+  PA_CUDA(cudaMemsetAsync(h->vsmax, 0, sizeof(unsigned int) * n_seq * h->HKV, st));
+  PA_CUDA(launch_widen(widen_params(h, kp, vp, ksc, vsc, bt, n_seq), st));
+  if (e1) PA_CUDA(cudaEventRecord(e1, st));
+  AttnParams a{};
+  a.seqs = h->d_seqs;
+  a.units = h->d_units;
+  a.n_units = (int)P.units.size();
+  a.ks = h->ks;
+  a.vs = h->vs;
+  a.vsmax = h->vsmax;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.HQ = h->HQ;
+  a.HKV = h->HKV;
+  a.G = h->G;
+  a.TQ = h->TQ;
+  a.n_tok_cap = h->n_tok_cap;
+  a.S = S;
+  a.W = W;
+  a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  a.q_mode = h->opt.q_mode;
+  a.p_mode = h->opt.p_mode;
+  a.err = h->d_err;
+  a.wait_ns = (unsigned long long)h->opt.wait_timeout_ms * 1000000ull;
+  a.unit_counter = h->d_counter;
+  PA_CUDA(launch_attention(a, h->maps, h->n_sm, st));
+  if (e2) {
+    PA_CUDA(cudaEventRecord(e2, st));
+    h->ev_pending.push_back(e0);
+    h->ev_pending.push_back(e1);
+    h->ev_pending.push_back(e2);
+  }
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void pa_default_options(pa_options* opt) {
+  if (!opt) return;
+  opt->q_mode = PA_Q_F16;
+  opt->p_mode = PA_P_F16;
+  opt->wait_timeout_ms = 2000;
+  opt->record_timing = 0;
+}
+
+const char* pa_strerror(int code) {
+  switch (code) {
+    case PA_OK: return "ok";
+    case PA_EINVAL: return "invalid argument";
+    case PA_EARCH: return "device is not an sm_103 GPU";
+    case PA_ECUDA: return "CUDA call failed";
+    case PA_ETIMEOUT: return "device-side wait timed out";
+    case PA_EBADPAGE: return "block-table entry outside the pool";
+    case PA_ENOMEM: return "out of device memory";
+    default: return "unknown error";
+  }
+}
+
+int pa_create(pa_handle* out, int n_q_heads, int n_kv_heads, int head_dim, int page_size, int n_pool_pages,
+              int max_pages_per_seq, const pa_options* opt) {
+  if (!out) return PA_EINVAL;
+  *out = nullptr;
+  if (head_dim != kHeadDim || page_size != kPage) return PA_EINVAL;
+  if (n_q_heads <= 0 || n_kv_heads <= 0 || n_kv_heads > 8 || n_q_heads % n_kv_heads) return PA_EINVAL;
+  const int G = n_q_heads / n_kv_heads;
+  if (G > kRows || kRows % G) return PA_EINVAL;
+  if (n_pool_pages <= 0 || max_pages_per_seq <= 0) return PA_EINVAL;
+  pa_options o;
+  pa_default_options(&o);
+  if (opt) o = *opt;
+  if ((o.q_mode != PA_Q_F16 && o.q_mode != PA_Q_INT8) || (o.p_mode != PA_P_F16 && o.p_mode != PA_P_U8) ||
+      o.wait_timeout_ms <= 0)
+    return PA_EINVAL;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ECUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return PA_ECUDA;
+  if (prop.major != 10 || prop.minor != 3) return PA_EARCH;
+  if (!encode_fn()) return PA_ECUDA;
+  pa_ctx* h = new pa_ctx();
+  h->HQ = n_q_heads;
+  h->HKV = n_kv_heads;
+  h->G = G;
+  h->TQ = kRows / G;
+  h->n_pool = n_pool_pages;
+  h->max_pages = max_pages_per_seq;
+  h->opt = o;
+  h->device = dev;
+  h->n_sm = prop.multiProcessorCount;
+  if (cudaMalloc(&h->d_err, sizeof(int)) != cudaSuccess || cudaMalloc(&h->d_counter, sizeof(int)) != cudaSuccess ||
+      cudaMemset(h->d_err, 0, sizeof(int)) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->upload_done, cudaEventDisableTiming) != cudaSuccess) {
+    pa_destroy(h);
+    return PA_ECUDA;
+  }
+  *out = h;
+  return PA_OK;
+}
+
+void pa_destroy(pa_handle h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  void* ptrs[] = {h->kw, h->vt, h->ks, h->vs, h->vsmax, h->d_seqs, h->d_units, h->d_err, h->d_counter};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+  for (int i = 0; i < 7; ++i)
+    if (h->hb[i]) cudaFree(h->hb[i]);
+  if (h->h_stage) cudaFreeHost(h->h_stage);
+  if (h->upload_done) cudaEventDestroy(h->upload_done);
+  for (cudaEvent_t e : h->ev_free) cudaEventDestroy(e);
+  for (cudaEvent_t e : h->ev_pending) cudaEventDestroy(e);
+  delete h;
+}
+
+int pa_prefill(pa_handle h, const void* q, const int8_t* k_pool, const int8_t* v_pool, const float* k_scale,
+               const float* v_scale, const int32_t* block_table, int q_start, int n_q, int n_ctx, int n_sink_blk,
+               int n_win_blk, float sm_scale, void* out, void* stream) {
+  pa_seq s{0, q_start, n_q, n_ctx};
+  return run(h, 1, &s, q, k_pool, v_pool, k_scale, v_scale, block_table, n_sink_blk, n_win_blk, sm_scale, out,
+             static_cast<cudaStream_t>(stream));
+}
+
+int pa_prefill_batch(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* k_pool,
+                     const int8_t* v_pool, const float* k_scale, const float* v_scale, const int32_t* block_table,
+                     int n_sink_blk, int n_win_blk, float sm_scale, void* out, void* stream) {
+  return run(h, n_seq, seqs, q, k_pool, v_pool, k_scale, v_scale, block_table, n_sink_blk, n_win_blk, sm_scale, out,
+             static_cast<cudaStream_t>(stream));
+}
+
+int pa_prefill_host(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* k_pool,
+                    const int8_t* v_pool, const float* k_scale, const float* v_scale, const int32_t* block_table,
+                    int n_sink_blk, int n_win_blk, float sm_scale, void* out, void* stream) {
+  if (!h || n_seq <= 0 || !seqs) return PA_EINVAL;
+  int total_q = 0;
+  for (int s = 0; s < n_seq; ++s) total_q = std::max(total_q, seqs[s].q_off + seqs[s].n_q);
+  const size_t bytes[7] = {
+      (size_t)total_q * h->HQ * kHeadDim * 2,                  // q
+      (size_t)h->n_pool * kPage * h->HKV * kHeadDim,          // k_pool
+      (size_t)h->n_pool * kPage * h->HKV * kHeadDim,          // v_pool
+      (size_t)h->n_pool * kPage * h->HKV * sizeof(float),     // k_scale
+      (size_t)h->n_pool * kPage * h->HKV * sizeof(float),     // v_scale
+      (size_t)n_seq * h->max_pages * sizeof(int32_t),         // block table
+      (size_t)total_q * h->HQ * kHeadDim * 2};                // out
+  const void* src[6] = {q, k_pool, v_pool, k_scale, v_scale, block_table};
+  for (int i = 0; i < 6; ++i)
+    if (!src[i]) return PA_EINVAL;
+  if (!out) return PA_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (int i = 0; i < 7; ++i) {
+    int rc = grow_bytes(h->hb[i], h->hb_cap[i], bytes[i]);
+    if (rc) return rc;
+  }
+  for (int i = 0; i < 6; ++i) PA_CUDA(cudaMemcpyAsync(h->hb[i], src[i], bytes[i], cudaMemcpyHostToDevice, st));
+  int rc = run(h, n_seq, seqs, h->hb[0], static_cast<const int8_t*>(h->hb[1]), static_cast<const int8_t*>(h->hb[2]),
+               static_cast<const float*>(h->hb[3]), static_cast<const float*>(h->hb[4]),
+               static_cast<const int32_t*>(h->hb[5]), n_sink_blk, n_win_blk, sm_scale, h->hb[6], st);
+  if (rc) return rc;
+  PA_CUDA(cudaMemcpyAsync(out, h->hb[6], bytes[6], cudaMemcpyDeviceToHost, st));
+  return pa_last_error(h, stream);
+}
+
+int pa_last_error(pa_handle h, void* stream) {
+  if (!h) return PA_EINVAL;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ECUDA;
+  int e = 0;
+  if (cudaMemcpy(&e, h->d_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ECUDA;
+  if (e != 0 && cudaMemset(h->d_err, 0, sizeof(int)) != cudaSuccess) return PA_ECUDA;
+  if (e & DEV_ERR_TIMEOUT) return PA_ETIMEOUT;
+  if (e & DEV_ERR_BAD_PAGE) return PA_EBADPAGE;
+  if (e != 0) return PA_ECUDA;
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ECUDA;
+}
+
+int pa_timing(pa_handle h, int reset, double* widen_ms, double* attention_ms, int* n_calls) {
+  if (!h) return PA_EINVAL;
+  for (size_t i = 0; i + 2 < h->ev_pending.size(); i += 3) {
+    cudaEvent_t* e = &h->ev_pending[i];
+    if (cudaEventSynchronize(e[2]) != cudaSuccess) return PA_ECUDA;
+    float a = 0.f, b = 0.f;
+    cudaEventElapsedTime(&a, e[0], e[1]);
+    cudaEventElapsedTime(&b, e[1], e[2]);
+    h->t_widen += a;
+    h->t_attn += b;
+    h->t_calls += 1;
+    for (int k = 0; k < 3; ++k) h->ev_free.push_back(e[k]);
+  }
+  h->ev_pending.clear();
+  if (widen_ms) *widen_ms = h->t_widen;
+  if (attention_ms) *attention_ms = h->t_attn;
+  if (n_calls) *n_calls = h->t_calls;
+  if (reset) {
+    h->t_widen = h->t_attn = 0.0;
+    h->t_calls = 0;
+  }
+  return PA_OK;
+}
+
+int pa_plan(int n_q_heads, int n_kv_heads, int n_seq, const pa_seq* seqs, int n_sink_blk, int n_win_blk,
+            int32_t* units_out, int cap, int* n_units, long long* n_tiles, int* n_widened_rows) {
+  Plan P;
+  int rc = build_plan(n_q_heads, n_kv_heads, n_seq, seqs, n_sink_blk, n_win_blk, 0, P);
+  if (rc) return rc;
+  if (n_units) *n_units = (int)P.units.size();
+  if (n_tiles) *n_tiles = P.n_tiles;
+  if (n_widened_rows) *n_widened_rows = P.n_tok_total;
+  if (units_out) {
+    const int n = std::min(cap, (int)P.units.size());
+    for (int i = 0; i < n; ++i) {
+      units_out[4 * i + 0] = P.units[i].seq;
+      units_out[4 * i + 1] = P.units[i].g;
+      units_out[4 * i + 2] = P.units[i].t0;
+      units_out[4 * i + 3] = P.units[i].n_tiles;
+    }
+  }
+  return PA_OK;
+}
+
+int pa_debug_gather(pa_handle h, int n_seq, const pa_seq* seqs, const int8_t* k_pool, const int8_t* v_pool,
+                    const float* k_scale, const float* v_scale, const int32_t* block_table, int n_sink_blk,
+                    int n_win_blk, int seq, int8_t* k_out, int8_t* v_out, float* ks_out, float* vs_out,
+                    int32_t* tok_out, int cap, int* n_rows, void* stream) {
+  if (!h || !k_out || !v_out || !ks_out || !vs_out || !tok_out || !n_rows || seq < 0 || seq >= n_seq)
+    return PA_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int rc = prepare(h, n_seq, seqs, n_sink_blk, n_win_blk, st);
+  if (rc) return rc;
+  const int rows = h->plan.seqs[seq].n_blocks * kPage;
+  *n_rows = rows;
+  if (rows > cap) return PA_EINVAL;
+  PA_CUDA(cudaMemsetAsync(h->vsmax, 0, sizeof(unsigned int) * n_seq * h->HKV, st));
+  PA_CUDA(launch_widen(widen_params(h, k_pool, v_pool, k_scale, v_scale, block_table, n_seq), st));
+  PA_CUDA(launch_debug_gather(widen_params(h, k_pool, v_pool, k_scale, v_scale, block_table, n_seq), seq, k_out,
+                              v_out, ks_out, vs_out, tok_out, st));
+  return pa_last_error(h, stream);
+}
+
+int pa_debug_maskset(pa_handle h, int n_seq, const pa_seq* seqs, int n_sink_blk, int n_win_blk,
+                     int32_t* row_counts, int32_t* unit_blocks, int cap, int32_t* units_out, int units_cap,
+                     int* n_units, void* stream) {
+  if (!h || !row_counts || !unit_blocks || !units_out || !n_units || cap <= 0) return PA_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int rc = prepare(h, n_seq, seqs, n_sink_blk, n_win_blk, st);
+  if (rc) return rc;
+  const Plan& P = h->plan;
+  *n_units = (int)P.units.size();
+  if ((int)P.units.size() > units_cap) return PA_EINVAL;
+  for (size_t i = 0; i < P.units.size(); ++i) {
+    units_out[4 * i + 0] = P.units[i].seq;
+    units_out[4 * i + 1] = P.units[i].g;
+    units_out[4 * i + 2] = P.units[i].t0;
+    units_out[4 * i + 3] = P.units[i].n_tiles;
+  }
+  PA_CUDA(launch_debug_maskset(h->d_seqs, h->d_units, (int)P.units.size(), h->TQ, h->G, n_sink_blk, n_win_blk,
+                               row_counts, unit_blocks, cap, st));
+  return pa_last_error(h, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,79 @@
+// Declarations shared by the C-ABI host code (pa_api.cu) and the kernels
+// (pa_kernels.cu).  Not part of the public interface.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+
+#include "pa_tiles.cuh"
+
+namespace pa {
+
+// One work unit: 128 query rows of one kv head (see pa_tiles.cuh).
+struct Unit {
+  int seq;      // sequence index
+  int g;        // kv head
+  int t0;       // absolute first token of the unit (multiple of TQ)
+  int n_tiles;  // key tiles it visits (its cost)
+};
+
+// Inputs of the widening (gather) pass: the paged int8 pool read through the
+// block table into contiguous per-kv-head buffers in logical key order.
+struct WidenParams {
+  const int8_t* k_pool;       // [n_pool][16][HKV][256]
+  const int8_t* v_pool;
+  const float* k_scale;       // [n_pool][16][HKV]
+  const float* v_scale;
+  const int32_t* block_table; // [n_seq][bt_stride]
+  int bt_stride;
+  int n_pool;
+  int HKV;
+  const SeqGeom* seqs;        // device
+  int n_seq;
+  int n_stored_blocks;        // sum over sequences of SeqGeom::n_blocks
+  int n_tok_cap;              // row stride of the widened buffers
+  __half* kw;                 // [HKV][n_tok_cap][256]   integer-valued fp16 K codes
+  __half* vt;                 // [HKV][256][n_tok_cap]   integer-valued fp16 V codes, transposed
+  float* ks;                  // [HKV][n_tok_cap]        per-token K scale
+  float* vs;                  // [HKV][n_tok_cap]        per-token V scale
+  unsigned int* vsmax;        // [n_seq][HKV] float bits: max V scale (atomicMax)
+  int* err;
+};
+
+struct AttnParams {
+  const SeqGeom* seqs;
+  const Unit* units;
+  int n_units;
+  const float* ks;
+  const float* vs;
+  const unsigned int* vsmax;
+  __nv_bfloat16* out;         // [total_q][HQ][256]
+  int HQ, HKV, G, TQ;
+  int n_tok_cap;
+  int S, W;
+  float sm_scale_log2;        // sm_scale * log2(e)
+  int q_mode, p_mode;
+  int* err;
+  unsigned long long wait_ns;
+  int* unit_counter;          // persistent-grid work counter (zeroed per launch)
+};
+
+struct AttnMaps {
+  CUtensorMap q;   // Q   [total_q][HQ][256] bf16, box {64, G, TQ}
+  CUtensorMap k;   // Kw  [HKV][n_tok][256] fp16, box {64, 64, 1}
+  CUtensorMap v;   // Vt  [HKV][256][n_tok] fp16, box {64, 256, 1}
+};
+
+// Launchers (return the launch's cudaError_t).
+cudaError_t launch_widen(const WidenParams& p, cudaStream_t st);
+cudaError_t launch_attention(const AttnParams& p, const AttnMaps& m, int n_sm, cudaStream_t st);
+
+// Debug exports (tests only).
+cudaError_t launch_debug_gather(const WidenParams& p, int seq, int8_t* k_out, int8_t* v_out, float* ks_out,
+                                float* vs_out, int32_t* tok_out, cudaStream_t st);
+cudaError_t launch_debug_maskset(const SeqGeom* seqs, const Unit* units, int n_units, int TQ, int G, int S, int W,
+                                 int32_t* row_counts, int32_t* unit_blocks, int cap, cudaStream_t st);
+
+}  // namespace pa

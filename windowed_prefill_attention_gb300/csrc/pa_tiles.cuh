@@ -1,0 +1,141 @@
+// Work-unit and key-tile geometry of the windowed prefill attention, shared
+// by the host planner and every kernel (one definition, so the planner's tile
+// counts, the producer's loads, the MMA issuer and the softmax agree).
+//
+// Mask ("int8 tensor-core prefill attention", section "Why the attention, and
+// why tensor cores"; "Relation to open PRs" for the window-off case): query
+// token t sees key j iff j <= t and, when the window is on (W > 0), j's 16-token
+// block is a sink block (< S) or lies in the last W blocks up to t's own block,
+// i.e. block(j) >= max(0, block(t) + 1 - W).  The window start is a function of
+// block(t) only, so it is constant over a 16-row query tile and only the
+// causal bound varies per row.
+//
+// A work unit is 128 query rows of one kv head g: TQ = 128 / G consecutive
+// tokens times the G q heads that share g (row r = token_in_unit * G + head_in_group).
+// Units start on absolute multiples of TQ, so for G = 8 a unit is exactly one
+// 16-token query block, the pages' 16-row tile.
+//
+// Key tiles: the unit's visible key blocks form at most two runs, the sink run
+// [0, S) and the window run [lo(first block), last block]; when they touch they
+// merge into one run from block 0.  Each run is cut into tiles of up to
+// kTileBlocks 16-key blocks (64 keys).  Masked blocks are never visited.
+#pragma once
+
+#ifdef __CUDACC__
+#define PA_HD __host__ __device__ __forceinline__
+#else
+#define PA_HD inline
+#endif
+
+namespace pa {
+
+constexpr int kPage = 16;         // tokens per KV page (= mask block)
+constexpr int kHeadDim = 256;     // head dimension
+constexpr int kRows = 128;        // query rows per work unit (MMA M)
+constexpr int kTileBlocks = 4;    // 16-key blocks per key tile
+constexpr int kTileKeys = kTileBlocks * kPage;  // 64
+
+PA_HD int imin(int a, int b) { return a < b ? a : b; }
+PA_HD int imax(int a, int b) { return a > b ? a : b; }
+
+// Per-sequence description, host-computed, read by the kernels.
+struct SeqGeom {
+  int q_off;       // first row of the sequence in q / out
+  int q_start;     // absolute position of that row
+  int n_q;         // query tokens
+  int n_ctx;       // context tokens (q_start + n_q)
+  int tok_off;     // first row of the sequence in the widened K/V buffers
+  int vis_lo;      // first window block any query of the call can see (0 if W <= 0)
+  int n_sink_vis;  // sink blocks stored ahead of vis_lo: min(S, vis_lo) (0 if W <= 0)
+  int n_blocks;    // blocks stored in the widened buffers for this sequence
+  int bt_row;      // row of this sequence in the block table
+  int pad[3];
+};
+
+// Widened-buffer geometry of one sequence.  Blocks below vis_lo that are not
+// sink blocks can never be seen by any query of this call and are not stored.
+PA_HD void seq_geom_fill(SeqGeom& s, int S, int W) {
+  const int last_blk = (s.q_start + s.n_q - 1) / kPage;
+  if (W > 0) {
+    s.vis_lo = imax(0, s.q_start / kPage + 1 - W);
+    s.n_sink_vis = imin(S, s.vis_lo);
+  } else {
+    s.vis_lo = 0;
+    s.n_sink_vis = 0;
+  }
+  s.n_blocks = s.n_sink_vis + (last_blk - s.vis_lo + 1);
+}
+
+// Stored block index (within the sequence) -> logical key block.
+PA_HD int stored_to_logical_block(const SeqGeom& s, int b) {
+  return b < s.n_sink_vis ? b : s.vis_lo + (b - s.n_sink_vis);
+}
+// Logical key block -> first widened row (global, all sequences).
+PA_HD int logical_block_row(const SeqGeom& s, int kb) {
+  const int b = kb < s.vis_lo ? kb : s.n_sink_vis + (kb - s.vis_lo);
+  return s.tok_off + b * kPage;
+}
+
+// Geometry of one work unit.
+struct UnitGeom {
+  int ta, tb;          // first / last query token of the unit inside the sequence's query range
+  int qa, qb;          // their 16-token blocks
+  int lo_b;            // window start of the last block (0 if W <= 0)
+  int nsk;             // blocks of the separate sink run (0 if merged or no window)
+  int ws;              // first block of the window run
+  int n_sink_tiles;    // tiles of the sink run
+  int n_tiles;         // all tiles
+};
+
+PA_HD UnitGeom unit_geom(int t0, int TQ, const SeqGeom& s, int S, int W) {
+  UnitGeom u;
+  u.ta = imax(t0, s.q_start);
+  u.tb = imin(t0 + TQ, s.q_start + s.n_q) - 1;
+  u.qa = u.ta / kPage;
+  u.qb = u.tb / kPage;
+  int lo_a = 0;
+  u.lo_b = 0;
+  if (W > 0) {
+    lo_a = imax(0, u.qa + 1 - W);
+    u.lo_b = imax(0, u.qb + 1 - W);
+  }
+  const bool separate = W > 0 && lo_a > S;
+  u.nsk = separate ? S : 0;
+  u.ws = separate ? lo_a : 0;
+  u.n_sink_tiles = (u.nsk + kTileBlocks - 1) / kTileBlocks;
+  u.n_tiles = u.n_sink_tiles + (u.qb + 1 - u.ws + kTileBlocks - 1) / kTileBlocks;
+  return u;
+}
+
+struct TileGeom {
+  int kb0;         // first logical key block
+  int nb;          // blocks in the tile (1..kTileBlocks)
+  bool needs_mask; // some row of the unit does not see some key of the tile
+};
+
+PA_HD TileGeom tile_geom(const UnitGeom& u, int i, int S, int W) {
+  TileGeom g;
+  if (i < u.n_sink_tiles) {
+    g.kb0 = i * kTileBlocks;
+    g.nb = imin(kTileBlocks, u.nsk - g.kb0);
+  } else {
+    g.kb0 = u.ws + (i - u.n_sink_tiles) * kTileBlocks;
+    g.nb = imin(kTileBlocks, u.qb + 1 - g.kb0);
+  }
+  const int kb1 = g.kb0 + g.nb;  // exclusive
+  // causal: blocks at or after the unit's first query block are partly hidden
+  // from its earlier rows; window: non-sink blocks below the last block's
+  // window start are hidden from the later rows.
+  g.needs_mask = (kb1 - 1 >= u.qa) || (W > 0 && imax(g.kb0, S) < imin(kb1, u.lo_b));
+  return g;
+}
+
+// The per-key predicate, used inside tiles that need masking.
+PA_HD bool key_visible(int t, int j, int S, int W) {
+  if (j > t) return false;
+  if (W <= 0) return true;
+  const int bj = j / kPage;
+  return bj < S || bj >= imax(0, t / kPage + 1 - W);
+}
+
+}  // namespace pa
