@@ -1,0 +1,350 @@
+#!/usr/bin/env python
+"""Benchmark of the windowed prefill attention over a paged int8 KV pool.
+
+One step = one pass of the whole hot path (page-widening gather + attention
+kernel) over the 32k windowed workload: 1 sequence of 32768 tokens, 16 Q / 2
+KV heads, head_dim 256, 1 sink block + 256-block window, 1% outlier tokens,
+random page placement.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 32k]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(replicas; weak scaling) and the timed region is bracketed by a barrier; the
+slowest rank's time counts.  --impl reference times the fp64 CPU oracle on a
+bounded sample of the same workload on the host cores.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth import CONFIGS, make_inputs  # noqa: E402
+
+METRIC = "prefill-attn int8 TOPS & tokens/s at 32k, fraction of dense int8 roofline"
+UNIT = "TOPS"
+HEAD_DIM = 256
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def visible_pairs(q_start, n_q, S, W, page=16):
+    """Visible (query, key) pairs of one sequence, from the per-token count:
+    t+1 keys when the window is off or reaches the sink blocks, else the sink
+    blocks plus the window blocks up to t."""
+    t = np.arange(q_start, q_start + n_q, dtype=np.int64)
+    if W <= 0:
+        return int((t + 1).sum())
+    lo = np.maximum(0, t // page + 1 - W)
+    cnt = np.where(lo <= S, t + 1, page * S + t - page * lo + 1)
+    return int(cnt.sum())
+
+
+def algorithmic_ops(wl):
+    """4 * head_dim ops (QK^T and PV multiply-adds) per visible pair and q head."""
+    pairs = sum(visible_pairs(qs, nq, wl.n_sink_blk, wl.n_win_blk) for qs, nq in wl.seqs)
+    return 4 * HEAD_DIM * wl.n_q_heads * pairs
+
+
+def workload_config(wl, l2_note):
+    return {"workload": wl.name, "n_seq": len(wl.seqs), "q_start_n_q": [list(s) for s in wl.seqs],
+            "n_q_heads": wl.n_q_heads, "n_kv_heads": wl.n_kv_heads, "head_dim": HEAD_DIM, "page": 16,
+            "n_sink_blk": wl.n_sink_blk, "n_win_blk": wl.n_win_blk, "outlier_frac": wl.outlier_frac,
+            "sm_scale": wl.sm_scale, "kv": "int8 paged pool, per-token per-kv-head fp32 scales", "l2": l2_note}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured bf16 burst (MEASURED_PEAKS.json)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback bf16"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "windowed_prefill_attention_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(config_name):
+    """DRAM bytes per attention launch from the committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "attention_kernel_%s.md" % config_name)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    if not m_t or not m_h or m_h.group(1) != kernel_source_hash():
+        return None
+    return float(m_t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.dev)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def max_over_ranks(x, device=None):
+    """The largest value of x over all ranks (x itself without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tops(ops_per_step, steps, slowest_ms, world):
+    """Whole-job throughput: every rank ran `steps` steps of `ops_per_step`; the
+    slowest rank's device time counts."""
+    return world * ops_per_step * steps / (slowest_ms / 1e3) / 1e12
+
+
+def cpu_baseline(wl, inp, seconds=12.0):
+    """The fp64 oracle, as it stands, on uniformly sampled rows of the workload."""
+    import oracle
+    prob = oracle.Problem.from_inputs(inp)
+    rng = np.random.default_rng(1234)
+    n_rows, n_heads = inp.q.shape[0], inp.q.shape[1]
+    cores = len(os.sched_getaffinity(0))
+    done_rows, ops, t_total = 0, 0, 0.0
+    batch = 8 * cores
+    while t_total < seconds:
+        rows = np.stack([rng.integers(0, n_rows, batch), rng.integers(0, n_heads, batch)], 1).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.exact(prob, rows, n_threads=cores)
+        dt = time.perf_counter() - t0
+        t_total += dt
+        done_rows += batch
+        ops += sum(4 * HEAD_DIM * _row_count(inp, int(i), wl) for i in rows[:, 0])
+        if dt < 1.0:
+            batch *= 2
+    return {"value": ops / t_total / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%d (token, head) rows of the %s workload, uniform, fp64 oracle on %d threads, %.1f s"
+                      % (done_rows, wl.name, cores, t_total)}
+
+
+def _row_count(inp, i, wl):
+    for (q_off, q_start, n_q, _), _s in zip(inp.seq_desc.tolist(), wl.seqs):
+        if q_off <= i < q_off + n_q:
+            return visible_pairs(q_start + i - q_off, 1, wl.n_sink_blk, wl.n_win_blk)
+    raise ValueError(i)
+
+
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    inp = make_inputs(wl)
+    prob = oracle.Problem.from_inputs(inp)
+    cores = len(os.sched_getaffinity(0))
+    rng = np.random.default_rng(4321)
+    n_rows, n_heads = inp.q.shape[0], inp.q.shape[1]
+    # size one step so that warmup + steps fit in about two minutes
+    probe = np.stack([rng.integers(0, n_rows, 4 * cores), rng.integers(0, n_heads, 4 * cores)], 1).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.exact(prob, probe, n_threads=cores)
+    per_row = (time.perf_counter() - t0) / probe.shape[0]
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n_step = int(max(cores, min(64 * cores, budget / max(per_row, 1e-9))))
+    rows = np.stack([rng.integers(0, n_rows, n_step), rng.integers(0, n_heads, n_step)], 1).astype(np.int32)
+    ops_step = sum(4 * HEAD_DIM * _row_count(inp, int(i), wl) for i in rows[:, 0])
+    for _ in range(args.warmup):
+        oracle.exact(prob, rows, n_threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.exact(prob, rows, n_threads=cores)
+    dt = time.perf_counter() - t0
+    value = ops_step * args.steps / dt / 1e12
+    sample = "%d (token, head) rows of the %s workload per step, fp64 oracle on %d threads" % (n_step, wl.name, cores)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl, "n/a (CPU)"), "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    import windowed_prefill_attention_gb300 as pa
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    inp = make_inputs(wl)
+    dev = torch.device("cuda", local)
+    q = torch.from_numpy(inp.q.view(np.int16)).view(torch.bfloat16).to(dev)
+    kp, vp = torch.from_numpy(inp.k_pool).to(dev), torch.from_numpy(inp.v_pool).to(dev)
+    ks, vs = torch.from_numpy(inp.k_scale).to(dev), torch.from_numpy(inp.v_scale).to(dev)
+    bt = torch.from_numpy(inp.block_table).to(dev)
+    out = torch.empty_like(q)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    h = pa.pa_create(wl.n_q_heads, wl.n_kv_heads, inp.k_pool.shape[0], inp.block_table.shape[1], record_timing=True)
+    seqs, S, W, sm = inp.seq_desc, wl.n_sink_blk, wl.n_win_blk, wl.sm_scale
+
+    def step():
+        pa.pa_prefill_batch(h, seqs, q, kp, vp, ks, vs, bt, S, W, sm, out)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    rc = pa.pa_last_error(h)
+    if rc != 0:
+        raise RuntimeError("device error in warm-up: %s" % pa.pa_strerror(rc))
+    pa.pa_timing(h, reset=True)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.2)  # let the sampler's first reading land inside the region
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record()
+        step()
+        ends[i].record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    rc = pa.pa_last_error(h)
+    if rc != 0:
+        raise RuntimeError("device error in timed steps: %s" % pa.pa_strerror(rc))
+    total_ms = float(sum(s.elapsed_time(e) for s, e in zip(starts, ends)))
+    widen_ms, attn_ms, n_calls = pa.pa_timing(h, reset=True)
+    if world > 1:
+        total_ms = max_over_ranks(total_ms, dev)
+
+    ops = algorithmic_ops(wl)
+    tokens = wl.total_q
+    value = aggregate_tops(ops, args.steps, total_ms, world)
+    attn_avg_ms = attn_ms / max(1, n_calls)
+    peak, peak_src = measured_peaks()
+    achieved = ops / (attn_avg_ms / 1e3) / 1e12
+
+    # end to end through the host-buffer C-ABI call: pinned inputs in, result out
+    pin = lambda a: torch.from_numpy(a).pin_memory()  # noqa: E731
+    hq = torch.from_numpy(inp.q.view(np.int16)).pin_memory()
+    hk, hv, hks, hvs, hbt = (pin(inp.k_pool), pin(inp.v_pool), pin(inp.k_scale), pin(inp.v_scale),
+                             pin(inp.block_table))
+    hout = torch.empty_like(hq).pin_memory()
+    h2d = sum(a.numel() * a.element_size() for a in (hq, hk, hv, hks, hvs, hbt))
+    d2h = hout.numel() * hout.element_size()
+    e2e_steps = max(3, min(args.steps, 10))
+    pa.pa_prefill_host(h, seqs, hq, hk, hv, hks, hvs, hbt, S, W, sm, hout)  # warm the staging buffers
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        pa.pa_prefill_host(h, seqs, hq, hk, hv, hks, hvs, hbt, S, W, sm, hout)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_value = world * ops / e2e_s / 1e12
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic",
+        "config": workload_config(wl, "flushed between timed steps (256 MiB write, untimed)"),
+        "tokens_per_s": world * tokens * args.steps / (total_ms / 1e3),
+        "algorithmic_ops_per_step": ops,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_s * 1e3, "call": "pa_prefill_host (pinned host buffers)"},
+        "roofline": {"bound": "tensor", "kernel": "attention_kernel", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_src,
+                     "traffic": profiled_traffic(wl.name), "launch_ms": attn_avg_ms,
+                     "widen_launch_ms": widen_ms / max(1, n_calls)},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, inp)
+    pa.pa_destroy(h)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="32k", choices=sorted(CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    wl = CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

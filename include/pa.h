@@ -70,6 +70,9 @@ typedef struct {
   int p_mode;           /* PA_P_F16 | PA_P_U8 */
   int wait_timeout_ms;  /* bound on every device-side wait (default 2000) */
   int record_timing;    /* nonzero: time each launch with CUDA events (pa_timing) */
+  int debug_stall;      /* test hook: nonzero makes the attention kernel's first wait target a
+                           barrier nothing arrives at, so the bounded wait runs out, the kernel
+                           exits cleanly and pa_last_error reports PA_ETIMEOUT; 0 in normal use */
 } pa_options;
 
 typedef struct {
@@ -79,7 +82,7 @@ typedef struct {
   int n_ctx;    /* context tokens in the pool; q_start + n_q <= n_ctx */
 } pa_seq;
 
-/* Fill *opt with the defaults (fp16 containers, 2000 ms waits, no timing). */
+/* Fill *opt with the defaults (fp16 containers, 2000 ms waits, no timing, no test hook). */
 void pa_default_options(pa_options* opt);
 
 /* Create a handle bound to the current CUDA device.  head_dim must be 256 and

@@ -1,0 +1,184 @@
+"""Host-side checks of the C-ABI library (no GPU): it loads, exports every
+symbol include/pa.h declares, validates arguments, and its work planner
+covers every query row once with the tiles the mask implies."""
+import ctypes as C
+import os
+import re
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import oracle
+from synth import CONFIGS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+LIB = os.path.join(ROOT, "windowed_prefill_attention_gb300", "libpa.so")
+
+
+@pytest.fixture(scope="module")
+def pa():
+    subprocess.run([sys.executable, os.path.join(ROOT, "windowed_prefill_attention_gb300", "build.py")], check=True,
+                   capture_output=True)
+    import windowed_prefill_attention_gb300 as mod
+    return mod
+
+
+def header_symbols():
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(pa):
+    lib = C.CDLL(LIB)
+    names = header_symbols()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(pa.EXPORTED) == set(names)
+
+
+def test_strerror_and_defaults(pa):
+    assert pa.pa_strerror(0) == "ok"
+    assert "timed out" in pa.pa_strerror(pa.PA_ETIMEOUT)
+    o = pa.pa_default_options()
+    assert (o.q_mode, o.p_mode, o.wait_timeout_ms, o.record_timing, o.debug_stall) == (0, 0, 2000, 0, 0)
+
+
+def test_null_handle_and_bad_arguments_are_rejected(pa):
+    lib = pa._lib
+    null = C.c_void_p()
+    assert lib.pa_prefill(null, *([None] * 6), 0, 16, 16, 1, 4, C.c_float(0.1), None, None) == pa.PA_EINVAL
+    assert lib.pa_last_error(null, None) == pa.PA_EINVAL
+    h = C.c_void_p()
+    # head_dim other than 256, page size other than 16, GQA ratio not dividing 128
+    assert lib.pa_create(C.byref(h), 16, 2, 128, 16, 10, 10, None) == pa.PA_EINVAL
+    assert lib.pa_create(C.byref(h), 16, 2, 256, 32, 10, 10, None) == pa.PA_EINVAL
+    assert lib.pa_create(C.byref(h), 12, 4, 256, 16, 10, 10, None) == pa.PA_EINVAL
+
+
+@pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="checks the no-GPU path")
+def test_create_without_gpu_fails_cleanly(pa):
+    h = C.c_void_p()
+    rc = pa._lib.pa_create(C.byref(h), 16, 2, 256, 16, 10, 10, None)
+    assert rc in (pa.PA_ECUDA, pa.PA_EARCH)
+    assert not h.value
+
+
+def test_plan_rejects_empty_and_inconsistent_sequences(pa):
+    with pytest.raises(pa.PAError):
+        pa.pa_plan(16, 2, [(0, 0, 0, 16)], 1, 256)          # n_q = 0
+    with pytest.raises(pa.PAError):
+        pa.pa_plan(16, 2, [(0, 10, 20, 25)], 1, 256)        # q_start + n_q > n_ctx
+    with pytest.raises(pa.PAError):
+        pa.pa_plan(16, 2, [(0, -1, 20, 25)], 1, 256)        # negative start
+
+
+def expected_tiles(block_set):
+    """Tiles of a set of key blocks: maximal runs of consecutive blocks, each cut
+    into pieces of at most 4 blocks."""
+    blocks = sorted(block_set)
+    n, i = 0, 0
+    while i < len(blocks):
+        j = i
+        while j + 1 < len(blocks) and blocks[j + 1] == blocks[j] + 1:
+            j += 1
+        n += (j - i + 1 + 3) // 4
+        i = j + 1
+    return n
+
+
+PLAN_CASES = [
+    ("tiny", CONFIGS["tiny"].n_q_heads, CONFIGS["tiny"].n_kv_heads, [(0, 0, 256, 256)], 0, 16),
+    ("4k", 16, 2, [(0, 0, 4096, 4096)], 1, 256),
+    ("chunked_ragged", 16, 2, [(0, 1024, 2048, 3072), (2048, 6144, 2048, 8192), (4096, 30720, 2048, 32768),
+                               (6144, 12005, 2048, 14053)], 1, 256),
+    ("g4_window", 4, 1, [(0, 37, 300, 337)], 2, 3),
+    ("g1_causal", 2, 2, [(0, 5, 100, 105)], 1, 0),
+    ("g16", 32, 2, [(0, 0, 200, 200)], 1, 4),
+]
+
+
+@pytest.mark.parametrize("case", PLAN_CASES, ids=[c[0] for c in PLAN_CASES])
+def test_plan_covers_rows_once_with_mask_tiles(pa, case):
+    _, HQ, HKV, seqs, S, W = case
+    units, n_tiles, n_rows = pa.pa_plan(HQ, HKV, seqs, S, W)
+    G = HQ // HKV
+    TQ = 128 // G
+    covered = {}
+    lists_of = {s: oracle.block_lists(q_start, n_q, S, W, cap=4096)
+                for s, (_, q_start, n_q, _) in enumerate(seqs)}
+    for s, g, t0, tiles in units.tolist():
+        q_off, q_start, n_q, n_ctx = seqs[s]
+        toks = [t for t in range(t0, t0 + TQ) if q_start <= t < q_start + n_q]
+        assert toks, "unit without query rows"
+        for t in toks:
+            key = (s, t, g)
+            assert key not in covered
+            covered[key] = True
+        # the unit visits the union of its query blocks' visible key blocks
+        lists = lists_of[s]
+        qb0 = q_start // 16
+        union = set()
+        for qb in sorted({t // 16 for t in toks}):
+            union.update(x for x in lists[qb - qb0].tolist() if x >= 0)
+        assert tiles == expected_tiles(union), (s, g, t0)
+    want = sum(n_q for _, _, n_q, _ in seqs) * HKV
+    assert len(covered) == want
+    assert n_tiles == int(units[:, 3].sum())
+    assert all(units[i, 3] >= units[i + 1, 3] for i in range(len(units) - 1)), "longest units first"
+
+
+def test_plan_skips_blocks_no_query_sees(pa):
+    # a 2048-token chunk after a 30720-token cache: only the sink block and the
+    # window blocks reachable from the chunk are widened
+    units, _, rows = pa.pa_plan(16, 2, [(0, 30720, 2048, 32768)], 1, 256)
+    first_lo = 30720 // 16 + 1 - 256
+    assert rows == 16 * (1 + (32768 // 16 - first_lo))
+
+
+def test_gloo_two_rank_reduction_and_aggregate():
+    """The bench's N>1 bookkeeping: slowest rank's time, whole-job throughput."""
+    code = r"""
+import os, sys
+sys.path.insert(0, %r)
+import torch.distributed as dist
+import bench
+dist.init_process_group("gloo")
+r = dist.get_rank()
+slow = bench.max_over_ranks(10.0 + 5.0 * r)
+v = bench.aggregate_tops(2e12, 10, slow, dist.get_world_size())
+print("RANK", r, slow, v, flush=True)
+dist.destroy_process_group()
+""" % ROOT
+    env = dict(os.environ, MASTER_ADDR="127.0.0.1", MASTER_PORT=str(29500 + os.getpid() % 1000), WORLD_SIZE="2")
+    procs = []
+    for r in range(2):
+        e = dict(env, RANK=str(r), LOCAL_RANK=str(r))
+        procs.append(subprocess.Popen([sys.executable, "-c", code], env=e, stdout=subprocess.PIPE,
+                                      stderr=subprocess.PIPE, text=True))
+    outs = [p.communicate(timeout=120) for p in procs]
+    for p, (o, e) in zip(procs, outs):
+        assert p.returncode == 0, e
+        _, _, slow, v = o.strip().split()[-4:]
+        assert float(slow) == 15.0
+        assert abs(float(v) - 2 * 2e12 * 10 / 0.015 / 1e12) < 1e-6
+
+
+def test_bench_ops_count_matches_oracle_enumeration():
+    import bench
+    for name in ("tiny", "4k", "32k", "chunked_ragged"):
+        wl = CONFIGS[name]
+        pairs = sum(oracle.visible_pairs(qs, nq, wl.n_sink_blk, wl.n_win_blk) for qs, nq in wl.seqs)
+        assert bench.algorithmic_ops(wl) == 4 * 256 * wl.n_q_heads * pairs
+
+
+def test_no_product_module_uses_the_oracle():
+    pkg = os.path.join(ROOT, "windowed_prefill_attention_gb300")
+    pat = re.compile(r"^\s*(import oracle|from oracle)|pa_oracle|_pa_oracle", re.M)
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                assert not pat.search(open(os.path.join(dirpath, f)).read()), f

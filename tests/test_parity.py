@@ -1,0 +1,172 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Every workload of the benchmark at full size (sampled rows for the long
+ones), in the launch configuration bench.py times (pa_prefill_batch), plus
+edge cases of the mask and the shapes.  The bar is the stated tolerance:
+max |err| <= 3e-2 * max(1, |ref|) and mean |err| / max(1, |ref|) <= 1e-2.
+
+A tighter check compares against the oracle's walk through the method's
+own quantisation steps, so a kernel bug hidden inside the quantisation
+budget still shows.  Its bound comes from the arithmetic: the output is
+rounded to bf16, whose 8-bit significand has unit roundoff 2^-8 ~ 3.9e-3
+(relative, so at most 3.9e-3 after normalising by max(1, |ref|)); P' is
+rounded to fp16 on both sides (a differing rounding changes one term by
+<= 2^-11 relative) and the fp32 accumulation adds ~1e-6; so 5e-3 on the max
+and 5e-4 on the mean.
+On the u8 grid a code may flip by one where the GPU's fp32 exp and the
+oracle's fp64 exp straddle a rounding boundary (1/255 of the tile's largest
+P' times one value), hence 1.5e-2 / 1e-3 there.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from pa_testutil import TOL_MAX, TOL_MEAN, compare, norm_errors, run_gpu, sample_rows
+from synth import CONFIGS, make_inputs
+from synth.workloads import Workload
+
+pytestmark = pytest.mark.gpu
+
+FULL = {
+    "tiny": None,       # all rows
+    "4k": 600,          # random tokens (x all heads) plus edges
+    "32k": 256,
+    "64k": 192,
+    "chunked": 256,
+    "chunked_ragged": 256,
+}
+
+
+@pytest.fixture(scope="module")
+def inputs():
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            cache[name] = make_inputs(CONFIGS[name])
+        return cache[name]
+    return get
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_default_mode_matches_oracle(name, inputs):
+    inp = inputs(name)
+    out, rc = run_gpu(inp)
+    assert rc == 0
+    rows = oracle.all_rows(inp) if FULL[name] is None else sample_rows(inp, FULL[name])
+    mx, mean = compare(out, inp, rows)
+    print("%s: max %.3g mean %.3g over %d rows" % (name, mx, mean, len(rows)))
+    assert mx <= TOL_MAX and mean <= TOL_MEAN
+    # rows outside every query range are never written: every output row is finite
+    assert np.isfinite(out).all()
+
+
+@pytest.mark.parametrize("name", ["tiny", "4k", "chunked_ragged"])
+def test_default_mode_matches_method_steps(name, inputs):
+    inp = inputs(name)
+    out, rc = run_gpu(inp)
+    assert rc == 0
+    rows = oracle.all_rows(inp) if name == "tiny" else sample_rows(inp, 200)
+    ref = oracle.method(oracle.Problem.from_inputs(inp), rows, oracle.Q_LOSSLESS, oracle.P_F16, tile=64)
+    mx, mean = norm_errors(out[rows[:, 0], rows[:, 1]].astype(np.float64), ref)
+    print("%s vs method: max %.3g mean %.3g" % (name, mx, mean))
+    assert mx <= 5e-3 and mean <= 5e-4
+
+
+@pytest.mark.parametrize("name", ["tiny", "4k"])
+def test_int8_grids_match_oracle_on_clean_data(name, inputs):
+    """The pages' literal int8 Q / u8 P grids, on the workloads without outliers."""
+    inp = inputs(name)
+    out, rc = run_gpu(inp, q_mode=1, p_mode=1)
+    assert rc == 0
+    rows = oracle.all_rows(inp) if name == "tiny" else sample_rows(inp, 300)
+    mx, mean = compare(out, inp, rows)
+    assert mx <= TOL_MAX and mean <= TOL_MEAN
+    ref = oracle.method(oracle.Problem.from_inputs(inp), rows, oracle.Q_INT8, oracle.P_U8, tile=64)
+    mx2, mean2 = norm_errors(out[rows[:, 0], rows[:, 1]].astype(np.float64), ref)
+    print("%s int8 grids: vs exact %.3g/%.3g, vs method %.3g/%.3g" % (name, mx, mean, mx2, mean2))
+    assert mx2 <= 1.5e-2 and mean2 <= 1e-3
+
+
+def test_int8_q_grid_alone_follows_method(inputs):
+    inp = inputs("chunked_ragged")
+    out, rc = run_gpu(inp, q_mode=1, p_mode=0)
+    assert rc == 0
+    rows = sample_rows(inp, 100)
+    ref = oracle.method(oracle.Problem.from_inputs(inp), rows, oracle.Q_INT8, oracle.P_F16, tile=64)
+    mx, mean = norm_errors(out[rows[:, 0], rows[:, 1]].astype(np.float64), ref)
+    assert mx <= 5e-3 and mean <= 5e-4
+
+
+EDGE = {
+    # name: (workload, S, W)
+    "window_off": (Workload("e_off", 16, 2, ((0, 2048),), 1, 256, seed=31), 1, 0),
+    "window_negative": (Workload("e_neg", 16, 2, ((0, 1500),), 2, 256, seed=32), 2, -1),
+    "window_one_block": (Workload("e_w1", 16, 2, ((0, 1200),), 0, 1, seed=33, outlier_frac=0.02), 0, 1),
+    "sink_covers_window_start": (Workload("e_sink", 16, 2, ((0, 1600),), 1, 4, seed=34), 90, 4),
+    "no_sink": (Workload("e_nosink", 16, 2, ((0, 1600),), 0, 8, seed=35), 0, 8),
+    "single_query_long_context": (Workload("e_one", 16, 2, ((5000, 1),), 1, 256, seed=36), 1, 256),
+    "ragged_rows": (Workload("e_rag", 16, 2, ((0, 1001),), 1, 16, seed=37), 1, 16),
+    "unaligned_start": (Workload("e_una", 16, 2, ((1003, 517),), 1, 8, seed=38), 1, 8),
+    "gqa_4_window": (Workload("e_g4", 8, 2, ((37, 700),), 2, 3, seed=39), 2, 3),
+    "gqa_2": (Workload("e_g2", 8, 4, ((0, 600),), 1, 5, seed=40), 1, 5),
+    "gqa_1": (Workload("e_g1", 4, 4, ((11, 333),), 1, 2, seed=41), 1, 2),
+    "gqa_16": (Workload("e_g16", 32, 2, ((0, 500),), 1, 4, seed=42), 1, 4),
+    "many_sequences": (Workload("e_many", 16, 2, ((0, 16), (100, 1), (7, 300), (2000, 64), (33, 33)), 1, 4,
+                                seed=43, outlier_frac=0.05), 1, 4),
+}
+
+
+@pytest.mark.parametrize("case", list(EDGE))
+def test_edge_cases_match_oracle(case):
+    wl, S, W = EDGE[case]
+    inp = make_inputs(wl)
+    out, rc = run_gpu(inp, S=S, W=W)
+    assert rc == 0
+    rows = oracle.all_rows(inp) if inp.q.shape[0] * inp.q.shape[1] <= 20000 else sample_rows(inp, 400)
+    mx, mean = compare(out, inp, rows, n_sink_blk=S, n_win_blk=W)
+    print("%s: max %.3g mean %.3g" % (case, mx, mean))
+    assert mx <= TOL_MAX and mean <= TOL_MEAN
+
+
+def test_window_covering_context_equals_window_off_bitwise():
+    inp = make_inputs(Workload("e_cov", 16, 2, ((0, 1024),), 1, 64, seed=44))
+    a, rc1 = run_gpu(inp, S=1, W=64)
+    b, rc2 = run_gpu(inp, S=1, W=0)
+    assert rc1 == 0 and rc2 == 0
+    assert np.array_equal(a, b)
+
+
+def test_page_permutation_is_bitwise_invariant():
+    wl = Workload("e_perm", 16, 2, ((0, 900),), 1, 8, seed=45, outlier_frac=0.02)
+    inp = make_inputs(wl)
+    a, _ = run_gpu(inp)
+    perm = np.random.default_rng(7).permutation(inp.k_pool.shape[0])
+    for arr in ("k_pool", "v_pool", "k_scale", "v_scale"):
+        x = getattr(inp, arr)
+        y = np.empty_like(x)
+        y[perm] = x
+        setattr(inp, arr, y)
+    bt = inp.block_table.copy()
+    bt[bt >= 0] = perm[bt[bt >= 0]]
+    inp.block_table = bt
+    b, rc = run_gpu(inp)
+    assert rc == 0 and np.array_equal(a, b)
+
+
+def test_host_buffer_entry_point_matches_device_entry_point(inputs):
+    import torch
+
+    import windowed_prefill_attention_gb300 as pa
+    inp = inputs("4k")
+    a, _ = run_gpu(inp)
+    wl = inp.wl
+    h = pa.pa_create(wl.n_q_heads, wl.n_kv_heads, inp.k_pool.shape[0], inp.block_table.shape[1])
+    try:
+        out = torch.empty(inp.q.shape, dtype=torch.int16).pin_memory()
+        pa.pa_prefill_host(h, inp.seq_desc, torch.from_numpy(inp.q.view(np.int16)), inp.k_pool, inp.v_pool,
+                           inp.k_scale, inp.v_scale, inp.block_table, wl.n_sink_blk, wl.n_win_blk, wl.sm_scale, out)
+    finally:
+        pa.pa_destroy(h)
+    b = out.view(torch.bfloat16).float().numpy()
+    assert np.array_equal(a, b)

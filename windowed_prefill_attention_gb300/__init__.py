@@ -31,7 +31,8 @@ EXPORTED = ("pa_default_options", "pa_create", "pa_destroy", "pa_prefill", "pa_p
 
 
 class pa_options(C.Structure):
-    _fields_ = [("q_mode", C.c_int), ("p_mode", C.c_int), ("wait_timeout_ms", C.c_int), ("record_timing", C.c_int)]
+    _fields_ = [("q_mode", C.c_int), ("p_mode", C.c_int), ("wait_timeout_ms", C.c_int), ("record_timing", C.c_int),
+                ("debug_stall", C.c_int)]
 
 
 class pa_seq(C.Structure):
@@ -120,8 +121,8 @@ def pa_default_options() -> pa_options:
 
 
 def pa_create(n_q_heads, n_kv_heads, n_pool_pages, max_pages_per_seq, head_dim=256, page_size=16,
-              q_mode=PA_Q_F16, p_mode=PA_P_F16, wait_timeout_ms=2000, record_timing=False):
-    o = pa_options(q_mode, p_mode, wait_timeout_ms, 1 if record_timing else 0)
+              q_mode=PA_Q_F16, p_mode=PA_P_F16, wait_timeout_ms=2000, record_timing=False, debug_stall=False):
+    o = pa_options(q_mode, p_mode, wait_timeout_ms, 1 if record_timing else 0, 1 if debug_stall else 0)
     h = C.c_void_p()
     _check(_lib.pa_create(C.byref(h), n_q_heads, n_kv_heads, head_dim, page_size, n_pool_pages, max_pages_per_seq,
                           C.byref(o)), "pa_create")

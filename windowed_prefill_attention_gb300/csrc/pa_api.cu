@@ -367,6 +367,7 @@ int run(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t*
   a.err = h->d_err;
   a.wait_ns = (unsigned long long)h->opt.wait_timeout_ms * 1000000ull;
   a.unit_counter = h->d_counter;
+  a.debug_stall = h->opt.debug_stall;
   PA_CUDA(launch_attention(a, h->maps, h->n_sm, st));
   if (e2) {
     PA_CUDA(cudaEventRecord(e2, st));
@@ -387,6 +388,7 @@ void pa_default_options(pa_options* opt) {
   opt->p_mode = PA_P_F16;
   opt->wait_timeout_ms = 2000;
   opt->record_timing = 0;
+  opt->debug_stall = 0;
 }
 
 const char* pa_strerror(int code) {

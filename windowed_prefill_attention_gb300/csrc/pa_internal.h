@@ -58,6 +58,7 @@ struct AttnParams {
   int* err;
   unsigned long long wait_ns;
   int* unit_counter;          // persistent-grid work counter (zeroed per launch)
+  int debug_stall;            // test hook: first wait targets a barrier nothing arrives at
 };
 
 struct AttnMaps {

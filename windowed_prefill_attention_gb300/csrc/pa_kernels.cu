@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     attention_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ AttnMaps m) {
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bars[4];  // 0: Q, 1-2: K/V stages, 3: MMA
+  __shared__ __align__(8) uint64_t bars[5];  // 0: Q, 1-2: K/V stages, 3: MMA, 4: never armed (test hook)
   __shared__ uint32_t tmem_base_s;
 
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t sm_base = smem_u32(sm);
 
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    for (int i = 0; i < 5; ++i) mbar_init(smem_u32(&bars[i]), 1);
     fence_mbar_init();
     tma_prefetch_map(&m.q);
     tma_prefetch_map(&m.k);
@@ -204,8 +204,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int r = tid;
   const int t_row = un.t0 + r / p.G;
   const int h_row = un.g * p.G + r % p.G;
-  bool ok = mbar_wait(bar_q, 0, wc, 1);
-  const bool q_landed = ok;
+  bool ok = mbar_wait(p.debug_stall ? smem_u32(&bars[4]) : bar_q, 0, wc, 1);
+  const bool q_landed = ok && !p.debug_stall;
   float c_row = 0.f;  // s_q * sm_scale * log2(e)
   if (ok) {
     const uint8_t* qs = sm + kSmQ;
@@ -407,12 +407,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   // ---- teardown: never leave copies or MMAs in flight, then free TMEM
   if (tid == 0) {
-    const WaitCtl drain{p.err, 50000000ull};
-    if (mma_pending) (void)mbar_wait(bar_mma, mma_phase, drain, 5);
+    const uint64_t drain_ns = 200000000ull;
+    if (mma_pending) (void)mbar_wait_drain(bar_mma, mma_phase, drain_ns);
     // loads issued but not consumed: tiles [consumed, issued); each stage has
     // at most one such load, whose phase is the stage's current one
-    for (int i = consumed; i < issued; ++i) (void)mbar_wait(bar_kv0 + 8 * (i & 1), (i >> 1) & 1, drain, 6);
-    if (!q_landed) (void)mbar_wait(bar_q, 0, drain, 7);
+    for (int i = consumed; i < issued; ++i) (void)mbar_wait_drain(bar_kv0 + 8 * (i & 1), (i >> 1) & 1, drain_ns);
+    if (!q_landed) (void)mbar_wait_drain(bar_q, 0, drain_ns);
   }
   tc_fence_before();
   __syncthreads();
