@@ -10,13 +10,20 @@ own quantisation steps, so a kernel bug hidden inside the quantisation
 budget still shows.  Its bound comes from the arithmetic: the output is
 rounded to bf16, whose 8-bit significand has unit roundoff 2^-8 ~ 3.9e-3
 (relative, so at most 3.9e-3 after normalising by max(1, |ref|)); P' is
-rounded to fp16 on both sides (a differing rounding changes one term by
-<= 2^-11 relative) and the fp32 accumulation adds ~1e-6; so 5e-3 on the max
-and 5e-4 on the mean.
+rounded to fp16 on both sides, where the two roundings differ (the GPU's
+running max lags by up to 2^8 and its V-scale normaliser shifts P'), each
+adding <= 2^-11 * sum_j p_j |V_j| / l, about 2^-11 on data without outliers;
+the fp32 accumulation adds ~1e-6.  So 5e-3 on the max and 5e-4 on the mean,
+on workloads without outliers.  With outlier tokens (K and V x8) the sum of
+|p_j V_j| reaches ~8x the output scale and cancels, so the fp16 rounding
+noise of the two sides alone reaches ~1e-2 and this comparison resolves no
+more than the one against the definition; it is not run there.
 On the u8 grid a code may flip by one where the GPU's fp32 exp and the
 oracle's fp64 exp straddle a rounding boundary (1/255 of the tile's largest
 P' times one value), hence 1.5e-2 / 1e-3 there.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -61,9 +68,12 @@ def test_default_mode_matches_oracle(name, inputs):
     assert np.isfinite(out).all()
 
 
-@pytest.mark.parametrize("name", ["tiny", "4k", "chunked_ragged"])
+CLEAN_CHUNKED = dataclasses.replace(CONFIGS["chunked_ragged"], name="chunked_clean", outlier_frac=0.0)
+
+
+@pytest.mark.parametrize("name", ["tiny", "4k", "chunked_clean"])
 def test_default_mode_matches_method_steps(name, inputs):
-    inp = inputs(name)
+    inp = inputs(name) if name != "chunked_clean" else make_inputs(CLEAN_CHUNKED)
     out, rc = run_gpu(inp)
     assert rc == 0
     rows = oracle.all_rows(inp) if name == "tiny" else sample_rows(inp, 200)
@@ -88,8 +98,8 @@ def test_int8_grids_match_oracle_on_clean_data(name, inputs):
     assert mx2 <= 1.5e-2 and mean2 <= 1e-3
 
 
-def test_int8_q_grid_alone_follows_method(inputs):
-    inp = inputs("chunked_ragged")
+def test_int8_q_grid_alone_follows_method():
+    inp = make_inputs(CLEAN_CHUNKED)
     out, rc = run_gpu(inp, q_mode=1, p_mode=0)
     assert rc == 0
     rows = sample_rows(inp, 100)
