@@ -55,6 +55,7 @@ extern "C" {
 #define PA_ETIMEOUT (-4)  /* a device-side wait ran out (see pa_options.wait_timeout_ms) */
 #define PA_EBADPAGE (-5)  /* a block-table entry read was outside [0, n_pool_pages) */
 #define PA_ENOMEM (-6)    /* workspace allocation failed */
+#define PA_ENOSCRATCH (-7) /* pa_prefill_noalloc: the call needs more than PA_NOALLOC_SCRATCH_BYTES */
 
 /* Query container (step "Q per-row quantise", fused into the kernel prologue). */
 #define PA_Q_F16 0   /* default: per-row power-of-two scale into fp16 (lossless for bf16 input) */
@@ -150,6 +151,35 @@ int pa_debug_gather(pa_handle h, int n_seq, const pa_seq* seqs, const int8_t* k_
 int pa_debug_maskset(pa_handle h, int n_seq, const pa_seq* seqs, int n_sink_blk, int n_win_blk,
                      int32_t* row_counts, int32_t* unit_blocks, int cap, int32_t* units_out, int units_cap,
                      int* n_units, void* stream);
+
+/* Allocation-free variant of pa_prefill (one sequence, default fp16
+ * containers).  The pages have no counterpart of this entry point: it exists
+ * for callers that may not call cudaMalloc / cudaFree, for example an engine
+ * that has reserved nearly all device memory for its own KV-cache pool and
+ * accounts for every byte, or code on a latency-critical path where an
+ * allocation, which can synchronise the device, is not allowed.
+ *
+ * It takes no handle and allocates nothing: its scratch (widened K/V copies
+ * of the visible pages, scales, work list, error word) lives in one static
+ * device array of PA_NOALLOC_SCRATCH_BYTES that every GPU loading this
+ * library holds until the process exits.  Arguments and layouts are those of
+ * pa_create + pa_prefill.  A call whose visible context does not fit
+ * (widened rows x n_kv_heads x 1032 bytes plus a 1 MiB work list) returns
+ * PA_ENOSCRATCH before touching the GPU; with the 32 MiB array that is about
+ * 32000 token-heads, e.g. 16000 visible tokens for 2 kv heads.
+ *
+ * All calls share the one array and each call clears what must start at
+ * zero, so calls on different streams, or from different threads, that
+ * overlap on the GPU race and corrupt each other: serialise them.  The first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current, so make the first call before any stream
+ * capture.  The call is synchronous: it waits for `stream` and returns the
+ * device-side status (PA_ETIMEOUT, PA_EBADPAGE) of this call. */
+#define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
+int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_pages, int max_pages_per_seq, const void* q,
+                       const int8_t* k_pool, const int8_t* v_pool, const float* k_scale, const float* v_scale,
+                       const int32_t* block_table, int q_start, int n_q, int n_ctx, int n_sink_blk, int n_win_blk,
+                       float sm_scale, void* out, void* stream);
 
 #ifdef __cplusplus
 }

@@ -22,12 +22,14 @@ if not os.path.exists(_LIB_PATH):
 
 _lib = C.CDLL(_LIB_PATH)
 
-PA_OK, PA_EINVAL, PA_EARCH, PA_ECUDA, PA_ETIMEOUT, PA_EBADPAGE, PA_ENOMEM = 0, -1, -2, -3, -4, -5, -6
+PA_OK, PA_EINVAL, PA_EARCH, PA_ECUDA, PA_ETIMEOUT, PA_EBADPAGE, PA_ENOMEM, PA_ENOSCRATCH = 0, -1, -2, -3, -4, -5, -6, -7
+PA_NOALLOC_SCRATCH_BYTES = 32 << 20
 PA_Q_F16, PA_Q_INT8 = 0, 1
 PA_P_F16, PA_P_U8 = 0, 1
 
 EXPORTED = ("pa_default_options", "pa_create", "pa_destroy", "pa_prefill", "pa_prefill_batch", "pa_prefill_host",
-            "pa_last_error", "pa_timing", "pa_strerror", "pa_plan", "pa_debug_gather", "pa_debug_maskset")
+            "pa_last_error", "pa_timing", "pa_strerror", "pa_plan", "pa_debug_gather", "pa_debug_maskset",
+            "pa_prefill_noalloc")
 
 
 class pa_options(C.Structure):
@@ -57,6 +59,7 @@ _lib.pa_plan.argtypes = [_i, _i, _i, C.POINTER(pa_seq), _i, _i, _vp, _i, C.POINT
 _lib.pa_debug_gather.argtypes = ([_vp, _i, C.POINTER(pa_seq)] + [_vp] * 5 + [_i, _i, _i] + [_vp] * 5
                                  + [_i, C.POINTER(_i), _vp])
 _lib.pa_debug_maskset.argtypes = [_vp, _i, C.POINTER(pa_seq), _i, _i, _vp, _vp, _i, _vp, _i, C.POINTER(_i), _vp]
+_lib.pa_prefill_noalloc.argtypes = [_i] * 4 + [_vp] * 6 + [_i] * 5 + [_f, _vp, _vp]
 
 
 class PAError(RuntimeError):
@@ -165,6 +168,16 @@ def pa_prefill_host(h, seqs, q, k_pool, v_pool, k_scale, v_scale, block_table, n
                                      (v_scale, "v_scale"), (block_table, "block_table"))]
     _check(_lib.pa_prefill_host(h, len(s), s, *args, n_sink_blk, n_win_blk, float(sm_scale), _host(out, "out"),
                                 _stream(stream)), "pa_prefill_host")
+
+
+def pa_prefill_noalloc(n_q_heads, n_kv_heads, n_pool_pages, max_pages_per_seq, q, k_pool, v_pool, k_scale, v_scale,
+                       block_table, q_start, n_q, n_ctx, n_sink_blk, n_win_blk, sm_scale, out, stream=None) -> None:
+    """Handle-free pa_prefill whose scratch is a static device array (no allocation); synchronous."""
+    import torch
+    args = _dev_inputs(q, k_pool, v_pool, k_scale, v_scale, block_table)
+    _check(_lib.pa_prefill_noalloc(n_q_heads, n_kv_heads, n_pool_pages, max_pages_per_seq, *args, q_start, n_q, n_ctx,
+                                   n_sink_blk, n_win_blk, float(sm_scale), _dev(out, torch.bfloat16, "out"),
+                                   _stream(stream)), "pa_prefill_noalloc")
 
 
 def pa_last_error(h, stream=None) -> int:

@@ -400,6 +400,7 @@ const char* pa_strerror(int code) {
     case PA_ETIMEOUT: return "device-side wait timed out";
     case PA_EBADPAGE: return "block-table entry outside the pool";
     case PA_ENOMEM: return "out of device memory";
+    case PA_ENOSCRATCH: return "call exceeds the static scratch of pa_prefill_noalloc";
     default: return "unknown error";
   }
 }

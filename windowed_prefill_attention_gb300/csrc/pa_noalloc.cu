@@ -1,0 +1,233 @@
+// Allocation-free entry point: the same widening and attention kernels as
+// pa_prefill, with every piece of scratch memory (widened K/V, scales, work
+// list, error word) carved out of one file-scope device array instead of a
+// handle's cudaMalloc'd workspace.
+//
+// Who needs it: callers that may not call cudaMalloc / cudaFree at all, for
+// example an engine that has reserved nearly all device memory for its own
+// KV-cache pool and accounts for every byte, or code on a latency-critical
+// path where an allocation (which can synchronise the device) is not allowed.
+// They pass inputs and outputs; this file allocates nothing.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+#include "pa_ptx.cuh"
+
+using namespace pa;
+
+namespace {
+
+// The scratch every call shares.  Each GPU that loads the library holds it
+// until the process exits.  Host code must not use the symbol as an address:
+// the device address comes from cudaGetSymbolAddress below.
+__device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+
+constexpr size_t kHeaderBytes = 4096;            // error word, V-scale maxima, sequence geometry
+constexpr size_t kUnitsBytes = 1u << 20;         // work list
+constexpr int kMaxUnits = (int)(kUnitsBytes / sizeof(Unit));
+constexpr size_t kWidenedOffset = kHeaderBytes + kUnitsBytes;
+
+// Device address of the scratch, resolved once per device with that device current.
+void* scratch_address(int device, int* rc) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  std::lock_guard<std::mutex> lock(mu);
+  if (device < 0 || device >= 64) {
+    *rc = PA_ECUDA;
+    return nullptr;
+  }
+  if (!addr[device]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+      *rc = PA_ECUDA;
+      return nullptr;
+    }
+    addr[device] = p;
+  }
+  *rc = PA_OK;
+  return addr[device];
+}
+
+// Writes the sequence geometry and the work list (units ordered by
+// decreasing first token: for one sequence the later query blocks see the
+// full window, so this is the longest-first order) and clears the words that
+// must start at zero.
+__global__ void noalloc_plan_kernel(SeqGeom sg, int S, int W, int HKV, int TQ, int n_t0, int t_first, SeqGeom* seq_out,
+                                    Unit* units, unsigned int* vsmax, int* err) {
+  const int n_units = n_t0 * HKV;
+  for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < n_units; u += gridDim.x * blockDim.x) {
+    const int t0 = t_first + (n_t0 - 1 - u / HKV) * TQ;
+    units[u] = Unit{0, u % HKV, t0, unit_geom(t0, TQ, sg, S, W).n_tiles};
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *seq_out = sg;
+    *err = 0;
+  }
+  if (blockIdx.x == 0 && threadIdx.x < HKV) vsmax[threadIdx.x] = 0u;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int encode3(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+            uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (!fn) return PA_ECUDA;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1, s2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? PA_OK
+             : PA_ECUDA;
+}
+
+bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_pages, int max_pages_per_seq,
+                                  const void* q, const int8_t* k_pool, const int8_t* v_pool, const float* k_scale,
+                                  const float* v_scale, const int32_t* block_table, int q_start, int n_q, int n_ctx,
+                                  int n_sink_blk, int n_win_blk, float sm_scale, void* out, void* stream) {
+  // argument checks (the same rules as pa_create / pa_prefill)
+  if (n_q_heads <= 0 || n_kv_heads <= 0 || n_kv_heads > 8 || n_q_heads % n_kv_heads) return PA_EINVAL;
+  const int G = n_q_heads / n_kv_heads;
+  if (G > kRows || kRows % G) return PA_EINVAL;
+  if (n_pool_pages <= 0 || max_pages_per_seq <= 0 || n_sink_blk < 0) return PA_EINVAL;
+  if (n_q < 1 || q_start < 0 || n_ctx < q_start + n_q || (long long)n_ctx > (long long)max_pages_per_seq * kPage)
+    return PA_EINVAL;
+  if (!q || !k_pool || !v_pool || !k_scale || !v_scale || !block_table || !out) return PA_EINVAL;
+  if (!aligned_to(q, 16) || !aligned_to(k_pool, 16) || !aligned_to(v_pool, 16) || !aligned_to(out, 16) ||
+      !aligned_to(k_scale, 4) || !aligned_to(v_scale, 4) || !aligned_to(block_table, 4))
+    return PA_EINVAL;
+  if (!(sm_scale == sm_scale) || sm_scale < 0.f) return PA_EINVAL;
+  const int TQ = kRows / G;
+
+  SeqGeom sg{};
+  sg.q_off = 0;
+  sg.q_start = q_start;
+  sg.n_q = n_q;
+  sg.n_ctx = n_ctx;
+  sg.tok_off = 0;
+  sg.bt_row = 0;
+  seq_geom_fill(sg, n_sink_blk, n_win_blk);
+  const long long n_rows = (long long)sg.n_blocks * kPage;
+  const int t_first = (q_start / TQ) * TQ;
+  const int n_t0 = (q_start + n_q - 1 - t_first) / TQ + 1;
+  // size limits of the static scratch: a clear error, never an overflow
+  const long long row_bytes = (long long)n_kv_heads * (2 * kHeadDim * (long long)sizeof(__half) + 2 * sizeof(float));
+  const long long cap_rows = ((long long)PA_NOALLOC_SCRATCH_BYTES - (long long)kWidenedOffset) / row_bytes / 64 * 64;
+  if (n_rows > cap_rows || (long long)n_t0 * n_kv_heads > kMaxUnits) return PA_ENOSCRATCH;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ECUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return PA_ECUDA;
+  if (prop.major != 10 || prop.minor != 3) return PA_EARCH;
+  int rc = PA_OK;
+  unsigned char* base = static_cast<unsigned char*>(scratch_address(dev, &rc));
+  if (rc) return rc;
+
+  // carve the scratch
+  const int cap = (int)cap_rows;  // row stride of the widened buffers
+  int* err = reinterpret_cast<int*>(base);
+  unsigned int* vsmax = reinterpret_cast<unsigned int*>(base + 256);
+  SeqGeom* seq_dev = reinterpret_cast<SeqGeom*>(base + 512);
+  Unit* units = reinterpret_cast<Unit*>(base + kHeaderBytes);
+  unsigned char* w = base + kWidenedOffset;
+  __half* kw = reinterpret_cast<__half*>(w);
+  w += (size_t)n_kv_heads * cap * kHeadDim * sizeof(__half);
+  __half* vt = reinterpret_cast<__half*>(w);
+  w += (size_t)n_kv_heads * cap * kHeadDim * sizeof(__half);
+  float* ks = reinterpret_cast<float*>(w);
+  w += (size_t)n_kv_heads * cap * sizeof(float);
+  float* vs = reinterpret_cast<float*>(w);
+
+  AttnMaps m;
+  if ((rc = encode3(&m.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, kHeadDim, n_q_heads, n_q, kHeadDim * 2,
+                    (uint64_t)n_q_heads * kHeadDim * 2, 64, G, TQ)))
+    return rc;
+  if ((rc = encode3(&m.k, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, kw, kHeadDim, n_rows, n_kv_heads, kHeadDim * 2,
+                    (uint64_t)cap * kHeadDim * 2, 64, kTileKeys, 1)))
+    return rc;
+  if ((rc = encode3(&m.v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, vt, n_rows, kHeadDim, n_kv_heads, (uint64_t)cap * 2,
+                    (uint64_t)cap * kHeadDim * 2, kTileKeys, kHeadDim, 1)))
+    return rc;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  noalloc_plan_kernel<<<(n_t0 * n_kv_heads + 255) / 256, 256, 0, st>>>(sg, n_sink_blk, n_win_blk, n_kv_heads, TQ, n_t0,
+                                                                       t_first, seq_dev, units, vsmax, err);
+  if (cudaGetLastError() != cudaSuccess) return PA_ECUDA;
+
+  WidenParams wp{};
+  wp.k_pool = k_pool;
+  wp.v_pool = v_pool;
+  wp.k_scale = k_scale;
+  wp.v_scale = v_scale;
+  wp.block_table = block_table;
+  wp.bt_stride = max_pages_per_seq;
+  wp.n_pool = n_pool_pages;
+  wp.HKV = n_kv_heads;
+  wp.seqs = seq_dev;
+  wp.n_seq = 1;
+  wp.n_stored_blocks = sg.n_blocks;
+  wp.n_tok_cap = cap;
+  wp.kw = kw;
+  wp.vt = vt;
+  wp.ks = ks;
+  wp.vs = vs;
+  wp.vsmax = vsmax;
+  wp.err = err;
+  if (launch_widen(wp, st) != cudaSuccess) return PA_ECUDA;
+
+  AttnParams a{};
+  a.seqs = seq_dev;
+  a.units = units;
+  a.n_units = n_t0 * n_kv_heads;
+  a.ks = ks;
+  a.vs = vs;
+  a.vsmax = vsmax;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.HQ = n_q_heads;
+  a.HKV = n_kv_heads;
+  a.G = G;
+  a.TQ = TQ;
+  a.n_tok_cap = cap;
+  a.S = n_sink_blk;
+  a.W = n_win_blk;
+  a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  a.q_mode = PA_Q_F16;
+  a.p_mode = PA_P_F16;
+  a.err = err;
+  a.wait_ns = 2000ull * 1000000ull;
+  a.unit_counter = nullptr;
+  a.debug_stall = 0;
+  if (launch_attention(a, m, prop.multiProcessorCount, st) != cudaSuccess) return PA_ECUDA;
+
+  // synchronous: report this call's device-side status
+  if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ECUDA;
+  int e = 0;
+  if (cudaMemcpy(&e, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ECUDA;
+  if (e & DEV_ERR_TIMEOUT) return PA_ETIMEOUT;
+  if (e & DEV_ERR_BAD_PAGE) return PA_EBADPAGE;
+  return e ? PA_ECUDA : PA_OK;
+}
