@@ -121,8 +121,6 @@ struct pa_ctx {
 
   // tensor maps
   AttnMaps maps{};
-  const void* q_ptr = nullptr;
-  int q_rows = -1;
   const void* kv_ptr = nullptr;
   int kv_rows = -1;
   int kv_cap = -1;
@@ -308,16 +306,6 @@ int run(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t*
   if ((rc = prepare(h, n_seq, seqs, S, W, st))) return rc;
   const Plan& P = h->plan;
   // tensor maps
-  if (q != h->q_ptr || P.total_q != h->q_rows) {
-    const uint64_t dims[3] = {(uint64_t)kHeadDim, (uint64_t)h->HQ, (uint64_t)P.total_q};
-    const uint64_t strides[2] = {(uint64_t)kHeadDim * 2, (uint64_t)h->HQ * kHeadDim * 2};
-    const uint32_t box[3] = {64, (uint32_t)h->G, (uint32_t)h->TQ};
-    if ((rc = encode(&h->maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box,
-                     CU_TENSOR_MAP_SWIZZLE_128B)))
-      return rc;
-    h->q_ptr = q;
-    h->q_rows = P.total_q;
-  }
   if (h->kw != h->kv_ptr || P.n_tok_total != h->kv_rows || h->n_tok_cap != h->kv_cap) {
     const uint64_t kd[3] = {(uint64_t)kHeadDim, (uint64_t)P.n_tok_total, (uint64_t)h->HKV};
     const uint64_t kst[2] = {(uint64_t)kHeadDim * 2, (uint64_t)h->n_tok_cap * kHeadDim * 2};
@@ -347,6 +335,8 @@ int run(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t*
   PA_CUDA(launch_widen(widen_params(h, kp, vp, ksc, vsc, bt, n_seq), st));
   if (e1) PA_CUDA(cudaEventRecord(e1, st));
   AttnParams a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.total_q = P.total_q;
   a.seqs = h->d_seqs;
   a.units = h->d_units;
   a.n_units = (int)P.units.size();

@@ -43,6 +43,8 @@ struct WidenParams {
 };
 
 struct AttnParams {
+  const __nv_bfloat16* q;     // [total_q][HQ][256]
+  int total_q;
   const SeqGeom* seqs;
   const Unit* units;
   int n_units;
@@ -62,7 +64,6 @@ struct AttnParams {
 };
 
 struct AttnMaps {
-  CUtensorMap q;   // Q   [total_q][HQ][256] bf16, box {64, G, TQ}
   CUtensorMap k;   // Kw  [HKV][n_tok][256] fp16, box {64, 64, 1}
   CUtensorMap v;   // Vt  [HKV][256][n_tok] fp16, box {64, 256, 1}
 };

@@ -163,9 +163,6 @@ extern "C" int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_page
   float* vs = reinterpret_cast<float*>(w);
 
   AttnMaps m;
-  if ((rc = encode3(&m.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, kHeadDim, n_q_heads, n_q, kHeadDim * 2,
-                    (uint64_t)n_q_heads * kHeadDim * 2, 64, G, TQ)))
-    return rc;
   if ((rc = encode3(&m.k, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, kw, kHeadDim, n_rows, n_kv_heads, kHeadDim * 2,
                     (uint64_t)cap * kHeadDim * 2, 64, kTileKeys, 1)))
     return rc;
@@ -200,6 +197,8 @@ extern "C" int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_page
   if (launch_widen(wp, st) != cudaSuccess) return PA_ECUDA;
 
   AttnParams a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.total_q = n_q;
   a.seqs = seq_dev;
   a.units = units;
   a.n_units = n_t0 * n_kv_heads;

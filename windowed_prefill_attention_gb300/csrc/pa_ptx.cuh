@@ -53,6 +53,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete may be suspended
+// for up to `hint_ns` (it resumes when the phase completes), so waiting warps
+// do not compete for issue slots with the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Where a bounded wait reports, and how long it may spin.
 struct WaitCtl {
   int* err;           // device error word (0 = fine); first error wins
@@ -67,7 +82,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if ((i & 31u) == 0u) {
       if (*reinterpret_cast<volatile int*>(w.err) != 0) return false;
       if (globaltimer_ns() - t0 > w.limit_ns) {
@@ -116,6 +131,17 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
           dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// ---------------------------------------------------------------- shared memory
+// 16-byte shared load by 32-bit shared address.  Volatile, so it stays after
+// the mbarrier wait that made the data visible.
+__device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
 }
 
 // ---------------------------------------------------------------- tcgen05

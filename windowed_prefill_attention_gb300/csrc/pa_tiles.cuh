@@ -130,12 +130,26 @@ PA_HD TileGeom tile_geom(const UnitGeom& u, int i, int S, int W) {
   return g;
 }
 
-// The per-key predicate, used inside tiles that need masking.
-PA_HD bool key_visible(int t, int j, int S, int W) {
-  if (j > t) return false;
-  if (W <= 0) return true;
-  const int bj = j / kPage;
-  return bj < S || bj >= imax(0, t / kPage + 1 - W);
+// Bits [0, n) set, for n clamped to [0, 64].
+PA_HD unsigned long long low_bits(int n) {
+  return n <= 0 ? 0ull : (n >= 64 ? ~0ull : ((1ull << n) - 1ull));
+}
+
+// Which of a tile's 64 key columns query token t sees, as a bit mask: the
+// tile's width and, where the tile needs masking, the causal bound (key <= t)
+// and the sink / window test (key block < S, or >= lo = max(0, t/16 + 1 - W)).
+// This is the mask the softmax applies, one bit test per score.
+PA_HD unsigned long long visible_columns(const TileGeom& tg, int t, int S, int W) {
+  const int key0 = tg.kb0 * kPage;
+  unsigned long long v = low_bits(tg.nb * kPage);
+  if (tg.needs_mask) {
+    v &= low_bits(t - key0 + 1);
+    if (W > 0) {
+      const int lo = imax(0, t / kPage + 1 - W);
+      v &= low_bits(S * kPage - key0) | ~low_bits(lo * kPage - key0);
+    }
+  }
+  return v;
 }
 
 }  // namespace pa
