@@ -17,8 +17,9 @@
 //   warp 1        TMEM allocator and the single MMA-issuing thread:
 //                 QK^T(j+1) is issued before PV(j), so the tensor core works on
 //                 the next scores while the softmax handles the current ones
-//   warps 4-7     softmax, one query row per thread (TMEM lane = row)
-//   warps 8-11    Q prologue of the next unit and epilogue of the previous one
+//   warps 4-11    softmax: one query row per thread (TMEM lane = row), two
+//                 warps per lane quadrant, each owning half of the key columns
+//   warps 12-15   Q prologue of the next unit and epilogue of the previous one
 // TMEM (512 columns): O fp32 [0,256), Q fp16 pairs [256,384), S0/S1 fp32
 // [384,448)/[448,512); P (fp16 pairs) overwrites the first half of its S.
 #include <cstdint>
@@ -33,7 +34,7 @@
 namespace pa {
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kSlots = 3;                              // depth of the K ring and of the V ring
 constexpr int kKTileBytes = kTileKeys * kHeadDim * 2;  // 32 KB: 4 regions of 64 keys x 128 B
 constexpr int kVTileBytes = kHeadDim * kTileKeys * 2;  // 32 KB: 256 dims x 128 B
@@ -41,13 +42,16 @@ constexpr int kVTileBytes = kHeadDim * kTileKeys * 2;  // 32 KB: 256 dims x 128 
 constexpr int kSmK = 0;
 constexpr int kSmV = kSmK + kSlots * kKTileBytes;
 constexpr int kSmScale = kSmV + kSlots * kVTileBytes;  // per V slot: ks[64] then vs[64]
-constexpr int kSmRows = kSmScale + kSlots * 512;       // c[2][128], l[2][128], sp[2][128] floats
-constexpr int kSmBars = kSmRows + 3 * 2 * kRows * 4;
+constexpr int kSmRows = kSmScale + kSlots * 512;       // c[2][128], l[2][2][128], sp[2][128] floats
+constexpr int kSmXchg = kSmRows + 8 * kRows * 4;       // softmax pair exchange: 2 x [2][2][128] floats
+constexpr int kSmBars = kSmXchg + 8 * kRows * 4;
 enum : int {
   B_KFULL = 0, B_KEMPTY = 3, B_VFULL = 6, B_VEMPTY = 9, B_SFULL = 12, B_PFULL = 14, B_PVDONE = 16,
   B_QFULL = 17, B_QEMPTY = 18, B_OFULL = 19, B_OEMPTY = 20, B_STATS = 21 /* two, by unit parity */,
   B_STALL = 23, B_DRAIN = 24, kNumBars = 25
 };
+constexpr float kLazy = 14.f;  // the softmax reference moves when a row max grows by more than 2^kLazy;
+                               // P' = p * v_scale * 2^-ev then stays below 2^14, inside the fp16 range
 constexpr int kSmTmemSlot = kSmBars + kNumBars * 8;
 constexpr int kAttnSmem = kSmTmemSlot + 16 + 1024;  // + alignment slack
 static_assert(kAttnSmem <= 227 * 1024, "shared memory budget");
@@ -89,9 +93,7 @@ struct Ctx {
 
 // ------------------------------------------------------------------ producer
 __device__ __forceinline__ void role_producer(const AttnParams& p, const AttnMaps& m, const Ctx& c) {
-  uint32_t kc = 0, vc = 0;
-  int k_last[kSlots], v_last[kSlots];
-  for (int s = 0; s < kSlots; ++s) k_last[s] = v_last[s] = -1;
+  uint32_t kc = 0, vc = 0;  // loads issued into the K ring and the V ring
   bool ok = true;
   for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
     const Unit un = p.units[u];
@@ -108,7 +110,6 @@ __device__ __forceinline__ void role_producer(const AttnParams& p, const AttnMap
         mbar_expect_tx(fb, kKTileBytes);
         const uint32_t dst = c.sbase + kSmK + s * kKTileBytes;
         for (int r = 0; r < 4; ++r) tma_load_3d(dst + r * 8192, &m.k, fb, r * 64, crow, un.g);
-        k_last[s] = (int)ph;
         ++kc;
       }
       {
@@ -122,15 +123,15 @@ __device__ __forceinline__ void role_producer(const AttnParams& p, const AttnMap
         const size_t soff = (size_t)un.g * p.n_tok_cap + crow;
         bulk_load(c.sbase + kSmScale + s * 512, p.ks + soff, sbytes, fb);
         bulk_load(c.sbase + kSmScale + s * 512 + 256, p.vs + soff, sbytes, fb);
-        v_last[s] = (int)ph;
         ++vc;
       }
     }
   }
-  // every issued copy lands before the CTA may exit
-  for (int s = 0; s < kSlots; ++s) {
-    if (k_last[s] >= 0) (void)mbar_wait_drain(c.bar(B_KFULL + s), (uint32_t)k_last[s], kDrainNs);
-    if (v_last[s] >= 0) (void)mbar_wait_drain(c.bar(B_VFULL + s), (uint32_t)v_last[s], kDrainNs);
+  // every issued copy lands before the CTA may exit: the last load into each
+  // slot was load number kc-1-i (K) / vc-1-i (V) for i < kSlots
+  for (uint32_t i = 0; i < (uint32_t)kSlots; ++i) {
+    if (kc > i) (void)mbar_wait_drain(c.bar(B_KFULL + (kc - 1 - i) % kSlots), ((kc - 1 - i) / kSlots) & 1, kDrainNs);
+    if (vc > i) (void)mbar_wait_drain(c.bar(B_VFULL + (vc - 1 - i) % kSlots), ((vc - 1 - i) / kSlots) & 1, kDrainNs);
   }
 }
 
@@ -156,9 +157,12 @@ __device__ __forceinline__ void role_mma(const AttnParams& p, const Ctx& c) {
         const uint32_t kaddr = c.sbase + kSmK + (t % kSlots) * kKTileBytes;
         const uint32_t d = c.tb + kTmS + (t & 1) * kTileKeys;
         const uint32_t id = idesc_f16(kRows, tg.nb * kPage, false, false);
+        // k-step s reads K bytes at kaddr + (s/4)*8192 + (s%4)*32: only the
+        // descriptor's start-address field (address >> 4) moves
+        const uint64_t kd0 = sdesc_k_sw128(kaddr);
 #pragma unroll
         for (int s = 0; s < kHeadDim / 16; ++s)
-          mma_ts(d, c.tb + kTmQ + 8 * s, sdesc_k_sw128(kaddr + (s >> 2) * 8192 + (s & 3) * 32), id, s > 0);
+          mma_ts(d, c.tb + kTmQ + 8 * s, kd0 + (uint64_t)(((s >> 2) * 8192 + (s & 3) * 32) >> 4), id, s > 0);
         mma_commit(c.bar(B_SFULL + (t & 1)));
         mma_commit(c.bar(B_KEMPTY + t % kSlots));
         if (j == n - 1) mma_commit(c.bar(B_QEMPTY));
@@ -173,8 +177,9 @@ __device__ __forceinline__ void role_mma(const AttnParams& p, const Ctx& c) {
         tc_fence_after();
         const uint32_t vaddr = c.sbase + kSmV + (t % kSlots) * kVTileBytes;
         const uint32_t a = c.tb + kTmS + (t & 1) * kTileKeys;
+        const uint64_t vd0 = sdesc_k_sw128(vaddr);
         for (int s = 0; s < tg.nb; ++s)
-          mma_ts(c.tb + kTmO, a + 8 * s, sdesc_k_sw128(vaddr + 32 * s), id_pv, (jj > 0 || s > 0) ? 1u : 0u);
+          mma_ts(c.tb + kTmO, a + 8 * s, vd0 + (uint64_t)(2 * s), id_pv, (jj > 0 || s > 0) ? 1u : 0u);
         mma_commit(c.bar(B_PVDONE));
         mma_commit(c.bar(B_VEMPTY + t % kSlots));
         if (jj == n - 1) mma_commit(c.bar(B_OFULL));
@@ -188,13 +193,22 @@ __device__ __forceinline__ void role_mma(const AttnParams& p, const Ctx& c) {
 }
 
 // ------------------------------------------------------------------ softmax
+// Two warps per TMEM lane quadrant: warp half h owns key columns [32h, 32h+32)
+// of every 64-key tile for the same 32 rows.  The pair agrees on each row's
+// running maximum through shared memory, so both halves use one reference and
+// their P', partial sums and halves of the O rescale add up exactly.
 __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, uint8_t* sm) {
-  const int r = threadIdx.x - 128;  // query row of this thread = TMEM lane
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+  const int qd = warp & 3;              // lane quadrant
+  const int h = (warp - 4) >> 2;        // column half
+  const int r = qd * 32 + lane;         // query row = TMEM lane
+  const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
   float* c_rows = reinterpret_cast<float*>(sm + kSmRows);
-  float* l_rows = c_rows + 2 * kRows;
-  float* sp_rows = c_rows + 4 * kRows;
+  float* l_rows = c_rows + 2 * kRows;           // [unit parity][half][row]
+  float* sp_rows = c_rows + 6 * kRows;          // [unit parity][row]
+  float* xbuf = reinterpret_cast<float*>(sm + kSmXchg);  // [tile parity][half][row] row maxima
+  float* pbuf = xbuf + 4 * kRows;                        // [tile parity][half][row] P' maxima (u8 grid)
+  const bool u8 = p.p_mode == 1;
   uint32_t tc = 0;
   int k_unit = 0;
   bool ok = true;
@@ -205,90 +219,111 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
     const int n = ug.n_tiles;
     const int t_row = un.t0 + r / p.G;
     const float ev = (float)pow2_ceil_exp(__uint_as_float(p.vsmax[un.seq * p.HKV + un.g]));
-    if (!(ok = c.warp_wait(B_QFULL, k_unit & 1, 30))) break;
-    const float c_row = c_rows[(k_unit & 1) * kRows + r];
+    // both warps of the pair agree before entering the unit's tiles
+    ok = bar_red_and(1 + qd, 64, c.warp_wait(B_QFULL, k_unit & 1, 30));
+    if (!ok) break;
+    // s_q * sm_scale * log2(e), kept positive so that -inf scores stay -inf
+    const float c_row = fmaxf(c_rows[(k_unit & 1) * kRows + r], 1e-30f);
     float m_run = -INFINITY, l_run = 0.f, sp_prev = 1.f;
     for (int j = 0; j < n; ++j) {
       const uint32_t t = tc + j;
       const TileGeom tg = tile_geom(ug, j, p.S, p.W);
-      if (!(ok = c.warp_wait(B_SFULL + (t & 1), (t >> 1) & 1, 31))) break;
-      if (!(ok = c.warp_wait(B_VFULL + t % kSlots, (t / kSlots) & 1, 32))) break;
-      tc_fence_after();
+      // Every path through a tile passes the pair barrier the same number of
+      // times, so a wait that runs out in one warp cannot strand its partner.
+      bool okl = c.warp_wait(B_SFULL + (t & 1), (t >> 1) & 1, 31);
+      okl = okl && c.warp_wait(B_VFULL + t % kSlots, (t / kSlots) & 1, 32);
       const uint32_t sd = c.tb + lane_off + kTmS + (t & 1) * kTileKeys;
-      uint32_t sa[32], sb[32];
-      tmem_ld32(sd, sa);
-      tmem_ld32(sd + 32, sb);
-      tmem_wait_ld(sa);
-      reg_fence(sb);
-      const uint32_t sc = c.sbase + kSmScale + (t % kSlots) * 512;  // ks[64] then vs[64]
-      const uint64_t vis = visible_columns(tg, t_row, p.S, p.W);
-      const uint32_t vis_lo = (uint32_t)vis, vis_hi = (uint32_t)(vis >> 32);
-      float x[64];
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      const uint32_t sc = c.sbase + kSmScale + (t % kSlots) * 512 + 128 * h;  // this half's ks; vs at +256
+      float y[32];
+      float my = -INFINITY;
+      if (okl) {
+        tc_fence_after();
+        uint32_t sa[32];
+        tmem_ld32(sd + 32 * h, sa);
+        tmem_wait_ld(sa);
+        const uint32_t vis = (uint32_t)(visible_columns(tg, t_row, p.S, p.W) >> (32 * h));
+        // y = S * k_scale (masked: -inf), and this half's row maximum
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int q4 = 0; q4 < 16; ++q4) {
-        const float4 k4 = lds_f32x4(sc + 16 * q4);
-        const float kq[4] = {k4.x, k4.y, k4.z, k4.w};
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 k4 = lds_f32x4(sc + 16 * q4);
+          const float kq[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int q = 4 * q4 + e;
-          const float sj = __uint_as_float(q < 32 ? sa[q] : sb[q - 32]);
-          const bool on = ((q < 32 ? vis_lo : vis_hi) >> (q & 31)) & 1u;
-          x[q] = on ? sj * kq[e] * c_row : -INFINITY;
-          mx4[e] = fmaxf(mx4[e], x[q]);
+          for (int e = 0; e < 4; ++e) {
+            const int q = 4 * q4 + e;
+            y[q] = ((vis >> q) & 1u) ? __uint_as_float(sa[q]) * kq[e] : -INFINITY;
+            m4[e] = fmaxf(m4[e], y[q]);
+          }
+        }
+        my = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c_row;  // log2 units
+      }
+      // the reference moves only when some row's max grew by more than 2^kLazy
+      const bool grow = okl && (m_run == -INFINITY || my > m_run + kLazy);
+      float alpha = 1.f;
+      if (bar_red_popc(1 + qd, 64, grow || !okl) != 0) {
+        float* xb = xbuf + (t & 1) * 2 * kRows;
+        xb[h * kRows + r] = my;
+        if (!bar_red_and(1 + qd, 64, okl)) {
+          ok = false;
+          break;
+        }
+        const float mx = fmaxf(xb[r], xb[kRows + r]);
+        if (m_run == -INFINITY || mx > m_run + kLazy) {
+          const float mnew = fmaxf(m_run, mx);
+          alpha = m_run == -INFINITY ? 0.f : ex2_approx(m_run - mnew);
+          m_run = mnew;
         }
       }
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      float alpha = 1.f;
-      if (m_run == -INFINITY || mx > m_run + 8.f) {  // move the reference only when it grows by > 2^8
-        const float mnew = fmaxf(m_run, mx);
-        alpha = m_run == -INFINITY ? 0.f : ex2_approx(m_run - mnew);
-        m_run = mnew;
-      }
       const float mref = m_run == -INFINITY ? 0.f : m_run + ev;
-      float ps4[4] = {0.f, 0.f, 0.f, 0.f}, pm4[4] = {0.f, 0.f, 0.f, 0.f};
+      // p = 2^(y c - mref); P' = p * v_scale (V scale folded into P)
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int q4 = 0; q4 < 16; ++q4) {
+      for (int q4 = 0; q4 < 8; ++q4) {
         const float4 v4 = lds_f32x4(sc + 256 + 16 * q4);
         const float vq[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int q = 4 * q4 + e;
-          const float pj = ex2_approx(x[q] - mref);
-          ps4[e] += pj;
-          const bool on = ((q < 32 ? vis_lo : vis_hi) >> (q & 31)) & 1u;
-          x[q] = on ? pj * vq[e] : 0.f;  // V scale folded into P
-          pm4[e] = fmaxf(pm4[e], x[q]);
+          const float pj = ex2_approx(fmaf(y[q], c_row, -mref));
+          s4[e] += pj;
+          y[q] = pj * vq[e];
         }
       }
-      const float psum = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
-      const float pmax = fmaxf(fmaxf(pm4[0], pm4[1]), fmaxf(pm4[2], pm4[3]));
-      l_run = l_run * alpha + psum;
+      l_run = l_run * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
       float corr = alpha;
-      if (p.p_mode == 1) {  // P' per row on the u8 grid, scale max/255
+      if (u8) {  // P' per row on the u8 grid over the whole tile, scale max/255
+        float pm = 0.f;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) pm = fmaxf(pm, y[q]);
+        float* pb = pbuf + (t & 1) * 2 * kRows;
+        pb[h * kRows + r] = pm;
+        bar_red_and(1 + qd, 64, true);
+        const float pmax = fmaxf(pb[r], pb[kRows + r]);
         const float sp = pmax > 0.f ? __fdiv_rn(pmax, 255.f) : sp_prev;
         const float inv = pmax > 0.f ? __fdiv_rn(255.f, pmax) : 0.f;
 #pragma unroll
-        for (int q = 0; q < 64; ++q) x[q] = rintf(x[q] * inv);
+        for (int q = 0; q < 32; ++q) y[q] = rintf(y[q] * inv);
         corr = alpha * __fdiv_rn(sp_prev, sp);
         sp_prev = sp;
       }
-      uint32_t pk[32];
+      uint32_t pk[16];
 #pragma unroll
-      for (int q = 0; q < 32; ++q) pk[q] = pack_half2(x[2 * q], x[2 * q + 1]);
-      tmem_st32(sd, pk);
-      if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
-        // O holds PV up to tile j-1 once that MMA is done; rescale it in place
-        if (!(ok = c.warp_wait(B_PVDONE, (t - 1) & 1, 33))) break;
+      for (int q = 0; q < 16; ++q) pk[q] = pack_half2(y[2 * q], y[2 * q + 1]);
+      tmem_st16(sd + 16 * h, pk);
+      // O holds PV up to tile j-1 once that MMA is done; rescale this half in
+      // place.  A wait that runs out skips the rescale without leaving the
+      // loop: the error word then fails the next tile's pair barrier for both.
+      if (j > 0 && __any_sync(0xffffffffu, corr != 1.f) && c.warp_wait(B_PVDONE, (t - 1) & 1, 33)) {
         tc_fence_after();
 #pragma unroll 1
-        for (int cc = 0; cc < 8; ++cc) {
+        for (int cc = 0; cc < 4; ++cc) {
           uint32_t o[32];
-          tmem_ld32(c.tb + lane_off + kTmO + cc * 32, o);
+          const uint32_t oa = c.tb + lane_off + kTmO + 128 * h + cc * 32;
+          tmem_ld32(oa, o);
           tmem_wait_ld(o);
 #pragma unroll
           for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * corr);
-          tmem_st32(c.tb + lane_off + kTmO + cc * 32, o);
+          tmem_st32(oa, o);
         }
       }
       tmem_wait_st();
@@ -298,8 +333,8 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
     }
     if (!ok) break;
     tc += n;
-    l_rows[(k_unit & 1) * kRows + r] = l_run;
-    sp_rows[(k_unit & 1) * kRows + r] = sp_prev;
+    l_rows[(k_unit & 1) * 2 * kRows + h * kRows + r] = l_run;
+    if (h == 0) sp_rows[(k_unit & 1) * kRows + r] = sp_prev;
     __syncwarp();
     if (lane == 0) mbar_arrive(c.bar(B_STATS + (k_unit & 1)));
   }
@@ -322,8 +357,10 @@ __device__ __forceinline__ RowInfo row_info(const AttnParams& p, const Unit& un,
   return ri;
 }
 
-// Q per-row quantise into TMEM (step a1); returns s_q * sm_scale * log2(e).
-__device__ __forceinline__ float q_prologue(const AttnParams& p, const RowInfo& ri, uint32_t tq) {
+// First pass of the Q prologue: the row's absolute maximum.  It touches no
+// TMEM, so it runs before the previous unit's Q is released and leaves the
+// row in L1/L2 for the second pass.
+__device__ __forceinline__ float q_absmax(const AttnParams& p, const RowInfo& ri) {
   const uint4* src = reinterpret_cast<const uint4*>(p.q + ri.off);
   float absmax = 0.f;
   if (ri.valid) {
@@ -338,6 +375,13 @@ __device__ __forceinline__ float q_prologue(const AttnParams& p, const RowInfo& 
       }
     }
   }
+  return absmax;
+}
+
+// Second pass: Q per-row quantise into TMEM (step a1); returns
+// s_q * sm_scale * log2(e).
+__device__ __forceinline__ float q_prologue(const AttnParams& p, const RowInfo& ri, float absmax, uint32_t tq) {
+  const uint4* src = reinterpret_cast<const uint4*>(p.q + ri.off);
   float mul, s_q;
   if (p.q_mode == 1) {  // int8 grid, scale absmax/127, round half even
     mul = absmax > 0.f ? __fdiv_rn(127.f, absmax) : 0.f;
@@ -376,7 +420,7 @@ __device__ __forceinline__ bool epilogue(const AttnParams& p, const Ctx& c, cons
   if (!c.warp_wait(B_OFULL, k_unit & 1, 41)) return false;
   if (!c.warp_wait(B_STATS + (k_unit & 1), (k_unit >> 1) & 1, 42)) return false;
   tc_fence_after();
-  const float l = l_rows[(k_unit & 1) * kRows + r];
+  const float l = l_rows[(k_unit & 1) * 2 * kRows + r] + l_rows[(k_unit & 1) * 2 * kRows + kRows + r];
   const float sp = sp_rows[(k_unit & 1) * kRows + r];
   const float fin = l > 0.f ? (p.p_mode == 1 ? sp : 1.f) / l : 0.f;
   __nv_bfloat16* orow = p.out + ri.off;
@@ -405,12 +449,12 @@ __device__ __forceinline__ bool epilogue(const AttnParams& p, const Ctx& c, cons
 }
 
 __device__ __forceinline__ void role_correction(const AttnParams& p, const Ctx& c, uint8_t* sm) {
-  const int r = threadIdx.x - 256;
+  const int r = threadIdx.x - 384;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
   float* c_rows = reinterpret_cast<float*>(sm + kSmRows);
   const float* l_rows = c_rows + 2 * kRows;
-  const float* sp_rows = c_rows + 4 * kRows;
+  const float* sp_rows = c_rows + 6 * kRows;
   int k_unit = 0;
   bool ok = true;
   RowInfo prev{};
@@ -418,10 +462,11 @@ __device__ __forceinline__ void role_correction(const AttnParams& p, const Ctx& 
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
     const RowInfo ri = row_info(p, un, sg, r);
+    const float absmax = q_absmax(p, ri);
     // Q of this unit may replace the previous unit's once its last QK^T is done
     if (k_unit > 0 && !(ok = c.warp_wait(B_QEMPTY, (k_unit - 1) & 1, 40))) break;
     tc_fence_after();
-    c_rows[(k_unit & 1) * kRows + r] = q_prologue(p, ri, c.tb + lane_off + kTmQ);
+    c_rows[(k_unit & 1) * kRows + r] = q_prologue(p, ri, absmax, c.tb + lane_off + kTmQ);
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
@@ -453,15 +498,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(c.bar(B_SFULL + b), 1);
-      mbar_init(c.bar(B_PFULL + b), 4);
+      mbar_init(c.bar(B_PFULL + b), 8);
     }
     mbar_init(c.bar(B_PVDONE), 1);
     mbar_init(c.bar(B_QFULL), 4);
     mbar_init(c.bar(B_QEMPTY), 1);
     mbar_init(c.bar(B_OFULL), 1);
     mbar_init(c.bar(B_OEMPTY), 4);
-    mbar_init(c.bar(B_STATS), 4);
-    mbar_init(c.bar(B_STATS + 1), 4);
+    mbar_init(c.bar(B_STATS), 8);
+    mbar_init(c.bar(B_STATS + 1), 8);
     mbar_init(c.bar(B_STALL), 1);
     mbar_init(c.bar(B_DRAIN), 1);
     fence_mbar_init();
@@ -472,6 +517,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
+  // scale slots start at zero: columns past a tile's width then hold finite
+  // stale scales, which the softmax multiplies by p = 0
+  for (int i = threadIdx.x; i < kSlots * 128; i += kThreads) reinterpret_cast<float*>(sm + kSmScale)[i] = 0.f;
+  fence_proxy_async_shared();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -481,9 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((threadIdx.x & 31) == 0) role_producer(p, m, c);
   } else if (warp == 1) {
     if ((threadIdx.x & 31) == 0) role_mma(p, c);
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 12) {
     role_softmax(p, c, sm);
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     role_correction(p, c, sm);
   }
 
