@@ -46,10 +46,11 @@ constexpr int kSmRows = kSmScale + kSlots * 512;       // c[2][128], l[2][2][128
 constexpr int kSmXchg = kSmRows + 8 * kRows * 4;       // softmax pair exchange: 2 x [2][2][128] floats
 constexpr int kSmBars = kSmXchg + 8 * kRows * 4;
 enum : int {
-  B_KFULL = 0, B_KEMPTY = 3, B_VFULL = 6, B_VEMPTY = 9, B_SFULL = 12, B_PFULL = 14, B_PVDONE = 16,
-  B_QFULL = 17, B_QEMPTY = 18, B_OFULL = 19, B_OEMPTY = 20, B_STATS = 21 /* two, by unit parity */,
-  B_STALL = 23, B_DRAIN = 24, kNumBars = 25
+  B_KFULL = 0, B_KEMPTY = 3, B_VFULL = 6, B_VEMPTY = 9, B_SFULL = 12, B_PFULL = 14,
+  B_QFULL = 16, B_QEMPTY = 17, B_OFULL = 18, B_OEMPTY = 19, B_STATS = 20 /* two, by unit parity */,
+  B_STALL = 22, B_DRAIN = 23, kNumBars = 24
 };
+constexpr float kLift = 6.f;   // a unit's first reference sits 2^kLift above its first tile's max
 constexpr float kLazy = 14.f;  // the softmax reference moves when a row max grows by more than 2^kLazy;
                                // P' = p * v_scale * 2^-ev then stays below 2^14, inside the fp16 range
 constexpr int kSmTmemSlot = kSmBars + kNumBars * 8;
@@ -163,8 +164,7 @@ __device__ __forceinline__ void role_mma(const AttnParams& p, const Ctx& c) {
 #pragma unroll
         for (int s = 0; s < kHeadDim / 16; ++s)
           mma_ts(d, c.tb + kTmQ + 8 * s, kd0 + (uint64_t)(((s >> 2) * 8192 + (s & 3) * 32) >> 4), id, s > 0);
-        mma_commit(c.bar(B_SFULL + (t & 1)));
-        mma_commit(c.bar(B_KEMPTY + t % kSlots));
+        mma_commit(c.bar(B_SFULL + (t & 1)));  // also frees K slot t: the softmax passes it on
         if (j == n - 1) mma_commit(c.bar(B_QEMPTY));
       }
       if (j >= 1) {  // O (+)= P(j-1) V(j-1)
@@ -180,8 +180,7 @@ __device__ __forceinline__ void role_mma(const AttnParams& p, const Ctx& c) {
         const uint64_t vd0 = sdesc_k_sw128(vaddr);
         for (int s = 0; s < tg.nb; ++s)
           mma_ts(c.tb + kTmO, a + 8 * s, vd0 + (uint64_t)(2 * s), id_pv, (jj > 0 || s > 0) ? 1u : 0u);
-        mma_commit(c.bar(B_PVDONE));
-        mma_commit(c.bar(B_VEMPTY + t % kSlots));
+        mma_commit(c.bar(B_VEMPTY + t % kSlots));  // V slot t free; O holds PV up to tile t
         if (jj == n - 1) mma_commit(c.bar(B_OFULL));
       }
     }
@@ -231,6 +230,8 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
       // Every path through a tile passes the pair barrier the same number of
       // times, so a wait that runs out in one warp cannot strand its partner.
       bool okl = c.warp_wait(B_SFULL + (t & 1), (t >> 1) & 1, 31);
+      // S(t) complete means QK(t) has finished reading K slot t: hand it back
+      if (okl && threadIdx.x == 128) mbar_arrive(c.bar(B_KEMPTY + t % kSlots));
       okl = okl && c.warp_wait(B_VFULL + t % kSlots, (t / kSlots) & 1, 32);
       const uint32_t sd = c.tb + lane_off + kTmS + (t & 1) * kTileKeys;
       const uint32_t sc = c.sbase + kSmScale + (t % kSlots) * 512 + 128 * h;  // this half's ks; vs at +256
@@ -268,10 +269,12 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
           break;
         }
         const float mx = fmaxf(xb[r], xb[kRows + r]);
-        if (m_run == -INFINITY || mx > m_run + kLazy) {
-          const float mnew = fmaxf(m_run, mx);
-          alpha = m_run == -INFINITY ? 0.f : ex2_approx(m_run - mnew);
-          m_run = mnew;
+        if (m_run == -INFINITY) {
+          m_run = mx == -INFINITY ? mx : mx + kLift;  // alpha irrelevant: nothing accumulated yet
+          alpha = 0.f;
+        } else if (mx > m_run + kLazy) {
+          alpha = ex2_approx(m_run - mx);
+          m_run = mx;
         }
       }
       const float mref = m_run == -INFINITY ? 0.f : m_run + ev;
@@ -313,7 +316,8 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
       // O holds PV up to tile j-1 once that MMA is done; rescale this half in
       // place.  A wait that runs out skips the rescale without leaving the
       // loop: the error word then fails the next tile's pair barrier for both.
-      if (j > 0 && __any_sync(0xffffffffu, corr != 1.f) && c.warp_wait(B_PVDONE, (t - 1) & 1, 33)) {
+      if (j > 0 && __any_sync(0xffffffffu, corr != 1.f) &&
+          c.warp_wait(B_VEMPTY + (t - 1) % kSlots, ((t - 1) / kSlots) & 1, 33)) {
         tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
@@ -500,7 +504,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(c.bar(B_SFULL + b), 1);
       mbar_init(c.bar(B_PFULL + b), 8);
     }
-    mbar_init(c.bar(B_PVDONE), 1);
     mbar_init(c.bar(B_QFULL), 4);
     mbar_init(c.bar(B_QEMPTY), 1);
     mbar_init(c.bar(B_OFULL), 1);
