@@ -41,7 +41,7 @@ constexpr int kVTileBytes = kHeadDim * kTileKeys * 2;  // 32 KB: 256 dims x 128 
 // Shared memory, offsets from a 1024-byte aligned base.
 constexpr int kSmK = 0;
 constexpr int kSmV = kSmK + kSlots * kKTileBytes;
-constexpr int kSmScale = kSmV + kSlots * kVTileBytes;  // per V slot: ks[64] then vs[64]
+constexpr int kSmScale = kSmV + kSlots * kVTileBytes;  // per slot: ks[64] (K ring) then vs[64] (V ring)
 constexpr int kSmRows = kSmScale + kSlots * 512;       // c[2][128], l[2][2][128], sp[2][128] floats
 constexpr int kSmXchg = kSmRows + 8 * kRows * 4;       // softmax pair exchange: 2 x [2][2][128] floats
 constexpr int kSmBars = kSmXchg + 8 * kRows * 4;
@@ -108,9 +108,11 @@ __device__ __forceinline__ void role_producer(const AttnParams& p, const AttnMap
         const uint32_t ph = (kc / kSlots) & 1;
         if (!(ok = mbar_wait(c.bar(B_KEMPTY + s), ph ^ 1, c.wc, 10))) break;
         const uint32_t fb = c.bar(B_KFULL + s);
-        mbar_expect_tx(fb, kKTileBytes);
+        const uint32_t sbytes = (uint32_t)(tg.nb * kPage * 4);
+        mbar_expect_tx(fb, kKTileBytes + sbytes);
         const uint32_t dst = c.sbase + kSmK + s * kKTileBytes;
         for (int r = 0; r < 4; ++r) tma_load_3d(dst + r * 8192, &m.k, fb, r * 64, crow, un.g);
+        bulk_load(c.sbase + kSmScale + s * 512, p.ks + (size_t)un.g * p.n_tok_cap + crow, sbytes, fb);
         ++kc;
       }
       {
@@ -119,11 +121,9 @@ __device__ __forceinline__ void role_producer(const AttnParams& p, const AttnMap
         if (!(ok = mbar_wait(c.bar(B_VEMPTY + s), ph ^ 1, c.wc, 11))) break;
         const uint32_t fb = c.bar(B_VFULL + s);
         const uint32_t sbytes = (uint32_t)(tg.nb * kPage * 4);
-        mbar_expect_tx(fb, kVTileBytes + 2 * sbytes);
+        mbar_expect_tx(fb, kVTileBytes + sbytes);
         tma_load_3d(c.sbase + kSmV + s * kVTileBytes, &m.v, fb, crow, 0, un.g);
-        const size_t soff = (size_t)un.g * p.n_tok_cap + crow;
-        bulk_load(c.sbase + kSmScale + s * 512, p.ks + soff, sbytes, fb);
-        bulk_load(c.sbase + kSmScale + s * 512 + 256, p.vs + soff, sbytes, fb);
+        bulk_load(c.sbase + kSmScale + s * 512 + 256, p.vs + (size_t)un.g * p.n_tok_cap + crow, sbytes, fb);
         ++vc;
       }
     }
@@ -230,9 +230,10 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
       // Every path through a tile passes the pair barrier the same number of
       // times, so a wait that runs out in one warp cannot strand its partner.
       bool okl = c.warp_wait(B_SFULL + (t & 1), (t >> 1) & 1, 31);
-      // S(t) complete means QK(t) has finished reading K slot t: hand it back
-      if (okl && threadIdx.x == 128) mbar_arrive(c.bar(B_KEMPTY + t % kSlots));
-      okl = okl && c.warp_wait(B_VFULL + t % kSlots, (t / kSlots) & 1, 32);
+      // the K scales landed with K slot t, which QK(t) already consumed; wait on
+      // that slot's barrier too so this warp observes the copy itself (the
+      // phase cannot move on before this warp releases the slot below)
+      okl = okl && c.warp_wait(B_KFULL + t % kSlots, (t / kSlots) & 1, 34);
       const uint32_t sd = c.tb + lane_off + kTmS + (t & 1) * kTileKeys;
       const uint32_t sc = c.sbase + kSmScale + (t % kSlots) * 512 + 128 * h;  // this half's ks; vs at +256
       float y[32];
@@ -242,22 +243,39 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
         uint32_t sa[32];
         tmem_ld32(sd + 32 * h, sa);
         tmem_wait_ld(sa);
-        const uint32_t vis = (uint32_t)(visible_columns(tg, t_row, p.S, p.W) >> (32 * h));
         // y = S * k_scale (masked: -inf), and this half's row maximum
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (!tg.needs_mask && tg.nb == kTileBlocks) {  // full tile, every row sees every key
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 k4 = lds_f32x4(sc + 16 * q4);
-          const float kq[4] = {k4.x, k4.y, k4.z, k4.w};
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 k4 = lds_f32x4(sc + 16 * q4);
+            const float kq[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int q = 4 * q4 + e;
-            y[q] = ((vis >> q) & 1u) ? __uint_as_float(sa[q]) * kq[e] : -INFINITY;
-            m4[e] = fmaxf(m4[e], y[q]);
+            for (int e = 0; e < 4; ++e) {
+              const int q = 4 * q4 + e;
+              y[q] = __uint_as_float(sa[q]) * kq[e];
+              m4[e] = fmaxf(m4[e], y[q]);
+            }
+          }
+        } else {
+          const uint32_t vis = (uint32_t)(visible_columns(tg, t_row, p.S, p.W) >> (32 * h));
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 k4 = lds_f32x4(sc + 16 * q4);
+            const float kq[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int q = 4 * q4 + e;
+              y[q] = ((vis >> q) & 1u) ? __uint_as_float(sa[q]) * kq[e] : -INFINITY;
+              m4[e] = fmaxf(m4[e], y[q]);
+            }
           }
         }
         my = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c_row;  // log2 units
       }
+      // this warp is done with K slot t (QK(t) finished before S(t) was complete)
+      __syncwarp();
+      if (okl && lane == 0) mbar_arrive(c.bar(B_KEMPTY + t % kSlots));
       // the reference moves only when some row's max grew by more than 2^kLazy
       const bool grow = okl && (m_run == -INFINITY || my > m_run + kLazy);
       float alpha = 1.f;
@@ -278,6 +296,9 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
         }
       }
       const float mref = m_run == -INFINITY ? 0.f : m_run + ev;
+      // the V scales of tile t arrive with the V tile; a wait that runs out
+      // leaves the loop after the next group barrier, like the others
+      if (!c.warp_wait(B_VFULL + t % kSlots, (t / kSlots) & 1, 32)) okl = false;
       // p = 2^(y c - mref); P' = p * v_scale (V scale folded into P)
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -496,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(c.bar(B_KFULL + s), 1);
-      mbar_init(c.bar(B_KEMPTY + s), 1);
+      mbar_init(c.bar(B_KEMPTY + s), 8);  // every softmax warp, after reading the K scales
       mbar_init(c.bar(B_VFULL + s), 1);
       mbar_init(c.bar(B_VEMPTY + s), 1);
     }

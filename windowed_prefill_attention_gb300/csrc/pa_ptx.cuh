@@ -306,6 +306,10 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[16]) {
   asm volatile("" : PA_RW8(0), PA_RW8(8) : : "memory");
 }
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), PA_W8(0)
+               : "memory");
+}
 #undef PA_RW8
 #undef PA_R8
 #undef PA_W8
