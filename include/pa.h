@@ -58,7 +58,7 @@ extern "C" {
 #define PA_ENOSCRATCH (-7) /* pa_prefill_noalloc: the call needs more than PA_NOALLOC_SCRATCH_BYTES */
 
 /* Query container (step "Q per-row quantise", fused into the kernel prologue). */
-#define PA_Q_F16 0   /* default: per-row power-of-two scale into fp16 (lossless for bf16 input) */
+#define PA_Q_BF16 0  /* default: Q's bf16 values enter the MMA unchanged (no rounding; s_q = 1) */
 #define PA_Q_INT8 1  /* the pages' grid: scale absmax/127, codes rint(q*127/absmax) in [-127,127] */
 /* P container (step "V scale folded into P, P quantised per row"). */
 #define PA_P_F16 0   /* default: P' = p * v_scale rounded to fp16 (11-bit significand) */
@@ -67,7 +67,7 @@ extern "C" {
 typedef struct pa_ctx* pa_handle;
 
 typedef struct {
-  int q_mode;           /* PA_Q_F16 | PA_Q_INT8 */
+  int q_mode;           /* PA_Q_BF16 | PA_Q_INT8 */
   int p_mode;           /* PA_P_F16 | PA_P_U8 */
   int wait_timeout_ms;  /* bound on every device-side wait (default 2000) */
   int record_timing;    /* nonzero: time each launch with CUDA events (pa_timing) */

@@ -24,7 +24,7 @@ _lib = C.CDLL(_LIB_PATH)
 
 PA_OK, PA_EINVAL, PA_EARCH, PA_ECUDA, PA_ETIMEOUT, PA_EBADPAGE, PA_ENOMEM, PA_ENOSCRATCH = 0, -1, -2, -3, -4, -5, -6, -7
 PA_NOALLOC_SCRATCH_BYTES = 32 << 20
-PA_Q_F16, PA_Q_INT8 = 0, 1
+PA_Q_BF16, PA_Q_INT8 = 0, 1
 PA_P_F16, PA_P_U8 = 0, 1
 
 EXPORTED = ("pa_default_options", "pa_create", "pa_destroy", "pa_prefill", "pa_prefill_batch", "pa_prefill_host",
@@ -124,7 +124,7 @@ def pa_default_options() -> pa_options:
 
 
 def pa_create(n_q_heads, n_kv_heads, n_pool_pages, max_pages_per_seq, head_dim=256, page_size=16,
-              q_mode=PA_Q_F16, p_mode=PA_P_F16, wait_timeout_ms=2000, record_timing=False, debug_stall=False):
+              q_mode=PA_Q_BF16, p_mode=PA_P_F16, wait_timeout_ms=2000, record_timing=False, debug_stall=False):
     o = pa_options(q_mode, p_mode, wait_timeout_ms, 1 if record_timing else 0, 1 if debug_stall else 0)
     h = C.c_void_p()
     _check(_lib.pa_create(C.byref(h), n_q_heads, n_kv_heads, head_dim, page_size, n_pool_pages, max_pages_per_seq,

@@ -97,7 +97,7 @@ struct pa_ctx {
   int device = 0, n_sm = 0;
 
   // workspace
-  __half* kw = nullptr;
+  __nv_bfloat16* kw = nullptr;
   __half* vt = nullptr;
   float* ks = nullptr;
   float* vs = nullptr;
@@ -223,7 +223,7 @@ int prepare(pa_handle h, int n_seq, const pa_seq* seqs, int S, int W, cudaStream
     h->vs = nullptr;
     h->n_tok_cap = 0;
     h->kv_ptr = nullptr;
-    PA_CUDA(cudaMalloc(&h->kw, cap * h->HKV * kHeadDim * sizeof(__half)));
+    PA_CUDA(cudaMalloc(&h->kw, cap * h->HKV * kHeadDim * sizeof(__nv_bfloat16)));
     PA_CUDA(cudaMalloc(&h->vt, cap * h->HKV * kHeadDim * sizeof(__half)));
     PA_CUDA(cudaMalloc(&h->ks, cap * h->HKV * sizeof(float)));
     PA_CUDA(cudaMalloc(&h->vs, cap * h->HKV * sizeof(float)));
@@ -310,7 +310,7 @@ int run(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t*
     const uint64_t kd[3] = {(uint64_t)kHeadDim, (uint64_t)P.n_tok_total, (uint64_t)h->HKV};
     const uint64_t kst[2] = {(uint64_t)kHeadDim * 2, (uint64_t)h->n_tok_cap * kHeadDim * 2};
     const uint32_t kbox[3] = {64, (uint32_t)kTileKeys, 1};
-    if ((rc = encode(&h->maps.k, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, h->kw, kd, kst, kbox,
+    if ((rc = encode(&h->maps.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, h->kw, kd, kst, kbox,
                      CU_TENSOR_MAP_SWIZZLE_128B)))
       return rc;
     const uint64_t vd[3] = {(uint64_t)P.n_tok_total, (uint64_t)kHeadDim, (uint64_t)h->HKV};
@@ -374,7 +374,7 @@ extern "C" {
 
 void pa_default_options(pa_options* opt) {
   if (!opt) return;
-  opt->q_mode = PA_Q_F16;
+  opt->q_mode = PA_Q_BF16;
   opt->p_mode = PA_P_F16;
   opt->wait_timeout_ms = 2000;
   opt->record_timing = 0;
@@ -407,7 +407,7 @@ int pa_create(pa_handle* out, int n_q_heads, int n_kv_heads, int head_dim, int p
   pa_options o;
   pa_default_options(&o);
   if (opt) o = *opt;
-  if ((o.q_mode != PA_Q_F16 && o.q_mode != PA_Q_INT8) || (o.p_mode != PA_P_F16 && o.p_mode != PA_P_U8) ||
+  if ((o.q_mode != PA_Q_BF16 && o.q_mode != PA_Q_INT8) || (o.p_mode != PA_P_F16 && o.p_mode != PA_P_U8) ||
       o.wait_timeout_ms <= 0)
     return PA_EINVAL;
   int dev = 0;

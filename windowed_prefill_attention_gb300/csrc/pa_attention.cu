@@ -44,12 +44,17 @@ constexpr int kSmV = kSmK + kSlots * kKTileBytes;
 constexpr int kSmScale = kSmV + kSlots * kVTileBytes;  // per slot: ks[64] (K ring) then vs[64] (V ring)
 constexpr int kSmRows = kSmScale + kSlots * 512;       // c[2][128], l[2][2][128], sp[2][128] floats
 constexpr int kSmXchg = kSmRows + 8 * kRows * 4;       // softmax pair exchange: 2 x [2][2][128] floats
-constexpr int kSmBars = kSmXchg + 8 * kRows * 4;
+constexpr int kSmStage = kSmXchg + 8 * kRows * 4;      // correction warps: 4 x [32 rows][128 B]
+constexpr int kSmBars = kSmStage + 4 * 4096;
 enum : int {
   B_KFULL = 0, B_KEMPTY = 3, B_VFULL = 6, B_VEMPTY = 9, B_SFULL = 12, B_PFULL = 14,
   B_QFULL = 16, B_QEMPTY = 17, B_OFULL = 18, B_OEMPTY = 19, B_STATS = 20 /* two, by unit parity */,
-  B_STALL = 22, B_DRAIN = 23, kNumBars = 24
+  B_STALL = 22, B_DRAIN = 23, B_QSOON = 24, kNumBars = 25
 };
+// The MMA issuer arrives on B_QSOON when it issues QK^T for the tile kQSoon
+// tiles before its unit's last; the correction warps then start loading the
+// next unit's Q rows, so that they are in L2 when the unit's Q may be stored.
+constexpr int kQSoon = 6;
 constexpr float kLift = 6.f;   // a unit's first reference sits 2^kLift above its first tile's max
 constexpr float kLazy = 14.f;  // the softmax reference moves when a row max grows by more than 2^kLazy;
                                // P' = p * v_scale * 2^-ev then stays below 2^14, inside the fp16 range
@@ -148,42 +153,54 @@ __device__ __forceinline__ void role_mma(const AttnParams& p, const Ctx& c) {
     const UnitGeom ug = unit_geom(un.t0, p.TQ, sg, p.S, p.W);
     const int n = ug.n_tiles;
     if (!(ok = mbar_wait(p.debug_stall ? c.bar(B_STALL) : c.bar(B_QFULL), k_unit & 1, c.wc, 20))) break;
-    tc_fence_after();
-    for (int j = 0; j <= n && ok; ++j) {
+    // Operands of the next QK^T.  They are prepared (K slot waited for,
+    // descriptors built) right after the previous QK^T is issued, so that
+    // PV(j-1) is followed at once by QK^T(j+1).
+    uint32_t qk_d = 0, qk_id = 0;
+    uint64_t qk_kd0 = 0;
+    auto prep_qk = [&](int j) -> bool {
+      const uint32_t t = tc + j;
+      const uint32_t slot = t % kSlots;
+      if (!mbar_wait(c.bar(B_KFULL + slot), (t / kSlots) & 1, c.wc, 21)) return false;
+      qk_d = c.tb + kTmS + (t & 1) * kTileKeys;
+      qk_id = idesc_f16(kRows, tile_width(ug, j) * kPage, true, true);  // bf16 Q, bf16 K codes
+      qk_kd0 = sdesc_k_sw128(c.sbase + kSmK + slot * kKTileBytes);
+      return true;
+    };
+    if (!(ok = prep_qk(0))) break;
+    for (int j = 0; j <= n; ++j) {
       if (j < n) {  // S(j) = Q K(j)^T
         const uint32_t t = tc + j;
-        const TileGeom tg = tile_geom(ug, j, p.S, p.W);
-        if (!(ok = mbar_wait(c.bar(B_KFULL + t % kSlots), (t / kSlots) & 1, c.wc, 21))) break;
         tc_fence_after();
-        const uint32_t kaddr = c.sbase + kSmK + (t % kSlots) * kKTileBytes;
-        const uint32_t d = c.tb + kTmS + (t & 1) * kTileKeys;
-        const uint32_t id = idesc_f16(kRows, tg.nb * kPage, false, false);
-        // k-step s reads K bytes at kaddr + (s/4)*8192 + (s%4)*32: only the
-        // descriptor's start-address field (address >> 4) moves
-        const uint64_t kd0 = sdesc_k_sw128(kaddr);
+        // k-step s reads K bytes at (s/4)*8192 + (s%4)*32 from the slot: only
+        // the descriptor's start-address field (address >> 4) moves
 #pragma unroll
         for (int s = 0; s < kHeadDim / 16; ++s)
-          mma_ts(d, c.tb + kTmQ + 8 * s, kd0 + (uint64_t)(((s >> 2) * 8192 + (s & 3) * 32) >> 4), id, s > 0);
+          mma_ts(qk_d, c.tb + kTmQ + 8 * s, qk_kd0 + (uint64_t)(((s >> 2) * 8192 + (s & 3) * 32) >> 4), qk_id, s > 0);
         mma_commit(c.bar(B_SFULL + (t & 1)));  // also frees K slot t: the softmax passes it on
         if (j == n - 1) mma_commit(c.bar(B_QEMPTY));
+        if (j == imax(0, n - kQSoon)) mbar_arrive(c.bar(B_QSOON));
+        if (j + 1 < n && !(ok = prep_qk(j + 1))) break;
       }
       if (j >= 1) {  // O (+)= P(j-1) V(j-1)
         const int jj = j - 1;
         const uint32_t t = tc + jj;
-        const TileGeom tg = tile_geom(ug, jj, p.S, p.W);
+        // V(t) has landed: every softmax warp waited for its barrier (for the
+        // V scales) before releasing P(t)
         if (!(ok = mbar_wait(c.bar(B_PFULL + (t & 1)), (t >> 1) & 1, c.wc, 22))) break;
-        if (!(ok = mbar_wait(c.bar(B_VFULL + t % kSlots), (t / kSlots) & 1, c.wc, 23))) break;
         if (jj == 0 && k_unit > 0 && !(ok = mbar_wait(c.bar(B_OEMPTY), (k_unit - 1) & 1, c.wc, 24))) break;
         tc_fence_after();
-        const uint32_t vaddr = c.sbase + kSmV + (t % kSlots) * kVTileBytes;
+        const uint32_t slot = t % kSlots;
         const uint32_t a = c.tb + kTmS + (t & 1) * kTileKeys;
-        const uint64_t vd0 = sdesc_k_sw128(vaddr);
-        for (int s = 0; s < tg.nb; ++s)
+        const uint64_t vd0 = sdesc_k_sw128(c.sbase + kSmV + slot * kVTileBytes);
+        const int nb = tile_width(ug, jj);
+        for (int s = 0; s < nb; ++s)
           mma_ts(c.tb + kTmO, a + 8 * s, vd0 + (uint64_t)(2 * s), id_pv, (jj > 0 || s > 0) ? 1u : 0u);
-        mma_commit(c.bar(B_VEMPTY + t % kSlots));  // V slot t free; O holds PV up to tile t
+        mma_commit(c.bar(B_VEMPTY + slot));  // V slot t free; O holds PV up to tile t
         if (jj == n - 1) mma_commit(c.bar(B_OFULL));
       }
     }
+    if (!ok) break;
     tc += n;
   }
   // every issued MMA completes before TMEM is freed
@@ -235,7 +252,9 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
       // phase cannot move on before this warp releases the slot below)
       okl = okl && c.warp_wait(B_KFULL + t % kSlots, (t / kSlots) & 1, 34);
       const uint32_t sd = c.tb + lane_off + kTmS + (t & 1) * kTileKeys;
-      const uint32_t sc = c.sbase + kSmScale + (t % kSlots) * 512 + 128 * h;  // this half's ks; vs at +256
+      // this half's K scales (32 floats); its V scales follow 256 bytes later
+      const float4* ks4 = reinterpret_cast<const float4*>(sm + kSmScale + (t % kSlots) * 512 + 128 * h);
+      const float4* vs4 = ks4 + 16;
       float y[32];
       float my = -INFINITY;
       if (okl) {
@@ -248,7 +267,7 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
         if (!tg.needs_mask && tg.nb == kTileBlocks) {  // full tile, every row sees every key
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
-            const float4 k4 = lds_f32x4(sc + 16 * q4);
+            const float4 k4 = ks4[q4];
             const float kq[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -261,7 +280,7 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
           const uint32_t vis = (uint32_t)(visible_columns(tg, t_row, p.S, p.W) >> (32 * h));
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
-            const float4 k4 = lds_f32x4(sc + 16 * q4);
+            const float4 k4 = ks4[q4];
             const float kq[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -303,7 +322,7 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int q4 = 0; q4 < 8; ++q4) {
-        const float4 v4 = lds_f32x4(sc + 256 + 16 * q4);
+        const float4 v4 = vs4[q4];
         const float vq[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -368,23 +387,48 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
 
 // ------------------------------------------------------------------ prologue / epilogue
 struct RowInfo {
-  int t_row, h_row;
   bool valid;
   size_t off;  // element offset of the row in q / out
 };
 
 __device__ __forceinline__ RowInfo row_info(const AttnParams& p, const Unit& un, const SeqGeom& sg, int r) {
   RowInfo ri;
-  ri.t_row = un.t0 + r / p.G;
-  ri.h_row = un.g * p.G + r % p.G;
-  ri.valid = ri.t_row >= sg.q_start && ri.t_row < sg.q_start + sg.n_q;
-  ri.off = ri.valid ? ((size_t)(sg.q_off + ri.t_row - sg.q_start) * p.HQ + ri.h_row) * kHeadDim : 0;
+  const int t_row = un.t0 + r / p.G;
+  const int h_row = un.g * p.G + r % p.G;
+  ri.valid = t_row >= sg.q_start && t_row < sg.q_start + sg.n_q;
+  ri.off = ri.valid ? ((size_t)(sg.q_off + t_row - sg.q_start) * p.HQ + h_row) * kHeadDim : 0;
   return ri;
 }
 
-// First pass of the Q prologue: the row's absolute maximum.  It touches no
-// TMEM, so it runs before the previous unit's Q is released and leaves the
-// row in L1/L2 for the second pass.
+// Row-major global traffic of the correction warps goes through shared
+// memory, 32 rows x 128 bytes per warp, so that one warp instruction moves
+// four whole 128-byte lines (lane l: row 4k + l/8, 16-byte piece l%8) while
+// the TMEM side keeps one row per thread.  Piece p of row i is kept at piece
+// p ^ (i & 7), which makes both access patterns free of bank conflicts.
+__device__ __forceinline__ uint4* stage_at(uint8_t* stage, int row, int piece) {
+  return reinterpret_cast<uint4*>(stage + row * 128 + ((piece ^ (row & 7)) << 4));
+}
+
+// The rows lane `lane` moves in the four-rows-per-instruction pattern:
+// row 4k + lane/8 of the warp's 32, k = 0..7.
+struct LaneRows {
+  uint32_t row[8];  // row index in q / out (element offset row * 256)
+  uint32_t valid;   // bit k: row k is a query row of the call
+};
+__device__ __forceinline__ LaneRows lane_rows(const AttnParams& p, const Unit& un, const SeqGeom& sg, int qd,
+                                              int lane) {
+  LaneRows lr;
+  lr.valid = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const RowInfo ri = row_info(p, un, sg, 32 * qd + 4 * k + (lane >> 3));
+    lr.row[k] = (uint32_t)(ri.off / kHeadDim);
+    lr.valid |= (ri.valid ? 1u : 0u) << k;
+  }
+  return lr;
+}
+
+// The row's absolute maximum, for the int8 grid only.
 __device__ __forceinline__ float q_absmax(const AttnParams& p, const RowInfo& ri) {
   const uint4* src = reinterpret_cast<const uint4*>(p.q + ri.off);
   float absmax = 0.f;
@@ -403,103 +447,167 @@ __device__ __forceinline__ float q_absmax(const AttnParams& p, const RowInfo& ri
   return absmax;
 }
 
-// Second pass: Q per-row quantise into TMEM (step a1); returns
-// s_q * sm_scale * log2(e).
-__device__ __forceinline__ float q_prologue(const AttnParams& p, const RowInfo& ri, float absmax, uint32_t tq) {
-  const uint4* src = reinterpret_cast<const uint4*>(p.q + ri.off);
-  float mul, s_q;
-  if (p.q_mode == 1) {  // int8 grid, scale absmax/127, round half even
+// Eight bf16 values -> their int8-grid codes rint(x * mul) clamped to
+// [-127, 127], as bf16 (exact), same positions.
+__device__ __forceinline__ uint4 quantise8(uint4 v, float mul) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float a = fminf(127.f, fmaxf(-127.f, rintf(__uint_as_float(w[e] << 16) * mul)));
+    const float b = fminf(127.f, fmaxf(-127.f, rintf(__uint_as_float(w[e] & 0xffff0000u) * mul)));
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    w[e] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Q per-row quantise into TMEM (step a1); returns s_q * sm_scale * log2(e).
+// PA_Q_BF16: Q's bf16 bits go to TMEM unchanged, s_q = 1.  PA_Q_INT8: codes
+// on the pages' grid, s_q = absmax / 127.  64 columns of every row per round;
+// the loads of the next round are in flight while one round is stored.
+template <bool kInt8>
+__device__ __forceinline__ float q_prologue(const AttnParams& p, const LaneRows& lr, float absmax, uint8_t* stage,
+                                            uint32_t tq, int lane) {
+  float s_q = 1.f, mul = 1.f;
+  if (kInt8) {
     mul = absmax > 0.f ? __fdiv_rn(127.f, absmax) : 0.f;
     s_q = __fdiv_rn(absmax, 127.f);
-  } else {  // lossless fp16 container: power-of-two scale, absmax in [64, 128)
-    const int k = absmax > 0.f ? imin(127, 133 - (int)((__float_as_uint(absmax) >> 23) & 0xff)) : 0;
-    mul = __uint_as_float((uint32_t)(127 + k) << 23);
-    s_q = __uint_as_float((uint32_t)(127 - k) << 23);
   }
-#pragma unroll 1
-  for (int cc = 0; cc < 4; ++cc) {
+  float mk[8];  // the scale of each row this lane loads
+  if (kInt8) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mk[k] = __shfl_sync(0xffffffffu, mul, 4 * k + (lane >> 3));
+  }
+  const int pc = lane & 7;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  uint4 v[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    v[k] = (lr.valid >> k) & 1u ? __ldg(reinterpret_cast<const uint4*>(p.q + (size_t)lr.row[k] * kHeadDim) + pc) : zero;
+#pragma unroll
+  for (int cb = 0; cb < 4; ++cb) {
+    uint4 vn[8];
+    if (cb < 3) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        vn[k] = (lr.valid >> k) & 1u
+                    ? __ldg(reinterpret_cast<const uint4*>(p.q + (size_t)lr.row[k] * kHeadDim + (cb + 1) * 64) + pc)
+                    : zero;
+    }
+    if (kInt8) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = quantise8(v[k], mk[k]);
+    }
+    __syncwarp();  // the previous round's reads of the stage are done
+#pragma unroll
+    for (int k = 0; k < 8; ++k) *stage_at(stage, 4 * k + (lane >> 3), pc) = v[k];
+    __syncwarp();
     uint32_t pk[32];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint4 v = ri.valid ? __ldg(src + cc * 8 + k) : make_uint4(0, 0, 0, 0);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float a = __uint_as_float(w[e] << 16) * mul;
-        float b = __uint_as_float(w[e] & 0xffff0000u) * mul;
-        if (p.q_mode == 1) {
-          a = fminf(127.f, fmaxf(-127.f, rintf(a)));
-          b = fminf(127.f, fmaxf(-127.f, rintf(b)));
-        }
-        pk[k * 4 + e] = pack_half2(a, b);
-      }
+    for (int pp = 0; pp < 8; ++pp) {
+      const uint4 u = *stage_at(stage, lane, pp);
+      pk[4 * pp] = u.x;
+      pk[4 * pp + 1] = u.y;
+      pk[4 * pp + 2] = u.z;
+      pk[4 * pp + 3] = u.w;
     }
-    tmem_st32(tq + cc * 32, pk);
+    tmem_st32(tq + cb * 32, pk);
+    if (cb < 3) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = vn[k];
+    }
   }
   return s_q * p.sm_scale_log2;
 }
 
-// out = O / l (x s_p on the u8 grid) -> bf16 (step a8).
-__device__ __forceinline__ bool epilogue(const AttnParams& p, const Ctx& c, const RowInfo& ri, int k_unit,
-                                         uint32_t to, const float* l_rows, const float* sp_rows, int r) {
+// out = O / l (x s_p on the u8 grid) -> bf16 (step a8), 64 columns per round.
+// O may be overwritten once the last round's TMEM loads are done, so the
+// MMA issuer is released before the last stores.
+__device__ __forceinline__ bool epilogue(const AttnParams& p, const Ctx& c, const LaneRows& lr, int k_unit,
+                                         uint32_t to, const float* l_rows, const float* sp_rows, int r,
+                                         uint8_t* stage, int lane) {
   if (!c.warp_wait(B_OFULL, k_unit & 1, 41)) return false;
   if (!c.warp_wait(B_STATS + (k_unit & 1), (k_unit >> 1) & 1, 42)) return false;
   tc_fence_after();
   const float l = l_rows[(k_unit & 1) * 2 * kRows + r] + l_rows[(k_unit & 1) * 2 * kRows + kRows + r];
   const float sp = sp_rows[(k_unit & 1) * kRows + r];
   const float fin = l > 0.f ? (p.p_mode == 1 ? sp : 1.f) / l : 0.f;
-  __nv_bfloat16* orow = p.out + ri.off;
+  const int pc = lane & 7;
 #pragma unroll 1
-  for (int cc = 0; cc < 8; ++cc) {
-    uint32_t o[32];
-    tmem_ld32(to + cc * 32, o);
-    tmem_wait_ld(o);
-    if (ri.valid) {
-      uint32_t w[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        __nv_bfloat162 v =
-            __floats2bfloat162_rn(__uint_as_float(o[2 * q]) * fin, __uint_as_float(o[2 * q + 1]) * fin);
-        w[q] = *reinterpret_cast<uint32_t*>(&v);
-      }
-      uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  for (int cb = 0; cb < 4; ++cb) {
+    uint32_t o0[32], o1[32];
+    tmem_ld32(to + cb * 64, o0);
+    tmem_ld32(to + cb * 64 + 32, o1);
+    tmem_wait_ld(o0);
+    reg_fence(o1);
+    if (cb == 3) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(B_OEMPTY));
     }
+    uint32_t w[32];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      __nv_bfloat162 a = __floats2bfloat162_rn(__uint_as_float(o0[2 * q]) * fin, __uint_as_float(o0[2 * q + 1]) * fin);
+      __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(o1[2 * q]) * fin, __uint_as_float(o1[2 * q + 1]) * fin);
+      w[q] = *reinterpret_cast<uint32_t*>(&a);
+      w[16 + q] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    __syncwarp();  // the previous round's reads of the stage are done
+#pragma unroll
+    for (int pp = 0; pp < 8; ++pp) *stage_at(stage, lane, pp) = make_uint4(w[4 * pp], w[4 * pp + 1], w[4 * pp + 2], w[4 * pp + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if ((lr.valid >> k) & 1u)
+        *(reinterpret_cast<uint4*>(p.out + (size_t)lr.row[k] * kHeadDim + cb * 64) + pc) =
+            *stage_at(stage, 4 * k + (lane >> 3), pc);
   }
-  tc_fence_before();
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(c.bar(B_OEMPTY));
   return true;
 }
 
 __device__ __forceinline__ void role_correction(const AttnParams& p, const Ctx& c, uint8_t* sm) {
   const int r = threadIdx.x - 384;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+  const int qd = warp & 3;
+  const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+  uint8_t* stage = sm + kSmStage + qd * 4096;
   float* c_rows = reinterpret_cast<float*>(sm + kSmRows);
   const float* l_rows = c_rows + 2 * kRows;
   const float* sp_rows = c_rows + 6 * kRows;
   int k_unit = 0;
   bool ok = true;
-  RowInfo prev{};
+  Unit prev_un{};
+  SeqGeom prev_sg{};
   for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++k_unit) {
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
     const RowInfo ri = row_info(p, un, sg, r);
-    const float absmax = q_absmax(p, ri);
+    // fetch this unit's Q rows only when the previous unit is close to its
+    // end: fetched earlier, they would be evicted from L2 before use
+    if (k_unit > 0 && !(ok = c.warp_wait(B_QSOON, (k_unit - 1) & 1, 43))) break;
+    if (ri.valid) bulk_prefetch_l2(p.q + ri.off, kHeadDim * 2);
+    const float absmax = p.q_mode == 1 ? q_absmax(p, ri) : 0.f;
+    const LaneRows lr = lane_rows(p, un, sg, qd, lane);
     // Q of this unit may replace the previous unit's once its last QK^T is done
     if (k_unit > 0 && !(ok = c.warp_wait(B_QEMPTY, (k_unit - 1) & 1, 40))) break;
     tc_fence_after();
-    c_rows[(k_unit & 1) * kRows + r] = q_prologue(p, ri, absmax, c.tb + lane_off + kTmQ);
+    const uint32_t tq = c.tb + lane_off + kTmQ;
+    c_rows[(k_unit & 1) * kRows + r] =
+        p.q_mode == 1 ? q_prologue<true>(p, lr, absmax, stage, tq, lane) : q_prologue<false>(p, lr, absmax, stage, tq, lane);
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(c.bar(B_QFULL));
-    if (k_unit > 0) ok = epilogue(p, c, prev, k_unit - 1, c.tb + lane_off + kTmO, l_rows, sp_rows, r);
-    prev = ri;
+    if (k_unit > 0)
+      ok = epilogue(p, c, lane_rows(p, prev_un, prev_sg, qd, lane), k_unit - 1, c.tb + lane_off + kTmO, l_rows,
+                    sp_rows, r, stage, lane);
+    prev_un = un;
+    prev_sg = sg;
   }
-  if (ok && k_unit > 0) (void)epilogue(p, c, prev, k_unit - 1, c.tb + lane_off + kTmO, l_rows, sp_rows, r);
+  if (ok && k_unit > 0)
+    (void)epilogue(p, c, lane_rows(p, prev_un, prev_sg, qd, lane), k_unit - 1, c.tb + lane_off + kTmO, l_rows,
+                   sp_rows, r, stage, lane);
   tmem_wait_st();
 }
 
@@ -533,6 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(c.bar(B_STATS + 1), 8);
     mbar_init(c.bar(B_STALL), 1);
     mbar_init(c.bar(B_DRAIN), 1);
+    mbar_init(c.bar(B_QSOON), 1);
     fence_mbar_init();
     tma_prefetch_map(&m.k);
     tma_prefetch_map(&m.v);

@@ -34,7 +34,7 @@ struct WidenParams {
   int n_seq;
   int n_stored_blocks;        // sum over sequences of SeqGeom::n_blocks
   int n_tok_cap;              // row stride of the widened buffers
-  __half* kw;                 // [HKV][n_tok_cap][256]   integer-valued fp16 K codes
+  __nv_bfloat16* kw;          // [HKV][n_tok_cap][256]   integer-valued bf16 K codes
   __half* vt;                 // [HKV][256][n_tok_cap]   integer-valued fp16 V codes, transposed
   float* ks;                  // [HKV][n_tok_cap]        per-token K scale
   float* vs;                  // [HKV][n_tok_cap]        per-token V scale

@@ -2,14 +2,15 @@
 // pool (sm_103a):
 //
 //   widen_kernel      page gather through the block table: int8 K/V pages ->
-//                     contiguous integer-valued fp16 copies (K row-major, V
-//                     transposed) plus per-token scales, visible blocks only.
+//                     contiguous integer-valued copies (K row-major in bf16, V
+//                     transposed in fp16) plus per-token scales, visible blocks only.
 //   debug kernels     exports of the gather and of the mask set for the tests,
 //                     built on the same geometry helpers as the attention kernel.
 //
 // sm_103a has no integer tcgen05 MMA, so the int8 codes are widened once per
-// call into fp16 containers (exact: |code| <= 127) that the attention kernel
-// (pa_attention.cu) feeds to tcgen05.mma kind::f16.
+// call into 16-bit float containers (exact: |code| <= 127) that the attention
+// kernel (pa_attention.cu) feeds to tcgen05.mma kind::f16: K in bf16, the type
+// of Q, and V in fp16, the type of P'.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -52,9 +53,9 @@ __global__ void __launch_bounds__(kWidenThreads) widen_kernel(const WidenParams 
     if (tk < n_valid)
       raw = *reinterpret_cast<const int4*>(p.k_pool + page_base + ((size_t)tk * HKV + g) * kHeadDim + c * 16);
     const int8_t* cb = reinterpret_cast<const int8_t*>(&raw);
-    __align__(16) __half h[16];
+    __align__(16) __nv_bfloat16 h[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) h[e] = __int2half_rn((int)cb[e]);
+    for (int e = 0; e < 16; ++e) h[e] = __int2bfloat16_rn((int)cb[e]);
     int4* dst = reinterpret_cast<int4*>(p.kw + ((size_t)g * p.n_tok_cap + row0 + tk) * kHeadDim + c * 16);
     dst[0] = reinterpret_cast<const int4*>(h)[0];
     dst[1] = reinterpret_cast<const int4*>(h)[1];
@@ -112,7 +113,7 @@ __global__ void debug_gather_kernel(const WidenParams p, int seq, int8_t* k_out,
     for (int gd = threadIdx.x; gd < p.HKV * kHeadDim; gd += blockDim.x) {
       const int g = gd / kHeadDim, d = gd % kHeadDim;
       k_out[((size_t)g * n_rows + rr) * kHeadDim + d] =
-          (int8_t)__half2int_rn(p.kw[((size_t)g * p.n_tok_cap + row) * kHeadDim + d]);
+          (int8_t)__bfloat162int_rn(p.kw[((size_t)g * p.n_tok_cap + row) * kHeadDim + d]);
       v_out[((size_t)g * n_rows + rr) * kHeadDim + d] =
           (int8_t)__half2int_rn(p.vt[((size_t)g * kHeadDim + d) * p.n_tok_cap + row]);
     }

@@ -134,7 +134,7 @@ extern "C" int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_page
   const int t_first = (q_start / TQ) * TQ;
   const int n_t0 = (q_start + n_q - 1 - t_first) / TQ + 1;
   // size limits of the static scratch: a clear error, never an overflow
-  const long long row_bytes = (long long)n_kv_heads * (2 * kHeadDim * (long long)sizeof(__half) + 2 * sizeof(float));
+  const long long row_bytes = (long long)n_kv_heads * (2 * kHeadDim * 2LL + 2 * sizeof(float));  // bf16 K + fp16 V^T, two scales
   const long long cap_rows = ((long long)PA_NOALLOC_SCRATCH_BYTES - (long long)kWidenedOffset) / row_bytes / 64 * 64;
   if (n_rows > cap_rows || (long long)n_t0 * n_kv_heads > kMaxUnits) return PA_ENOSCRATCH;
 
@@ -154,16 +154,16 @@ extern "C" int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_page
   SeqGeom* seq_dev = reinterpret_cast<SeqGeom*>(base + 512);
   Unit* units = reinterpret_cast<Unit*>(base + kHeaderBytes);
   unsigned char* w = base + kWidenedOffset;
-  __half* kw = reinterpret_cast<__half*>(w);
-  w += (size_t)n_kv_heads * cap * kHeadDim * sizeof(__half);
+  __nv_bfloat16* kw = reinterpret_cast<__nv_bfloat16*>(w);
+  w += (size_t)n_kv_heads * cap * kHeadDim * 2;
   __half* vt = reinterpret_cast<__half*>(w);
-  w += (size_t)n_kv_heads * cap * kHeadDim * sizeof(__half);
+  w += (size_t)n_kv_heads * cap * kHeadDim * 2;
   float* ks = reinterpret_cast<float*>(w);
   w += (size_t)n_kv_heads * cap * sizeof(float);
   float* vs = reinterpret_cast<float*>(w);
 
   AttnMaps m;
-  if ((rc = encode3(&m.k, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, kw, kHeadDim, n_rows, n_kv_heads, kHeadDim * 2,
+  if ((rc = encode3(&m.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kw, kHeadDim, n_rows, n_kv_heads, kHeadDim * 2,
                     (uint64_t)cap * kHeadDim * 2, 64, kTileKeys, 1)))
     return rc;
   if ((rc = encode3(&m.v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, vt, n_rows, kHeadDim, n_kv_heads, (uint64_t)cap * 2,
@@ -214,7 +214,7 @@ extern "C" int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_page
   a.S = n_sink_blk;
   a.W = n_win_blk;
   a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
-  a.q_mode = PA_Q_F16;
+  a.q_mode = PA_Q_BF16;
   a.p_mode = PA_P_F16;
   a.err = err;
   a.wait_ns = 2000ull * 1000000ull;

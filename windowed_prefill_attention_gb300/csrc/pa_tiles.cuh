@@ -130,6 +130,14 @@ PA_HD TileGeom tile_geom(const UnitGeom& u, int i, int S, int W) {
   return g;
 }
 
+// Width in blocks of tile i, the same as tile_geom(u, i, S, W).nb: only the
+// last tile of each run can be narrower than kTileBlocks.
+PA_HD int tile_width(const UnitGeom& u, int i) {
+  if (i == u.n_tiles - 1) return (u.qb + 1 - u.ws) - (u.n_tiles - 1 - u.n_sink_tiles) * kTileBlocks;
+  if (i == u.n_sink_tiles - 1) return u.nsk - i * kTileBlocks;
+  return kTileBlocks;
+}
+
 // Bits [0, n) set, for n clamped to [0, 64].
 PA_HD unsigned long long low_bits(int n) {
   return n <= 0 ? 0ull : (n >= 64 ? ~0ull : ((1ull << n) - 1ull));
