@@ -78,14 +78,14 @@ def test_plan_rejects_empty_and_inconsistent_sequences(pa):
 
 def expected_tiles(block_set):
     """Tiles of a set of key blocks: maximal runs of consecutive blocks, each cut
-    into pieces of at most 4 blocks."""
+    into pieces of at most 8 blocks (128-key tiles)."""
     blocks = sorted(block_set)
     n, i = 0, 0
     while i < len(blocks):
         j = i
         while j + 1 < len(blocks) and blocks[j + 1] == blocks[j] + 1:
             j += 1
-        n += (j - i + 1 + 3) // 4
+        n += (j - i + 1 + 7) // 8
         i = j + 1
     return n
 

@@ -28,6 +28,9 @@ import numpy as np
 import pytest
 
 import oracle
+
+# keys per tile of the kernel: the u8 grid of P' is per row and per tile
+KEY_TILE = 128
 from pa_testutil import TOL_MAX, TOL_MEAN, compare, norm_errors, run_gpu, sample_rows
 from synth import CONFIGS, make_inputs
 from synth.workloads import Workload
@@ -77,7 +80,7 @@ def test_default_mode_matches_method_steps(name, inputs):
     out, rc = run_gpu(inp)
     assert rc == 0
     rows = oracle.all_rows(inp) if name == "tiny" else sample_rows(inp, 200)
-    ref = oracle.method(oracle.Problem.from_inputs(inp), rows, oracle.Q_LOSSLESS, oracle.P_F16, tile=64)
+    ref = oracle.method(oracle.Problem.from_inputs(inp), rows, oracle.Q_LOSSLESS, oracle.P_F16, tile=KEY_TILE)
     mx, mean = norm_errors(out[rows[:, 0], rows[:, 1]].astype(np.float64), ref)
     print("%s vs method: max %.3g mean %.3g" % (name, mx, mean))
     assert mx <= 5e-3 and mean <= 5e-4
@@ -92,7 +95,7 @@ def test_int8_grids_match_oracle_on_clean_data(name, inputs):
     rows = oracle.all_rows(inp) if name == "tiny" else sample_rows(inp, 300)
     mx, mean = compare(out, inp, rows)
     assert mx <= TOL_MAX and mean <= TOL_MEAN
-    ref = oracle.method(oracle.Problem.from_inputs(inp), rows, oracle.Q_INT8, oracle.P_U8, tile=64)
+    ref = oracle.method(oracle.Problem.from_inputs(inp), rows, oracle.Q_INT8, oracle.P_U8, tile=KEY_TILE)
     mx2, mean2 = norm_errors(out[rows[:, 0], rows[:, 1]].astype(np.float64), ref)
     print("%s int8 grids: vs exact %.3g/%.3g, vs method %.3g/%.3g" % (name, mx, mean, mx2, mean2))
     assert mx2 <= 1.5e-2 and mean2 <= 1e-3
@@ -103,7 +106,7 @@ def test_int8_q_grid_alone_follows_method():
     out, rc = run_gpu(inp, q_mode=1, p_mode=0)
     assert rc == 0
     rows = sample_rows(inp, 100)
-    ref = oracle.method(oracle.Problem.from_inputs(inp), rows, oracle.Q_INT8, oracle.P_F16, tile=64)
+    ref = oracle.method(oracle.Problem.from_inputs(inp), rows, oracle.Q_INT8, oracle.P_F16, tile=KEY_TILE)
     mx, mean = norm_errors(out[rows[:, 0], rows[:, 1]].astype(np.float64), ref)
     assert mx <= 5e-3 and mean <= 5e-4
 

@@ -49,13 +49,14 @@ int main() {
           bool any_hidden = false;
           for (int b = tg.kb0; b < tg.kb0 + tg.nb; ++b) ++visits[b];
           for (int t = ta; t <= tb; ++t) {
-            const unsigned long long v = visible_columns(tg, t, S, W);
-            for (int c = 0; c < 64; ++c) {
+            const unsigned long long vh[2] = {visible_columns(tg, t, S, W, 0), visible_columns(tg, t, S, W, 1)};
+            for (int c = 0; c < kTileKeys; ++c) {
+              const unsigned long long v = vh[c / 64];
               const int j = tg.kb0 * kPage + c;
               const bool in_tile = c < tg.nb * kPage;
               const bool want = in_tile && sees(t, j, S, W);
               if (in_tile && !sees(t, j, S, W)) any_hidden = true;
-              const bool got = (v >> c) & 1ull;
+              const bool got = (v >> (c % 64)) & 1ull;
               if (tg.needs_mask && got != want) { printf("FAIL cols t=%d j=%d\n", t, j); return 1; }
               if (!tg.needs_mask && in_tile && !want) { printf("FAIL unmasked t=%d j=%d\n", t, j); return 1; }
               ++checked;

@@ -315,13 +315,22 @@ int run(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t*
       return rc;
     const uint64_t vd[3] = {(uint64_t)P.n_tok_total, (uint64_t)kHeadDim, (uint64_t)h->HKV};
     const uint64_t vst[2] = {(uint64_t)h->n_tok_cap * 2, (uint64_t)h->n_tok_cap * kHeadDim * 2};
-    const uint32_t vbox[3] = {(uint32_t)kTileKeys, (uint32_t)kHeadDim, 1};
+    const uint32_t vbox[3] = {(uint32_t)kChunkKeys, (uint32_t)kHeadDim, 1};
     if ((rc = encode(&h->maps.v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, h->vt, vd, vst, vbox,
                      CU_TENSOR_MAP_SWIZZLE_128B)))
       return rc;
     h->kv_ptr = h->kw;
     h->kv_rows = P.n_tok_total;
     h->kv_cap = h->n_tok_cap;
+  }
+  // the query's map: q as [tokens][HQ][256], a unit's rows are TQ tokens x G heads
+  AttnMaps maps = h->maps;
+  {
+    const uint64_t qd[3] = {(uint64_t)kHeadDim, (uint64_t)h->HQ, (uint64_t)P.total_q};
+    const uint64_t qst[2] = {(uint64_t)kHeadDim * 2, (uint64_t)h->HQ * kHeadDim * 2};
+    const uint32_t qbox[3] = {64, (uint32_t)h->G, (uint32_t)h->TQ};
+    if ((rc = encode(&maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, qd, qst, qbox, CU_TENSOR_MAP_SWIZZLE_128B)))
+      return rc;
   }
   cudaEvent_t e0 = nullptr, e1 = nullptr, e2 = nullptr;
   if (h->opt.record_timing) {
@@ -358,7 +367,7 @@ int run(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t*
   a.wait_ns = (unsigned long long)h->opt.wait_timeout_ms * 1000000ull;
   a.unit_counter = h->d_counter;
   a.debug_stall = h->opt.debug_stall;
-  PA_CUDA(launch_attention(a, h->maps, h->n_sm, st));
+  PA_CUDA(launch_attention(a, maps, h->n_sm, st));
   if (e2) {
     PA_CUDA(cudaEventRecord(e2, st));
     h->ev_pending.push_back(e0);

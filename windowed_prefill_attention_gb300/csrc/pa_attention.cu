@@ -7,21 +7,31 @@
 // pool; the per-row Q, per-token K and softmax scales applied to the integer-
 // valued scores; the online-softmax recurrence; the per-token V scale folded
 // into P before P is quantised per row; PV on the tensor cores; masked blocks
-// never visited.  The int8 codes travel in fp16 containers (tcgen05.mma
-// kind::f16), which hold them exactly.
+// never visited.  The int8 codes travel in 16-bit float containers
+// (tcgen05.mma kind::f16), which hold them exactly: K in bf16 against the bf16
+// query, V in fp16 against P' in fp16.
 //
 // One CTA per SM walks the longest-first unit list with stride gridDim.x.  A
-// unit is 128 query rows of one kv head (pa_tiles.cuh).  Roles:
-//   warp 0        TMA producer: K tiles into a 3-slot ring, V^T tiles and the
-//                 tile's K/V scales into another 3-slot ring
-//   warp 1        TMEM allocator and the single MMA-issuing thread:
-//                 QK^T(j+1) is issued before PV(j), so the tensor core works on
-//                 the next scores while the softmax handles the current ones
+// unit is 128 query rows of one kv head; key tiles are 128 keys (pa_tiles.cuh).
+// With N = 128 a QK^T instruction runs at the tensor core's full rate (at
+// N = 64 it does not), which sets the memory plan:
+//   TMEM (512 columns)   O fp32 [0,256), S0 [256,384), S1 [384,512); P (fp16
+//                        pairs) of warp half h overwrites S columns [64h, 64h+32)
+//   shared memory        Q (64 KB, bf16, TMA), K as four 16 KB slots, one per
+//                        64-dim region of a tile, V^T as two 32 KB slots of 64
+//                        keys, the tiles' K/V scales in two 1 KB slots
+// Each K region slot is released by the commit after the four k-steps that
+// read it, so region r of the next tile loads while this tile's later regions
+// are multiplied.  Roles:
+//   warp 0        TMA producer of the K regions
+//   warp 1        TMEM allocator and the single MMA-issuing thread; QK^T(j+1)
+//                 is issued before PV(j), so the tensor core works on the next
+//                 scores while the softmax handles the current ones
+//   warp 2        TMA producer of the V^T chunks
+//   warp 3        producer of Q (TMA, after an L2 prefetch) and of the scales
 //   warps 4-11    softmax: one query row per thread (TMEM lane = row), two
-//                 warps per lane quadrant, each owning half of the key columns
-//   warps 12-15   Q prologue of the next unit and epilogue of the previous one
-// TMEM (512 columns): O fp32 [0,256), Q fp16 pairs [256,384), S0/S1 fp32
-// [384,448)/[448,512); P (fp16 pairs) overwrites the first half of its S.
+//                 warps per lane quadrant, each owning 64 of the 128 key columns
+//   warps 12-15   epilogue of each unit (and Q codes on the int8 grid)
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -35,36 +45,36 @@ namespace pa {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kSlots = 3;                              // depth of the K ring and of the V ring
-constexpr int kKTileBytes = kTileKeys * kHeadDim * 2;  // 32 KB: 4 regions of 64 keys x 128 B
-constexpr int kVTileBytes = kHeadDim * kTileKeys * 2;  // 32 KB: 256 dims x 128 B
+constexpr int kRegionBytes = kTileKeys * 128;           // 16 KB: 128 rows x 64 dims (bf16)
+constexpr int kChunkBytes = kHeadDim * kChunkKeys * 2;  // 32 KB: 256 dims x 64 keys (fp16)
 // Shared memory, offsets from a 1024-byte aligned base.
-constexpr int kSmK = 0;
-constexpr int kSmV = kSmK + kSlots * kKTileBytes;
-constexpr int kSmScale = kSmV + kSlots * kVTileBytes;  // per slot: ks[64] (K ring) then vs[64] (V ring)
-constexpr int kSmRows = kSmScale + kSlots * 512;       // c[2][128], l[2][2][128], sp[2][128] floats
-constexpr int kSmXchg = kSmRows + 8 * kRows * 4;       // softmax pair exchange: 2 x [2][2][128] floats
-constexpr int kSmStage = kSmXchg + 8 * kRows * 4;      // correction warps: 4 x [32 rows][128 B]
+constexpr int kSmQ = 0;                                 // 4 regions of 128 rows x 128 B
+constexpr int kSmK = kSmQ + 4 * kRegionBytes;           // 4 region slots
+constexpr int kSmV = kSmK + 4 * kRegionBytes;           // 2 chunk slots
+constexpr int kSmScale = kSmV + 2 * kChunkBytes;        // 2 slots: ks[128], vs[128]
+constexpr int kSmRows = kSmScale + 2 * 1024;            // c[2][128], l[2][2][128], sp[2][128] floats
+constexpr int kSmXchg = kSmRows + 8 * kRows * 4;        // softmax pair exchange: 2 x [2][2][128] floats
+constexpr int kSmStage = kSmXchg + 8 * kRows * 4;       // epilogue: 4 x [32 rows][128 B]
 constexpr int kSmBars = kSmStage + 4 * 4096;
 enum : int {
-  B_KFULL = 0, B_KEMPTY = 3, B_VFULL = 6, B_VEMPTY = 9, B_SFULL = 12, B_PFULL = 14,
-  B_QFULL = 16, B_QEMPTY = 17, B_OFULL = 18, B_OEMPTY = 19, B_STATS = 20 /* two, by unit parity */,
-  B_STALL = 22, B_DRAIN = 23, B_QSOON = 24, kNumBars = 25
+  B_KFULL = 0, B_KEMPTY = 4, B_VFULL = 8, B_VEMPTY = 10, B_SCFULL = 12, B_SCEMPTY = 14, B_SFULL = 16,
+  B_PFULL = 18, B_QFULL = 20, B_QREADY = 21, B_QEMPTY = 22, B_OFULL = 23, B_OEMPTY = 24,
+  B_STATS = 25 /* two, by unit parity */, B_STALL = 27, B_DRAIN = 28, B_QSOON = 29, kNumBars = 30
 };
-// The MMA issuer arrives on B_QSOON when it issues QK^T for the tile kQSoon
-// tiles before its unit's last; the correction warps then start loading the
-// next unit's Q rows, so that they are in L2 when the unit's Q may be stored.
-constexpr int kQSoon = 6;
-constexpr float kLift = 6.f;   // a unit's first reference sits 2^kLift above its first tile's max
-constexpr float kLazy = 14.f;  // the softmax reference moves when a row max grows by more than 2^kLazy;
-                               // P' = p * v_scale * 2^-ev then stays below 2^14, inside the fp16 range
 constexpr int kSmTmemSlot = kSmBars + kNumBars * 8;
 constexpr int kAttnSmem = kSmTmemSlot + 16 + 1024;  // + alignment slack
 static_assert(kAttnSmem <= 227 * 1024, "shared memory budget");
 
+// The MMA issuer arrives on B_QSOON when it issues QK^T for the tile kQSoon
+// tiles before its unit's last; the Q producer then prefetches the next
+// unit's Q rows into L2, so that they are there when Q's slot frees up.
+constexpr int kQSoon = 4;
+constexpr float kLift = 6.f;   // a unit's first reference sits 2^kLift above its first tile's max
+constexpr float kLazy = 14.f;  // the softmax reference moves when a row max grows by more than 2^kLazy;
+                               // P' = p * v_scale * 2^-ev then stays below 2^14, inside the fp16 range
+
 constexpr uint32_t kTmO = 0;
-constexpr uint32_t kTmQ = 256;
-constexpr uint32_t kTmS = 384;
+constexpr uint32_t kTmS = 256;
 constexpr uint64_t kDrainNs = 200000000ull;
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -82,6 +92,8 @@ __device__ __forceinline__ int pow2_ceil_exp(float x) {
   const int eb = (int)((__float_as_uint(x) >> 23) & 0xff);
   return imax(-100, imin(100, eb - 126));
 }
+// V^T chunks of a tile of nb blocks.
+__device__ __forceinline__ int n_chunks(int nb) { return (nb + 3) / 4; }
 
 struct Ctx {
   uint32_t sbase;  // shared address of the aligned base
@@ -97,53 +109,105 @@ struct Ctx {
   }
 };
 
-// ------------------------------------------------------------------ producer
-__device__ __forceinline__ void role_producer(const AttnParams& p, const AttnMaps& m, const Ctx& c) {
-  uint32_t kc = 0, vc = 0;  // loads issued into the K ring and the V ring
+// ------------------------------------------------------------------ producers
+// K: per tile, region r (dims [64r, 64r+64), 128 keys) into slot r.  Slot r
+// is used once per tile, so its phases follow the tile counter.
+__device__ __forceinline__ void role_producer_k(const AttnParams& p, const AttnMaps& m, const Ctx& c) {
+  uint32_t kt = 0;  // tiles loaded
   bool ok = true;
   for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
     const UnitGeom ug = unit_geom(un.t0, p.TQ, sg, p.S, p.W);
-    for (int j = 0; j < ug.n_tiles; ++j) {
+    for (int j = 0; j < ug.n_tiles && ok; ++j, ++kt) {
+      const int crow = logical_block_row(sg, tile_geom(ug, j, p.S, p.W).kb0);
+      for (int r = 0; r < 4; ++r) {
+        if (!(ok = mbar_wait(c.bar(B_KEMPTY + r), (kt & 1) ^ 1, c.wc, 10))) break;
+        const uint32_t fb = c.bar(B_KFULL + r);
+        mbar_expect_tx(fb, kRegionBytes);
+        tma_load_3d(c.sbase + kSmK + r * kRegionBytes, &m.k, fb, r * 64, crow, un.g);
+      }
+    }
+  }
+  // every issued copy lands before the CTA may exit (a load that was never
+  // issued leaves its slot's previous phase complete, which passes too)
+  if (kt > 0)
+    for (int r = 0; r < 4; ++r) (void)mbar_wait_drain(c.bar(B_KFULL + r), (kt - 1) & 1, kDrainNs);
+}
+
+// V^T: per tile, its 64-key chunks into a two-slot ring.
+__device__ __forceinline__ void role_producer_v(const AttnParams& p, const AttnMaps& m, const Ctx& c) {
+  uint32_t vc = 0;  // chunks loaded
+  bool ok = true;
+  for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+    const Unit un = p.units[u];
+    const SeqGeom sg = p.seqs[un.seq];
+    const UnitGeom ug = unit_geom(un.t0, p.TQ, sg, p.S, p.W);
+    for (int j = 0; j < ug.n_tiles && ok; ++j) {
       const TileGeom tg = tile_geom(ug, j, p.S, p.W);
       const int crow = logical_block_row(sg, tg.kb0);
-      {
-        const int s = kc % kSlots;
-        const uint32_t ph = (kc / kSlots) & 1;
-        if (!(ok = mbar_wait(c.bar(B_KEMPTY + s), ph ^ 1, c.wc, 10))) break;
-        const uint32_t fb = c.bar(B_KFULL + s);
-        const uint32_t sbytes = (uint32_t)(tg.nb * kPage * 4);
-        mbar_expect_tx(fb, kKTileBytes + sbytes);
-        const uint32_t dst = c.sbase + kSmK + s * kKTileBytes;
-        for (int r = 0; r < 4; ++r) tma_load_3d(dst + r * 8192, &m.k, fb, r * 64, crow, un.g);
-        bulk_load(c.sbase + kSmScale + s * 512, p.ks + (size_t)un.g * p.n_tok_cap + crow, sbytes, fb);
-        ++kc;
-      }
-      {
-        const int s = vc % kSlots;
-        const uint32_t ph = (vc / kSlots) & 1;
-        if (!(ok = mbar_wait(c.bar(B_VEMPTY + s), ph ^ 1, c.wc, 11))) break;
+      for (int ch = 0; ch < n_chunks(tg.nb); ++ch) {
+        const uint32_t s = vc & 1;
+        if (!(ok = mbar_wait(c.bar(B_VEMPTY + s), ((vc >> 1) & 1) ^ 1, c.wc, 11))) break;
         const uint32_t fb = c.bar(B_VFULL + s);
-        const uint32_t sbytes = (uint32_t)(tg.nb * kPage * 4);
-        mbar_expect_tx(fb, kVTileBytes + sbytes);
-        tma_load_3d(c.sbase + kSmV + s * kVTileBytes, &m.v, fb, crow, 0, un.g);
-        bulk_load(c.sbase + kSmScale + s * 512 + 256, p.vs + (size_t)un.g * p.n_tok_cap + crow, sbytes, fb);
+        mbar_expect_tx(fb, kChunkBytes);
+        tma_load_3d(c.sbase + kSmV + s * kChunkBytes, &m.v, fb, crow + ch * kChunkKeys, 0, un.g);
         ++vc;
       }
     }
   }
-  // every issued copy lands before the CTA may exit: the last load into each
-  // slot was load number kc-1-i (K) / vc-1-i (V) for i < kSlots
-  for (uint32_t i = 0; i < (uint32_t)kSlots; ++i) {
-    if (kc > i) (void)mbar_wait_drain(c.bar(B_KFULL + (kc - 1 - i) % kSlots), ((kc - 1 - i) / kSlots) & 1, kDrainNs);
-    if (vc > i) (void)mbar_wait_drain(c.bar(B_VFULL + (vc - 1 - i) % kSlots), ((vc - 1 - i) / kSlots) & 1, kDrainNs);
+  for (uint32_t i = 0; i < 2; ++i)
+    if (vc > i) (void)mbar_wait_drain(c.bar(B_VFULL + ((vc - 1 - i) & 1)), ((vc - 1 - i) >> 1) & 1, kDrainNs);
+}
+
+// Q of each unit (after the previous unit's last QK^T) and the K/V scales of
+// each tile (two-slot ring by tile parity).
+__device__ __forceinline__ void role_producer_q(const AttnParams& p, const AttnMaps& m, const Ctx& c) {
+  uint32_t ts = 0;  // tiles whose scales were loaded
+  int k_unit = 0;   // units whose Q was loaded
+  bool ok = true;
+  for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+    const Unit un = p.units[u];
+    const SeqGeom sg = p.seqs[un.seq];
+    const UnitGeom ug = unit_geom(un.t0, p.TQ, sg, p.S, p.W);
+    // q row (token position in q) of the unit's first token; negative or past
+    // the sequence where the unit overhangs it: those rows are never output
+    const int tok0 = sg.q_off + (un.t0 - sg.q_start);
+    if (k_unit > 0) {
+      if (!(ok = mbar_wait(c.bar(B_QSOON), (k_unit - 1) & 1, c.wc, 12))) break;
+      for (int i = 0; i < p.TQ; ++i) {
+        const int tok = tok0 + i;
+        if (tok >= sg.q_off && tok < sg.q_off + sg.n_q)
+          bulk_prefetch_l2(p.q + ((size_t)tok * p.HQ + (size_t)un.g * p.G) * kHeadDim, (uint32_t)p.G * kHeadDim * 2);
+      }
+      if (!(ok = mbar_wait(c.bar(B_QEMPTY), (k_unit - 1) & 1, c.wc, 13))) break;
+    }
+    mbar_expect_tx(c.bar(B_QFULL), 4 * kRegionBytes);
+    for (int r = 0; r < 4; ++r)
+      tma_load_3d(c.sbase + kSmQ + r * kRegionBytes, &m.q, c.bar(B_QFULL), r * 64, un.g * p.G, tok0);
+    ++k_unit;
+    for (int j = 0; j < ug.n_tiles; ++j) {
+      const uint32_t s = ts & 1;
+      if (!(ok = mbar_wait(c.bar(B_SCEMPTY + s), ((ts >> 1) & 1) ^ 1, c.wc, 14))) break;
+      const TileGeom tg = tile_geom(ug, j, p.S, p.W);
+      const int crow = logical_block_row(sg, tg.kb0);
+      const uint32_t bytes = (uint32_t)(tg.nb * kPage * 4);
+      const uint32_t fb = c.bar(B_SCFULL + s);
+      mbar_expect_tx(fb, 2 * bytes);
+      bulk_load(c.sbase + kSmScale + s * 1024, p.ks + (size_t)un.g * p.n_tok_cap + crow, bytes, fb);
+      bulk_load(c.sbase + kSmScale + s * 1024 + 512, p.vs + (size_t)un.g * p.n_tok_cap + crow, bytes, fb);
+      ++ts;
+    }
   }
+  if (k_unit > 0) (void)mbar_wait_drain(c.bar(B_QFULL), (k_unit - 1) & 1, kDrainNs);
+  for (uint32_t i = 0; i < 2; ++i)
+    if (ts > i) (void)mbar_wait_drain(c.bar(B_SCFULL + ((ts - 1 - i) & 1)), ((ts - 1 - i) >> 1) & 1, kDrainNs);
 }
 
 // ------------------------------------------------------------------ MMA issuer
 __device__ __forceinline__ void role_mma(const AttnParams& p, const Ctx& c) {
-  uint32_t tc = 0;  // global tile counter: K slot, V slot and S buffer of every tile
+  uint32_t tc = 0;  // global tile counter: K phases and S buffer of every tile
+  uint32_t vc = 0;  // global V^T chunk counter
   int k_unit = 0;
   bool ok = true;
   const uint32_t id_pv = idesc_f16(kRows, kHeadDim, false, false);
@@ -152,51 +216,50 @@ __device__ __forceinline__ void role_mma(const AttnParams& p, const Ctx& c) {
     const SeqGeom sg = p.seqs[un.seq];
     const UnitGeom ug = unit_geom(un.t0, p.TQ, sg, p.S, p.W);
     const int n = ug.n_tiles;
-    if (!(ok = mbar_wait(p.debug_stall ? c.bar(B_STALL) : c.bar(B_QFULL), k_unit & 1, c.wc, 20))) break;
-    // Operands of the next QK^T.  They are prepared (K slot waited for,
-    // descriptors built) right after the previous QK^T is issued, so that
-    // PV(j-1) is followed at once by QK^T(j+1).
-    uint32_t qk_d = 0, qk_id = 0;
-    uint64_t qk_kd0 = 0;
-    auto prep_qk = [&](int j) -> bool {
-      const uint32_t t = tc + j;
-      const uint32_t slot = t % kSlots;
-      if (!mbar_wait(c.bar(B_KFULL + slot), (t / kSlots) & 1, c.wc, 21)) return false;
-      qk_d = c.tb + kTmS + (t & 1) * kTileKeys;
-      qk_id = idesc_f16(kRows, tile_width(ug, j) * kPage, true, true);  // bf16 Q, bf16 K codes
-      qk_kd0 = sdesc_k_sw128(c.sbase + kSmK + slot * kKTileBytes);
-      return true;
-    };
-    if (!(ok = prep_qk(0))) break;
+    const int qbar = p.debug_stall ? B_STALL : (p.q_mode == 1 ? B_QREADY : B_QFULL);
+    if (!(ok = mbar_wait(c.bar(qbar), k_unit & 1, c.wc, 20))) break;
     for (int j = 0; j <= n; ++j) {
-      if (j < n) {  // S(j) = Q K(j)^T
+      if (j < n) {  // S(j) = Q K(j)^T, region by region
         const uint32_t t = tc + j;
-        tc_fence_after();
-        // k-step s reads K bytes at (s/4)*8192 + (s%4)*32 from the slot: only
-        // the descriptor's start-address field (address >> 4) moves
+        const uint32_t d = c.tb + kTmS + (t & 1) * kTileKeys;
+        const uint32_t id = idesc_f16(kRows, tile_width(ug, j) * kPage, true, true);  // bf16 Q, bf16 K codes
+        for (int r = 0; r < 4; ++r) {
+          if (!(ok = mbar_wait(c.bar(B_KFULL + r), t & 1, c.wc, 21))) break;
+          tc_fence_after();
+          // Q region r and K slot r: SW128 K-major, k-step s at +32 s bytes
+          const uint64_t qd = sdesc_k_sw128(c.sbase + kSmQ + r * kRegionBytes);
+          const uint64_t kd = sdesc_k_sw128(c.sbase + kSmK + r * kRegionBytes);
 #pragma unroll
-        for (int s = 0; s < kHeadDim / 16; ++s)
-          mma_ts(qk_d, c.tb + kTmQ + 8 * s, qk_kd0 + (uint64_t)(((s >> 2) * 8192 + (s & 3) * 32) >> 4), qk_id, s > 0);
-        mma_commit(c.bar(B_SFULL + (t & 1)));  // also frees K slot t: the softmax passes it on
+          for (int s = 0; s < 4; ++s) mma_ss(d, qd + 2 * s, kd + 2 * s, id, (r | s) != 0 ? 1u : 0u);
+          mma_commit(c.bar(B_KEMPTY + r));  // region slot r free once these four are done
+        }
+        if (!ok) break;
+        mma_commit(c.bar(B_SFULL + (t & 1)));
         if (j == n - 1) mma_commit(c.bar(B_QEMPTY));
         if (j == imax(0, n - kQSoon)) mbar_arrive(c.bar(B_QSOON));
-        if (j + 1 < n && !(ok = prep_qk(j + 1))) break;
       }
-      if (j >= 1) {  // O (+)= P(j-1) V(j-1)
+      if (j >= 1) {  // O (+)= P(j-1) V(j-1), chunk by chunk
         const int jj = j - 1;
         const uint32_t t = tc + jj;
-        // V(t) has landed: every softmax warp waited for its barrier (for the
-        // V scales) before releasing P(t)
         if (!(ok = mbar_wait(c.bar(B_PFULL + (t & 1)), (t >> 1) & 1, c.wc, 22))) break;
         if (jj == 0 && k_unit > 0 && !(ok = mbar_wait(c.bar(B_OEMPTY), (k_unit - 1) & 1, c.wc, 24))) break;
-        tc_fence_after();
-        const uint32_t slot = t % kSlots;
         const uint32_t a = c.tb + kTmS + (t & 1) * kTileKeys;
-        const uint64_t vd0 = sdesc_k_sw128(c.sbase + kSmV + slot * kVTileBytes);
         const int nb = tile_width(ug, jj);
-        for (int s = 0; s < nb; ++s)
-          mma_ts(c.tb + kTmO, a + 8 * s, vd0 + (uint64_t)(2 * s), id_pv, (jj > 0 || s > 0) ? 1u : 0u);
-        mma_commit(c.bar(B_VEMPTY + slot));  // V slot t free; O holds PV up to tile t
+        for (int ch = 0; ch < n_chunks(nb); ++ch) {
+          const uint32_t s = vc & 1;
+          if (!(ok = mbar_wait(c.bar(B_VFULL + s), (vc >> 1) & 1, c.wc, 23))) break;
+          tc_fence_after();
+          const uint64_t vd = sdesc_k_sw128(c.sbase + kSmV + s * kChunkBytes);
+          // k-step ks covers keys [16 ks, 16 ks + 16) of the chunk; P of
+          // chunk ch sits at S columns [64 ch, 64 ch + 32)
+          const int nks = imin(4, nb - 4 * ch);
+          for (int ks = 0; ks < nks; ++ks)
+            mma_ts(c.tb + kTmO, a + 64 * ch + 8 * ks, vd + (uint64_t)(2 * ks), id_pv,
+                   (jj > 0 || ch > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(c.bar(B_VEMPTY + s));  // V slot free; O holds PV up to this chunk
+          ++vc;
+        }
+        if (!ok) break;
         if (jj == n - 1) mma_commit(c.bar(B_OFULL));
       }
     }
@@ -209,8 +272,8 @@ __device__ __forceinline__ void role_mma(const AttnParams& p, const Ctx& c) {
 }
 
 // ------------------------------------------------------------------ softmax
-// Two warps per TMEM lane quadrant: warp half h owns key columns [32h, 32h+32)
-// of every 64-key tile for the same 32 rows.  The pair agrees on each row's
+// Two warps per TMEM lane quadrant: warp half h owns key columns [64h, 64h+64)
+// of every 128-key tile for the same 32 rows.  The pair agrees on each row's
 // running maximum through shared memory, so both halves use one reference and
 // their P', partial sums and halves of the O rescale add up exactly.
 __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, uint8_t* sm) {
@@ -225,7 +288,7 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
   float* xbuf = reinterpret_cast<float*>(sm + kSmXchg);  // [tile parity][half][row] row maxima
   float* pbuf = xbuf + 4 * kRows;                        // [tile parity][half][row] P' maxima (u8 grid)
   const bool u8 = p.p_mode == 1;
-  uint32_t tc = 0;
+  uint32_t tc = 0, vc = 0;
   int k_unit = 0;
   bool ok = true;
   for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++k_unit) {
@@ -235,11 +298,16 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
     const int n = ug.n_tiles;
     const int t_row = un.t0 + r / p.G;
     const float ev = (float)pow2_ceil_exp(__uint_as_float(p.vsmax[un.seq * p.HKV + un.g]));
-    // both warps of the pair agree before entering the unit's tiles
-    ok = bar_red_and(1 + qd, 64, c.warp_wait(B_QFULL, k_unit & 1, 30));
-    if (!ok) break;
-    // s_q * sm_scale * log2(e), kept positive so that -inf scores stay -inf
-    const float c_row = fmaxf(c_rows[(k_unit & 1) * kRows + r], 1e-30f);
+    // s_q * sm_scale * log2(e), kept positive so that -inf scores stay -inf;
+    // s_q = 1 for the bf16 query, per row on the int8 grid
+    float c_row = p.sm_scale_log2;
+    if (p.q_mode == 1) {
+      // both warps of the pair agree before entering the unit's tiles
+      ok = bar_red_and(1 + qd, 64, c.warp_wait(B_QREADY, k_unit & 1, 30));
+      if (!ok) break;
+      c_row = c_rows[(k_unit & 1) * kRows + r];
+    }
+    c_row = fmaxf(c_row, 1e-30f);
     float m_run = -INFINITY, l_run = 0.f, sp_prev = 1.f;
     for (int j = 0; j < n; ++j) {
       const uint32_t t = tc + j;
@@ -247,54 +315,53 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
       // Every path through a tile passes the pair barrier the same number of
       // times, so a wait that runs out in one warp cannot strand its partner.
       bool okl = c.warp_wait(B_SFULL + (t & 1), (t >> 1) & 1, 31);
-      // the K scales landed with K slot t, which QK(t) already consumed; wait on
-      // that slot's barrier too so this warp observes the copy itself (the
-      // phase cannot move on before this warp releases the slot below)
-      okl = okl && c.warp_wait(B_KFULL + t % kSlots, (t / kSlots) & 1, 34);
-      const uint32_t sd = c.tb + lane_off + kTmS + (t & 1) * kTileKeys;
-      // this half's K scales (32 floats); its V scales follow 256 bytes later
-      const float4* ks4 = reinterpret_cast<const float4*>(sm + kSmScale + (t % kSlots) * 512 + 128 * h);
-      const float4* vs4 = ks4 + 16;
-      float y[32];
+      okl = okl && c.warp_wait(B_SCFULL + (t & 1), (t >> 1) & 1, 32);
+      const uint32_t sd = c.tb + lane_off + kTmS + (t & 1) * kTileKeys + 64 * h;
+      // this half's K scales (64 floats); its V scales follow 512 bytes later
+      const float4* ks4 = reinterpret_cast<const float4*>(sm + kSmScale + (t & 1) * 1024 + 256 * h);
+      const float4* vs4 = ks4 + 32;
+      float y[64];
       float my = -INFINITY;
       if (okl) {
         tc_fence_after();
-        uint32_t sa[32];
-        tmem_ld32(sd + 32 * h, sa);
+        uint32_t sa[32], sb[32];
+        tmem_ld32(sd, sa);
+        tmem_ld32(sd + 32, sb);
         tmem_wait_ld(sa);
+        reg_fence(sb);
         // y = S * k_scale (masked: -inf), and this half's row maximum
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (!tg.needs_mask && tg.nb == kTileBlocks) {  // full tile, every row sees every key
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
+          for (int q4 = 0; q4 < 16; ++q4) {
             const float4 k4 = ks4[q4];
             const float kq[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int q = 4 * q4 + e;
-              y[q] = __uint_as_float(sa[q]) * kq[e];
+              y[q] = __uint_as_float(q < 32 ? sa[q] : sb[q - 32]) * kq[e];
               m4[e] = fmaxf(m4[e], y[q]);
             }
           }
         } else {
-          const uint32_t vis = (uint32_t)(visible_columns(tg, t_row, p.S, p.W) >> (32 * h));
+          const unsigned long long vis = visible_columns(tg, t_row, p.S, p.W, h);
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
+          for (int q4 = 0; q4 < 16; ++q4) {
             const float4 k4 = ks4[q4];
             const float kq[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int q = 4 * q4 + e;
-              y[q] = ((vis >> q) & 1u) ? __uint_as_float(sa[q]) * kq[e] : -INFINITY;
+              y[q] = ((vis >> q) & 1ull) ? __uint_as_float(q < 32 ? sa[q] : sb[q - 32]) * kq[e] : -INFINITY;
               m4[e] = fmaxf(m4[e], y[q]);
             }
           }
         }
         my = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c_row;  // log2 units
+      } else {
+#pragma unroll
+        for (int q = 0; q < 64; ++q) y[q] = -INFINITY;
       }
-      // this warp is done with K slot t (QK(t) finished before S(t) was complete)
-      __syncwarp();
-      if (okl && lane == 0) mbar_arrive(c.bar(B_KEMPTY + t % kSlots));
       // the reference moves only when some row's max grew by more than 2^kLazy
       const bool grow = okl && (m_run == -INFINITY || my > m_run + kLazy);
       float alpha = 1.f;
@@ -315,13 +382,10 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
         }
       }
       const float mref = m_run == -INFINITY ? 0.f : m_run + ev;
-      // the V scales of tile t arrive with the V tile; a wait that runs out
-      // leaves the loop after the next group barrier, like the others
-      if (!c.warp_wait(B_VFULL + t % kSlots, (t / kSlots) & 1, 32)) okl = false;
       // p = 2^(y c - mref); P' = p * v_scale (V scale folded into P)
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int q4 = 0; q4 < 8; ++q4) {
+      for (int q4 = 0; q4 < 16; ++q4) {
         const float4 v4 = vs4[q4];
         const float vq[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
@@ -332,12 +396,15 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
           y[q] = pj * vq[e];
         }
       }
+      // this warp is done with the tile's scales
+      __syncwarp();
+      if (okl && lane == 0) mbar_arrive(c.bar(B_SCEMPTY + (t & 1)));
       l_run = l_run * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
       float corr = alpha;
       if (u8) {  // P' per row on the u8 grid over the whole tile, scale max/255
         float pm = 0.f;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) pm = fmaxf(pm, y[q]);
+        for (int q = 0; q < 64; ++q) pm = fmaxf(pm, y[q]);
         float* pb = pbuf + (t & 1) * 2 * kRows;
         pb[h * kRows + r] = pm;
         bar_red_and(1 + qd, 64, true);
@@ -345,19 +412,20 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
         const float sp = pmax > 0.f ? __fdiv_rn(pmax, 255.f) : sp_prev;
         const float inv = pmax > 0.f ? __fdiv_rn(255.f, pmax) : 0.f;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) y[q] = rintf(y[q] * inv);
+        for (int q = 0; q < 64; ++q) y[q] = rintf(y[q] * inv);
         corr = alpha * __fdiv_rn(sp_prev, sp);
         sp_prev = sp;
       }
-      uint32_t pk[16];
+      uint32_t pk[32];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) pk[q] = pack_half2(y[2 * q], y[2 * q + 1]);
-      tmem_st16(sd + 16 * h, pk);
-      // O holds PV up to tile j-1 once that MMA is done; rescale this half in
-      // place.  A wait that runs out skips the rescale without leaving the
-      // loop: the error word then fails the next tile's pair barrier for both.
+      for (int q = 0; q < 32; ++q) pk[q] = pack_half2(y[2 * q], y[2 * q + 1]);
+      tmem_st32(sd, pk);
+      // O holds PV up to tile j-1 once that MMA's last chunk is done; rescale
+      // this half in place.  A wait that runs out skips the rescale without
+      // leaving the loop: the error word then fails the next tile's pair
+      // barrier for both.
       if (j > 0 && __any_sync(0xffffffffu, corr != 1.f) &&
-          c.warp_wait(B_VEMPTY + (t - 1) % kSlots, ((t - 1) / kSlots) & 1, 33)) {
+          c.warp_wait(B_VEMPTY + ((vc - 1) & 1), ((vc - 1) >> 1) & 1, 33)) {
         tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
@@ -374,6 +442,7 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bar(B_PFULL + (t & 1)));
+      vc += n_chunks(tg.nb);
     }
     if (!ok) break;
     tc += n;
@@ -385,7 +454,7 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
   tmem_wait_st();
 }
 
-// ------------------------------------------------------------------ prologue / epilogue
+// ------------------------------------------------------------------ Q codes / epilogue
 struct RowInfo {
   bool valid;
   size_t off;  // element offset of the row in q / out
@@ -400,13 +469,13 @@ __device__ __forceinline__ RowInfo row_info(const AttnParams& p, const Unit& un,
   return ri;
 }
 
-// Row-major global traffic of the correction warps goes through shared
-// memory, 32 rows x 128 bytes per warp, so that one warp instruction moves
-// four whole 128-byte lines (lane l: row 4k + l/8, 16-byte piece l%8) while
-// the TMEM side keeps one row per thread.  Piece p of row i is kept at piece
-// p ^ (i & 7), which makes both access patterns free of bank conflicts.
-__device__ __forceinline__ uint4* stage_at(uint8_t* stage, int row, int piece) {
-  return reinterpret_cast<uint4*>(stage + row * 128 + ((piece ^ (row & 7)) << 4));
+// 16-byte piece `piece` of row `row` of a tile of 128-byte rows written by TMA
+// with the 128-byte swizzle (1024-byte aligned): the pieces of a row are
+// permuted by the row's index mod 8.  The epilogue stage uses the same layout,
+// which makes both a thread per row and four rows per warp instruction free of
+// bank conflicts.
+__device__ __forceinline__ uint4* swz(uint8_t* base, int row, int piece) {
+  return reinterpret_cast<uint4*>(base + row * 128 + ((piece ^ (row & 7)) << 4));
 }
 
 // The rows lane `lane` moves in the four-rows-per-instruction pattern:
@@ -428,14 +497,16 @@ __device__ __forceinline__ LaneRows lane_rows(const AttnParams& p, const Unit& u
   return lr;
 }
 
-// The row's absolute maximum, for the int8 grid only.
-__device__ __forceinline__ float q_absmax(const AttnParams& p, const RowInfo& ri) {
-  const uint4* src = reinterpret_cast<const uint4*>(p.q + ri.off);
+// Q on the pages' int8 grid (step a1), in place in shared memory: the row's
+// codes rint(q * 127/absmax) clamped to [-127, 127], held exactly as bf16;
+// returns s_q * sm_scale * log2(e) with s_q = absmax / 127.
+__device__ __forceinline__ float q_codes_int8(const AttnParams& p, uint8_t* qs, int r) {
   float absmax = 0.f;
-  if (ri.valid) {
-#pragma unroll 8
-    for (int k = 0; k < 32; ++k) {
-      const uint4 v = __ldg(src + k);
+#pragma unroll 1
+  for (int reg = 0; reg < 4; ++reg)
+#pragma unroll
+    for (int pc = 0; pc < 8; ++pc) {
+      const uint4 v = *swz(qs + reg * kRegionBytes, r, pc);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -443,81 +514,24 @@ __device__ __forceinline__ float q_absmax(const AttnParams& p, const RowInfo& ri
         absmax = fmaxf(absmax, fabsf(__uint_as_float(w[e] & 0xffff0000u)));
       }
     }
-  }
-  return absmax;
-}
-
-// Eight bf16 values -> their int8-grid codes rint(x * mul) clamped to
-// [-127, 127], as bf16 (exact), same positions.
-__device__ __forceinline__ uint4 quantise8(uint4 v, float mul) {
-  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const float mul = absmax > 0.f ? __fdiv_rn(127.f, absmax) : 0.f;
+#pragma unroll 1
+  for (int reg = 0; reg < 4; ++reg)
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float a = fminf(127.f, fmaxf(-127.f, rintf(__uint_as_float(w[e] << 16) * mul)));
-    const float b = fminf(127.f, fmaxf(-127.f, rintf(__uint_as_float(w[e] & 0xffff0000u) * mul)));
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    w[e] = *reinterpret_cast<uint32_t*>(&h);
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// Q per-row quantise into TMEM (step a1); returns s_q * sm_scale * log2(e).
-// PA_Q_BF16: Q's bf16 bits go to TMEM unchanged, s_q = 1.  PA_Q_INT8: codes
-// on the pages' grid, s_q = absmax / 127.  64 columns of every row per round;
-// the loads of the next round are in flight while one round is stored.
-template <bool kInt8>
-__device__ __forceinline__ float q_prologue(const AttnParams& p, const LaneRows& lr, float absmax, uint8_t* stage,
-                                            uint32_t tq, int lane) {
-  float s_q = 1.f, mul = 1.f;
-  if (kInt8) {
-    mul = absmax > 0.f ? __fdiv_rn(127.f, absmax) : 0.f;
-    s_q = __fdiv_rn(absmax, 127.f);
-  }
-  float mk[8];  // the scale of each row this lane loads
-  if (kInt8) {
+    for (int pc = 0; pc < 8; ++pc) {
+      uint4* a = swz(qs + reg * kRegionBytes, r, pc);
+      const uint4 v = *a;
+      uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int k = 0; k < 8; ++k) mk[k] = __shfl_sync(0xffffffffu, mul, 4 * k + (lane >> 3));
-  }
-  const int pc = lane & 7;
-  const uint4 zero = make_uint4(0, 0, 0, 0);
-  uint4 v[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k)
-    v[k] = (lr.valid >> k) & 1u ? __ldg(reinterpret_cast<const uint4*>(p.q + (size_t)lr.row[k] * kHeadDim) + pc) : zero;
-#pragma unroll
-  for (int cb = 0; cb < 4; ++cb) {
-    uint4 vn[8];
-    if (cb < 3) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        vn[k] = (lr.valid >> k) & 1u
-                    ? __ldg(reinterpret_cast<const uint4*>(p.q + (size_t)lr.row[k] * kHeadDim + (cb + 1) * 64) + pc)
-                    : zero;
+      for (int e = 0; e < 4; ++e) {
+        const float lo = fminf(127.f, fmaxf(-127.f, rintf(__uint_as_float(w[e] << 16) * mul)));
+        const float hi = fminf(127.f, fmaxf(-127.f, rintf(__uint_as_float(w[e] & 0xffff0000u) * mul)));
+        __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+        w[e] = *reinterpret_cast<uint32_t*>(&b);
+      }
+      *a = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    if (kInt8) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = quantise8(v[k], mk[k]);
-    }
-    __syncwarp();  // the previous round's reads of the stage are done
-#pragma unroll
-    for (int k = 0; k < 8; ++k) *stage_at(stage, 4 * k + (lane >> 3), pc) = v[k];
-    __syncwarp();
-    uint32_t pk[32];
-#pragma unroll
-    for (int pp = 0; pp < 8; ++pp) {
-      const uint4 u = *stage_at(stage, lane, pp);
-      pk[4 * pp] = u.x;
-      pk[4 * pp + 1] = u.y;
-      pk[4 * pp + 2] = u.z;
-      pk[4 * pp + 3] = u.w;
-    }
-    tmem_st32(tq + cb * 32, pk);
-    if (cb < 3) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = vn[k];
-    }
-  }
-  return s_q * p.sm_scale_log2;
+  return __fdiv_rn(absmax, 127.f) * p.sm_scale_log2;
 }
 
 // out = O / l (x s_p on the u8 grid) -> bf16 (step a8), 64 columns per round.
@@ -555,13 +569,13 @@ __device__ __forceinline__ bool epilogue(const AttnParams& p, const Ctx& c, cons
     }
     __syncwarp();  // the previous round's reads of the stage are done
 #pragma unroll
-    for (int pp = 0; pp < 8; ++pp) *stage_at(stage, lane, pp) = make_uint4(w[4 * pp], w[4 * pp + 1], w[4 * pp + 2], w[4 * pp + 3]);
+    for (int pp = 0; pp < 8; ++pp) *swz(stage, lane, pp) = make_uint4(w[4 * pp], w[4 * pp + 1], w[4 * pp + 2], w[4 * pp + 3]);
     __syncwarp();
 #pragma unroll
     for (int k = 0; k < 8; ++k)
       if ((lr.valid >> k) & 1u)
         *(reinterpret_cast<uint4*>(p.out + (size_t)lr.row[k] * kHeadDim + cb * 64) + pc) =
-            *stage_at(stage, 4 * k + (lane >> 3), pc);
+            *swz(stage, 4 * k + (lane >> 3), pc);
   }
   return true;
 }
@@ -582,23 +596,13 @@ __device__ __forceinline__ void role_correction(const AttnParams& p, const Ctx& 
   for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++k_unit) {
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
-    const RowInfo ri = row_info(p, un, sg, r);
-    // fetch this unit's Q rows only when the previous unit is close to its
-    // end: fetched earlier, they would be evicted from L2 before use
-    if (k_unit > 0 && !(ok = c.warp_wait(B_QSOON, (k_unit - 1) & 1, 43))) break;
-    if (ri.valid) bulk_prefetch_l2(p.q + ri.off, kHeadDim * 2);
-    const float absmax = p.q_mode == 1 ? q_absmax(p, ri) : 0.f;
-    const LaneRows lr = lane_rows(p, un, sg, qd, lane);
-    // Q of this unit may replace the previous unit's once its last QK^T is done
-    if (k_unit > 0 && !(ok = c.warp_wait(B_QEMPTY, (k_unit - 1) & 1, 40))) break;
-    tc_fence_after();
-    const uint32_t tq = c.tb + lane_off + kTmQ;
-    c_rows[(k_unit & 1) * kRows + r] =
-        p.q_mode == 1 ? q_prologue<true>(p, lr, absmax, stage, tq, lane) : q_prologue<false>(p, lr, absmax, stage, tq, lane);
-    tmem_wait_st();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(c.bar(B_QFULL));
+    if (p.q_mode == 1) {  // the unit's Q codes, in place, before the MMA may read Q
+      if (!(ok = c.warp_wait(B_QFULL, k_unit & 1, 40))) break;
+      c_rows[(k_unit & 1) * kRows + r] = q_codes_int8(p, sm + kSmQ, r);
+      fence_proxy_async_shared();  // generic-proxy writes, read next by the tensor core
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(B_QREADY));
+    }
     if (k_unit > 0)
       ok = epilogue(p, c, lane_rows(p, prev_un, prev_sg, qd, lane), k_unit - 1, c.tb + lane_off + kTmO, l_rows,
                     sp_rows, r, stage, lane);
@@ -608,7 +612,6 @@ __device__ __forceinline__ void role_correction(const AttnParams& p, const Ctx& 
   if (ok && k_unit > 0)
     (void)epilogue(p, c, lane_rows(p, prev_un, prev_sg, qd, lane), k_unit - 1, c.tb + lane_off + kTmO, l_rows,
                    sp_rows, r, stage, lane);
-  tmem_wait_st();
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -623,28 +626,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   c.wc = WaitCtl{p.err, p.wait_ns};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kSmTmemSlot);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kSlots; ++s) {
-      mbar_init(c.bar(B_KFULL + s), 1);
-      mbar_init(c.bar(B_KEMPTY + s), 8);  // every softmax warp, after reading the K scales
-      mbar_init(c.bar(B_VFULL + s), 1);
-      mbar_init(c.bar(B_VEMPTY + s), 1);
+    for (int r = 0; r < 4; ++r) {
+      mbar_init(c.bar(B_KFULL + r), 1);
+      mbar_init(c.bar(B_KEMPTY + r), 1);
     }
     for (int b = 0; b < 2; ++b) {
+      mbar_init(c.bar(B_VFULL + b), 1);
+      mbar_init(c.bar(B_VEMPTY + b), 1);
+      mbar_init(c.bar(B_SCFULL + b), 1);
+      mbar_init(c.bar(B_SCEMPTY + b), 8);  // every softmax warp, after reading the scales
       mbar_init(c.bar(B_SFULL + b), 1);
       mbar_init(c.bar(B_PFULL + b), 8);
+      mbar_init(c.bar(B_STATS + b), 8);
     }
-    mbar_init(c.bar(B_QFULL), 4);
+    mbar_init(c.bar(B_QFULL), 1);
+    mbar_init(c.bar(B_QREADY), 4);
     mbar_init(c.bar(B_QEMPTY), 1);
     mbar_init(c.bar(B_OFULL), 1);
     mbar_init(c.bar(B_OEMPTY), 4);
-    mbar_init(c.bar(B_STATS), 8);
-    mbar_init(c.bar(B_STATS + 1), 8);
     mbar_init(c.bar(B_STALL), 1);
     mbar_init(c.bar(B_DRAIN), 1);
     mbar_init(c.bar(B_QSOON), 1);
     fence_mbar_init();
     tma_prefetch_map(&m.k);
     tma_prefetch_map(&m.v);
+    tma_prefetch_map(&m.q);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -652,20 +658,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // scale slots start at zero: columns past a tile's width then hold finite
   // stale scales, which the softmax multiplies by p = 0
-  for (int i = threadIdx.x; i < kSlots * 128; i += kThreads) reinterpret_cast<float*>(sm + kSmScale)[i] = 0.f;
+  for (int i = threadIdx.x; i < 2 * 256; i += kThreads) reinterpret_cast<float*>(sm + kSmScale)[i] = 0.f;
   fence_proxy_async_shared();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   c.tb = *tmem_slot;
 
+  const bool lane0 = (threadIdx.x & 31) == 0;
   if (warp == 0) {
-    if ((threadIdx.x & 31) == 0) role_producer(p, m, c);
+    if (lane0) role_producer_k(p, m, c);
   } else if (warp == 1) {
-    if ((threadIdx.x & 31) == 0) role_mma(p, c);
-  } else if (warp >= 4 && warp < 12) {
+    if (lane0) role_mma(p, c);
+  } else if (warp == 2) {
+    if (lane0) role_producer_v(p, m, c);
+  } else if (warp == 3) {
+    if (lane0) role_producer_q(p, m, c);
+  } else if (warp < 12) {
     role_softmax(p, c, sm);
-  } else if (warp >= 12) {
+  } else {
     role_correction(p, c, sm);
   }
 

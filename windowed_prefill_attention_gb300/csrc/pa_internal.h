@@ -64,8 +64,9 @@ struct AttnParams {
 };
 
 struct AttnMaps {
-  CUtensorMap k;   // Kw  [HKV][n_tok][256] fp16, box {64, 64, 1}
-  CUtensorMap v;   // Vt  [HKV][256][n_tok] fp16, box {64, 256, 1}
+  CUtensorMap k;   // Kw  [HKV][n_tok][256] bf16, box {64, 128, 1}: one 64-dim region of a key tile
+  CUtensorMap v;   // Vt  [HKV][256][n_tok] fp16, box {64, 256, 1}: one 64-key chunk
+  CUtensorMap q;   // q   [tokens][HQ][256] bf16, box {64, G, TQ}: one region of a unit's 128 rows
 };
 
 // Launchers (return the launch's cudaError_t).

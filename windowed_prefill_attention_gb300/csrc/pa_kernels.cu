@@ -148,7 +148,7 @@ __global__ void debug_maskset_kernel(const SeqGeom* seqs, const Unit* units, int
         if (nblk < cap) unit_blocks[(size_t)blockIdx.x * cap + nblk] = tg.kb0 + b;
         ++nblk;
       }
-    count += __popcll(visible_columns(tg, t_row, S, W));
+    count += __popcll(visible_columns(tg, t_row, S, W, 0)) + __popcll(visible_columns(tg, t_row, S, W, 1));
   }
   if (r == 0)
     for (int k = nblk; k < cap; ++k) unit_blocks[(size_t)blockIdx.x * cap + k] = -1;

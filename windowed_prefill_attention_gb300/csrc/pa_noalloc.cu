@@ -167,7 +167,10 @@ extern "C" int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_page
                     (uint64_t)cap * kHeadDim * 2, 64, kTileKeys, 1)))
     return rc;
   if ((rc = encode3(&m.v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, vt, n_rows, kHeadDim, n_kv_heads, (uint64_t)cap * 2,
-                    (uint64_t)cap * kHeadDim * 2, kTileKeys, kHeadDim, 1)))
+                    (uint64_t)cap * kHeadDim * 2, kChunkKeys, kHeadDim, 1)))
+    return rc;
+  if ((rc = encode3(&m.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, kHeadDim, n_q_heads, n_q, kHeadDim * 2,
+                    (uint64_t)n_q_heads * kHeadDim * 2, 64, G, TQ)))
     return rc;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);

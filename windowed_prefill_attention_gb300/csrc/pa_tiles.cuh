@@ -18,7 +18,7 @@
 // Key tiles: the unit's visible key blocks form at most two runs, the sink run
 // [0, S) and the window run [lo(first block), last block]; when they touch they
 // merge into one run from block 0.  Each run is cut into tiles of up to
-// kTileBlocks 16-key blocks (64 keys).  Masked blocks are never visited.
+// kTileBlocks 16-key blocks (128 keys).  Masked blocks are never visited.
 #pragma once
 
 #ifdef __CUDACC__
@@ -32,8 +32,9 @@ namespace pa {
 constexpr int kPage = 16;         // tokens per KV page (= mask block)
 constexpr int kHeadDim = 256;     // head dimension
 constexpr int kRows = 128;        // query rows per work unit (MMA M)
-constexpr int kTileBlocks = 4;    // 16-key blocks per key tile
-constexpr int kTileKeys = kTileBlocks * kPage;  // 64
+constexpr int kTileBlocks = 8;    // 16-key blocks per key tile
+constexpr int kTileKeys = kTileBlocks * kPage;  // 128
+constexpr int kChunkKeys = 64;    // keys per V^T chunk (PV works through a tile in chunks)
 
 PA_HD int imin(int a, int b) { return a < b ? a : b; }
 PA_HD int imax(int a, int b) { return a > b ? a : b; }
@@ -143,13 +144,14 @@ PA_HD unsigned long long low_bits(int n) {
   return n <= 0 ? 0ull : (n >= 64 ? ~0ull : ((1ull << n) - 1ull));
 }
 
-// Which of a tile's 64 key columns query token t sees, as a bit mask: the
-// tile's width and, where the tile needs masking, the causal bound (key <= t)
-// and the sink / window test (key block < S, or >= lo = max(0, t/16 + 1 - W)).
-// This is the mask the softmax applies, one bit test per score.
-PA_HD unsigned long long visible_columns(const TileGeom& tg, int t, int S, int W) {
-  const int key0 = tg.kb0 * kPage;
-  unsigned long long v = low_bits(tg.nb * kPage);
+// Which of the 64 key columns [64 half, 64 half + 64) of a tile query token t
+// sees, as a bit mask: the tile's width and, where the tile needs masking, the
+// causal bound (key <= t) and the sink / window test (key block < S, or
+// >= lo = max(0, t/16 + 1 - W)).  This is the mask the softmax applies, one
+// bit test per score.
+PA_HD unsigned long long visible_columns(const TileGeom& tg, int t, int S, int W, int half) {
+  const int key0 = tg.kb0 * kPage + 64 * half;
+  unsigned long long v = low_bits(tg.nb * kPage - 64 * half);
   if (tg.needs_mask) {
     v &= low_bits(t - key0 + 1);
     if (W > 0) {
