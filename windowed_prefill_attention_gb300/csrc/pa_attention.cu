@@ -315,7 +315,6 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
       // Every path through a tile passes the pair barrier the same number of
       // times, so a wait that runs out in one warp cannot strand its partner.
       bool okl = c.warp_wait(B_SFULL + (t & 1), (t >> 1) & 1, 31);
-      okl = okl && c.warp_wait(B_SCFULL + (t & 1), (t >> 1) & 1, 32);
       const uint32_t sd = c.tb + lane_off + kTmS + (t & 1) * kTileKeys + 64 * h;
       // this half's K scales (64 floats); its V scales follow 512 bytes later
       const float4* ks4 = reinterpret_cast<const float4*>(sm + kSmScale + (t & 1) * 1024 + 256 * h);
@@ -327,6 +326,9 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
         uint32_t sa[32], sb[32];
         tmem_ld32(sd, sa);
         tmem_ld32(sd + 32, sb);
+        // the tile's scales (normally there long since), checked while the
+        // score loads are in flight
+        okl = c.warp_wait(B_SCFULL + (t & 1), (t >> 1) & 1, 32);
         tmem_wait_ld(sa);
         reg_fence(sb);
         // y = S * k_scale (masked: -inf), and this half's row maximum
