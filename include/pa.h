@@ -62,7 +62,7 @@ extern "C" {
 #define PA_Q_INT8 1  /* the pages' grid: scale absmax/127, codes rint(q*127/absmax) in [-127,127] */
 /* P container (step "V scale folded into P, P quantised per row"). */
 #define PA_P_F16 0   /* default: P' = p * v_scale rounded to fp16 (11-bit significand) */
-#define PA_P_U8 1    /* the pages' grid per row and 64-key tile: scale max/255, codes in [0,255] */
+#define PA_P_U8 1    /* the pages' grid per row and 128-key tile: scale max/255, codes in [0,255] */
 
 typedef struct pa_ctx* pa_handle;
 
@@ -83,7 +83,7 @@ typedef struct {
   int n_ctx;    /* context tokens in the pool; q_start + n_q <= n_ctx */
 } pa_seq;
 
-/* Fill *opt with the defaults (fp16 containers, 2000 ms waits, no timing, no test hook). */
+/* Fill *opt with the defaults (bf16 query as given, fp16 P', 2000 ms waits, no timing, no test hook). */
 void pa_default_options(pa_options* opt);
 
 /* Create a handle bound to the current CUDA device.  head_dim must be 256 and
