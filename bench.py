@@ -246,9 +246,13 @@ def run_ours(args, wl):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     h = pa.pa_create(wl.n_q_heads, wl.n_kv_heads, inp.k_pool.shape[0], inp.block_table.shape[1], record_timing=True)
     seqs, S, W, sm = inp.seq_desc, wl.n_sink_blk, wl.n_win_blk, wl.sm_scale
+    q_gate = None
+    if args.gate:  # the output gate fused into the epilogue: out * sigmoid(q_gate)
+        from synth import make_gate
+        q_gate = torch.from_numpy(make_gate(inp).view(np.int16)).view(torch.bfloat16).to(dev)
 
     def step():
-        pa.pa_prefill_batch(h, seqs, q, kp, vp, ks, vs, bt, S, W, sm, out)
+        pa.pa_prefill_batch(h, seqs, q, kp, vp, ks, vs, bt, S, W, sm, out, q_gate=q_gate)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -313,9 +317,10 @@ def run_ours(args, wl):
         "tokens_per_s": world * tokens * args.steps / (total_ms / 1e3),
         "algorithmic_ops_per_step": ops,
         "gpu_launches": 2 * args.steps,
+        "output_gate": bool(args.gate),
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_s * 1e3, "call": "pa_prefill_host (pinned host buffers)"},
+                "ms_per_step": e2e_s * 1e3, "call": "pa_prefill_host (pinned host buffers, no output gate)"},
         "roofline": {"bound": "tensor", "kernel": "attention_kernel", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_src,
                      "traffic": profiled_traffic(wl.name), "launch_ms": attn_avg_ms,
@@ -338,6 +343,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="32k", choices=sorted(CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gate", action="store_true", help="fuse the output gate out * sigmoid(q_gate) (extra row)")
     args = ap.parse_args()
     wl = CONFIGS[args.config]
     if args.impl == "reference":

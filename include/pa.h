@@ -109,6 +109,19 @@ int pa_prefill_batch(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, 
                      const int8_t* v_pool, const float* k_scale, const float* v_scale, const int32_t* block_table,
                      int n_sink_blk, int n_win_blk, float sm_scale, void* out, void* stream);
 
+/* pa_prefill_batch with the output gate fused into the epilogue ("int8
+ * tensor-core prefill attention", section "Correctness": the attention output
+ * is multiplied by sigmoid(q_gate) before the next layer):
+ *   out[t][h][d] = bf16( bf16(attention[t][h][d]) * sigmoid(q_gate[t][h][d]) )
+ * i.e. the value a separate elementwise gate kernel would produce from the
+ * ungated bf16 output.  q_gate is a device pointer, bf16 [total_q][n_q_heads]
+ * [256] like q and out, 16-byte aligned, caller-owned, read once.  Errors as
+ * pa_prefill_batch; PA_EINVAL for a NULL or misaligned q_gate. */
+int pa_prefill_batch_gated(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const void* q_gate,
+                           const int8_t* k_pool, const int8_t* v_pool, const float* k_scale, const float* v_scale,
+                           const int32_t* block_table, int n_sink_blk, int n_win_blk, float sm_scale, void* out,
+                           void* stream);
+
 /* pa_prefill_batch on HOST buffers: copies the inputs to handle-owned device
  * memory on `stream`, runs, copies out back and synchronises the stream; the
  * return value includes device-side errors.  Pinned host memory is fastest. */
@@ -152,7 +165,7 @@ int pa_debug_maskset(pa_handle h, int n_seq, const pa_seq* seqs, int n_sink_blk,
                      int32_t* row_counts, int32_t* unit_blocks, int cap, int32_t* units_out, int units_cap,
                      int* n_units, void* stream);
 
-/* Allocation-free variant of pa_prefill (one sequence, default fp16
+/* Allocation-free variant of pa_prefill (one sequence, default
  * containers).  The pages have no counterpart of this entry point: it exists
  * for callers that may not call cudaMalloc / cudaFree, for example an engine
  * that has reserved nearly all device memory for its own KV-cache pool and

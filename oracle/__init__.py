@@ -9,7 +9,9 @@ It is a plain fp64 CPU implementation (``pa_oracle.c``) of
   sections "Why the attention, and why tensor cores" and "Relation to open PRs";
   "fp16 shared-memory tiles for windowed prefill attention", "Summary"), and
 * the pages' quantised method, step by step (int8 Q per row, integer scores,
-  online softmax over key tiles, V scale folded into P, P quantised per row).
+  online softmax over key tiles, V scale folded into P, P quantised per row),
+* the output gate that follows it on the pages' path, out * sigmoid(q_gate)
+  ("int8 tensor-core prefill attention", section "Correctness").
 
 It shares no code with the CUDA path.  Parity pins live in tests/.
 """
@@ -107,6 +109,15 @@ def exact(prob: Problem, rows: np.ndarray, n_threads: int = 0) -> np.ndarray:
     if lib().pa_oracle_exact(C.byref(prob.s), rows.shape[0], _ptr(rows), _ptr(out), _threads(n_threads)):
         raise ValueError("row outside every sequence")
     return out
+
+
+def gate(out_rows: np.ndarray, gate_rows: np.ndarray) -> np.ndarray:
+    """The gated attention output out * sigmoid(g), elementwise, in fp64:
+    sigmoid(g) = 1 / (1 + exp(-g)).  ``gate_rows`` are the gate values of the
+    same (row, head) pairs as ``out_rows`` (any float dtype)."""
+    g = np.asarray(gate_rows, dtype=np.float64)
+    with np.errstate(over="ignore"):  # exp(-g) = inf for g << 0 gives sigmoid 0, as it should
+        return np.asarray(out_rows, dtype=np.float64) * (1.0 / (1.0 + np.exp(-g)))
 
 
 def method(prob: Problem, rows: np.ndarray, q_mode: int, p_mode: int, tile: int = 64,

@@ -3,4 +3,4 @@
 This package only synthesises inputs (shapes, value distributions, page
 placement); none of the attention arithmetic lives here.
 """
-from .workloads import CONFIGS, Workload, Inputs, make_inputs  # noqa: F401
+from .workloads import CONFIGS, Workload, Inputs, make_inputs, make_gate  # noqa: F401

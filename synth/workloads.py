@@ -188,3 +188,16 @@ def make_inputs(wl: Workload) -> Inputs:
         desc.append((off, qs, nq, qs + nq))
         off += nq
     return Inputs(wl, q, k_pool, v_pool, k_scale, v_scale, bt, np.asarray(desc, dtype=np.int32))
+
+
+def make_gate(inp: Inputs) -> np.ndarray:
+    """Output-gate pre-activations for the gated attention output, bf16 bit
+    patterns shaped like q: N(0, 2) from a generator of its own (so every other
+    input is unchanged), with 0.1 % of entries at +-40 so that the sigmoid's
+    saturated ends are exercised."""
+    rng = np.random.default_rng(inp.wl.seed + 7919)
+    g = rng.normal(0.0, 2.0, size=inp.q.shape).astype(np.float32)
+    n_ext = max(1, g.size // 1000)
+    idx = rng.choice(g.size, size=n_ext, replace=False)
+    g.reshape(-1)[idx] = rng.choice(np.array([-40.0, 40.0], dtype=np.float32), size=n_ext)
+    return _to_bf16_bits(g)

@@ -18,8 +18,10 @@ def to_device(inp, device="cuda"):
                 block_table=torch.from_numpy(inp.block_table).to(device))
 
 
-def run_gpu(inp, S=None, W=None, sm_scale=None, **opts):
-    """One pa_prefill_batch call; returns (out as float32 numpy [total_q, HQ, D], device status)."""
+def run_gpu(inp, S=None, W=None, sm_scale=None, gate_bits=None, **opts):
+    """One pa_prefill_batch call (pa_prefill_batch_gated when gate_bits, bf16 bit
+    patterns shaped like q, is given); returns (out as float32 numpy [total_q,
+    HQ, D], device status)."""
     import torch
 
     import windowed_prefill_attention_gb300 as pa
@@ -31,8 +33,11 @@ def run_gpu(inp, S=None, W=None, sm_scale=None, **opts):
     out = torch.full_like(d["q"], float("nan"))
     h = pa.pa_create(wl.n_q_heads, wl.n_kv_heads, inp.k_pool.shape[0], inp.block_table.shape[1], **opts)
     try:
+        q_gate = None
+        if gate_bits is not None:
+            q_gate = torch.from_numpy(np.ascontiguousarray(gate_bits).view(np.int16)).view(torch.bfloat16).cuda()
         pa.pa_prefill_batch(h, inp.seq_desc, d["q"], d["k_pool"], d["v_pool"], d["k_scale"], d["v_scale"],
-                            d["block_table"], S, W, sm_scale, out)
+                            d["block_table"], S, W, sm_scale, out, q_gate=q_gate)
         rc = pa.pa_last_error(h)
     finally:
         pa.pa_destroy(h)

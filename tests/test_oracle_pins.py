@@ -267,3 +267,17 @@ def test_f16_p_rounding_is_exact_on_dyadic_values():
     a = oracle.exact(prob, rows)
     b = oracle.method(prob, rows, oracle.Q_LOSSLESS, oracle.P_F16, tile=64)
     assert norm_err(b, a).max() < 1e-12
+
+
+def test_gate_against_library_sigmoid_and_special_values():
+    """The output gate (out * sigmoid(g)) against scipy's logistic function on
+    random values and on the special points: sigmoid(0) = 1/2 exactly, the
+    saturated ends, and sigmoid(x) + sigmoid(-x) = 1."""
+    rng = np.random.default_rng(5)
+    out = rng.normal(size=(64, 256))
+    g = rng.normal(0.0, 3.0, size=(64, 256))
+    np.testing.assert_allclose(oracle.gate(out, g), out * scipy.special.expit(g), rtol=1e-14, atol=0)
+    assert np.array_equal(oracle.gate(out, np.zeros_like(g)), out * 0.5)
+    np.testing.assert_allclose(oracle.gate(out, np.full_like(g, 40.0)), out, rtol=1e-15)
+    assert np.all(np.abs(oracle.gate(out, np.full_like(g, -800.0))) == 0.0)
+    np.testing.assert_allclose(oracle.gate(out, g) + oracle.gate(out, -g), out, rtol=1e-13, atol=1e-15)

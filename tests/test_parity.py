@@ -28,14 +28,14 @@ import numpy as np
 import pytest
 
 import oracle
-
-# keys per tile of the kernel: the u8 grid of P' is per row and per tile
-KEY_TILE = 128
 from pa_testutil import TOL_MAX, TOL_MEAN, compare, norm_errors, run_gpu, sample_rows
 from synth import CONFIGS, make_inputs
 from synth.workloads import Workload
 
 pytestmark = pytest.mark.gpu
+
+# keys per tile of the kernel: the u8 grid of P' is per row and per tile
+KEY_TILE = 128
 
 FULL = {
     "tiny": None,       # all rows
@@ -183,3 +183,34 @@ def test_host_buffer_entry_point_matches_device_entry_point(inputs):
         pa.pa_destroy(h)
     b = out.view(torch.bfloat16).float().numpy()
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("name", ["tiny", "4k", "32k"])
+def test_output_gate_matches_oracle(name):
+    """pa_prefill_batch_gated against the fp64 definition of the gated output."""
+    from synth import make_gate
+    from synth.workloads import bf16_bits_to_f32
+    inp = make_inputs(CONFIGS[name])
+    g_bits = make_gate(inp)
+    out, rc = run_gpu(inp, gate_bits=g_bits)
+    assert rc == 0
+    n = FULL.get(name)
+    rows = oracle.all_rows(inp) if n is None else sample_rows(inp, n, seed=11)
+    ref = oracle.gate(oracle.exact(oracle.Problem.from_inputs(inp), rows),
+                      bf16_bits_to_f32(g_bits)[rows[:, 0], rows[:, 1]])
+    got = out[rows[:, 0], rows[:, 1]].astype(np.float64)
+    assert np.isfinite(got).all()
+    mx, mean = norm_errors(got, ref)
+    assert mx <= TOL_MAX and mean <= TOL_MEAN, (name, mx, mean)
+
+
+def test_output_gate_special_values_bitwise():
+    """Gate 0 halves the ungated bf16 output exactly; gate +40 (sigmoid = 1 in
+    fp32) returns it unchanged."""
+    inp = make_inputs(CONFIGS["4k"])
+    plain, rc0 = run_gpu(inp)
+    half, rc1 = run_gpu(inp, gate_bits=np.zeros_like(inp.q))
+    one, rc2 = run_gpu(inp, gate_bits=np.full_like(inp.q, 0x4220))  # bf16 40.0
+    assert rc0 == rc1 == rc2 == 0
+    assert np.array_equal(half, plain * 0.5)
+    assert np.array_equal(one, plain)

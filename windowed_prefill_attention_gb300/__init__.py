@@ -27,7 +27,8 @@ PA_NOALLOC_SCRATCH_BYTES = 32 << 20
 PA_Q_BF16, PA_Q_INT8 = 0, 1
 PA_P_F16, PA_P_U8 = 0, 1
 
-EXPORTED = ("pa_default_options", "pa_create", "pa_destroy", "pa_prefill", "pa_prefill_batch", "pa_prefill_host",
+EXPORTED = ("pa_default_options", "pa_create", "pa_destroy", "pa_prefill", "pa_prefill_batch",
+            "pa_prefill_batch_gated", "pa_prefill_host",
             "pa_last_error", "pa_timing", "pa_strerror", "pa_plan", "pa_debug_gather", "pa_debug_maskset",
             "pa_prefill_noalloc")
 
@@ -50,6 +51,7 @@ _lib.pa_destroy.restype = None
 _lib.pa_prefill.argtypes = [_vp] + [_vp] * 6 + [_i] * 5 + [_f, _vp, _vp]
 _lib.pa_prefill_batch.argtypes = [_vp, _i, C.POINTER(pa_seq)] + [_vp] * 6 + [_i, _i, _f, _vp, _vp]
 _lib.pa_prefill_host.argtypes = _lib.pa_prefill_batch.argtypes
+_lib.pa_prefill_batch_gated.argtypes = [_vp, _i, C.POINTER(pa_seq)] + [_vp] * 7 + [_i, _i, _f, _vp, _vp]
 _lib.pa_last_error.argtypes = [_vp, _vp]
 _lib.pa_timing.argtypes = [_vp, _i, C.POINTER(C.c_double), C.POINTER(C.c_double), C.POINTER(_i)]
 _lib.pa_strerror.argtypes = [_i]
@@ -152,12 +154,18 @@ def pa_prefill(h, q, k_pool, v_pool, k_scale, v_scale, block_table, q_start, n_q
 
 
 def pa_prefill_batch(h, seqs, q, k_pool, v_pool, k_scale, v_scale, block_table, n_sink_blk, n_win_blk, sm_scale,
-                     out, stream=None) -> None:
+                     out, stream=None, q_gate=None) -> None:
+    """q_gate (bf16, shaped like out) selects pa_prefill_batch_gated."""
     import torch
     s = _seqs(seqs)
     args = _dev_inputs(q, k_pool, v_pool, k_scale, v_scale, block_table)
-    _check(_lib.pa_prefill_batch(h, len(s), s, *args, n_sink_blk, n_win_blk, float(sm_scale),
-                                 _dev(out, torch.bfloat16, "out"), _stream(stream)), "pa_prefill_batch")
+    if q_gate is None:
+        _check(_lib.pa_prefill_batch(h, len(s), s, *args, n_sink_blk, n_win_blk, float(sm_scale),
+                                     _dev(out, torch.bfloat16, "out"), _stream(stream)), "pa_prefill_batch")
+    else:
+        _check(_lib.pa_prefill_batch_gated(h, len(s), s, args[0], _dev(q_gate, torch.bfloat16, "q_gate"), *args[1:],
+                                           n_sink_blk, n_win_blk, float(sm_scale), _dev(out, torch.bfloat16, "out"),
+                                           _stream(stream)), "pa_prefill_batch_gated")
 
 
 def pa_prefill_host(h, seqs, q, k_pool, v_pool, k_scale, v_scale, block_table, n_sink_blk, n_win_blk, sm_scale,

@@ -299,9 +299,10 @@ cudaEvent_t take_event(pa_handle h) {
 
 int run(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* kp, const int8_t* vp,
         const float* ksc, const float* vsc, const int32_t* bt, int S, int W, float sm_scale, void* out,
-        cudaStream_t st) {
+        cudaStream_t st, const void* gate = nullptr) {
   int rc = check_inputs(h, q, kp, vp, ksc, vsc, bt, out);
   if (rc) return rc;
+  if (gate && !aligned(gate, 16)) return PA_EINVAL;
   if (!(sm_scale == sm_scale) || sm_scale < 0.f) return PA_EINVAL;
   if ((rc = prepare(h, n_seq, seqs, S, W, st))) return rc;
   const Plan& P = h->plan;
@@ -353,6 +354,7 @@ int run(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t*
   a.vs = h->vs;
   a.vsmax = h->vsmax;
   a.out = static_cast<__nv_bfloat16*>(out);
+  a.gate = static_cast<const __nv_bfloat16*>(gate);
   a.HQ = h->HQ;
   a.HKV = h->HKV;
   a.G = h->G;
@@ -473,6 +475,15 @@ int pa_prefill_batch(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, 
                      int n_sink_blk, int n_win_blk, float sm_scale, void* out, void* stream) {
   return run(h, n_seq, seqs, q, k_pool, v_pool, k_scale, v_scale, block_table, n_sink_blk, n_win_blk, sm_scale, out,
              static_cast<cudaStream_t>(stream));
+}
+
+int pa_prefill_batch_gated(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const void* q_gate,
+                           const int8_t* k_pool, const int8_t* v_pool, const float* k_scale, const float* v_scale,
+                           const int32_t* block_table, int n_sink_blk, int n_win_blk, float sm_scale, void* out,
+                           void* stream) {
+  if (!q_gate) return PA_EINVAL;
+  return run(h, n_seq, seqs, q, k_pool, v_pool, k_scale, v_scale, block_table, n_sink_blk, n_win_blk, sm_scale, out,
+             static_cast<cudaStream_t>(stream), q_gate);
 }
 
 int pa_prefill_host(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* k_pool,

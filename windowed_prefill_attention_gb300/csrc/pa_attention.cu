@@ -23,12 +23,13 @@
 // Each K region slot is released by the commit after the four k-steps that
 // read it, so region r of the next tile loads while this tile's later regions
 // are multiplied.  Roles:
-//   warp 0        TMA producer of the K regions
+//   warp 0        TMA producer of the K regions (one lane per region)
 //   warp 1        TMEM allocator and the single MMA-issuing thread; QK^T(j+1)
 //                 is issued before PV(j), so the tensor core works on the next
 //                 scores while the softmax handles the current ones
-//   warp 2        TMA producer of the V^T chunks
-//   warp 3        producer of Q (TMA, after an L2 prefetch) and of the scales
+//   warp 2        TMA producer of the V^T chunks (one lane per slot)
+//   warp 3        producer of Q (TMA, one lane per region, after an L2
+//                 prefetch) and of the scales
 //   warps 4-11    softmax: one query row per thread (TMEM lane = row), two
 //                 warps per lane quadrant, each owning 64 of the 128 key columns
 //   warps 12-15   epilogue of each unit (and Q codes on the int8 grid)
@@ -110,34 +111,37 @@ struct Ctx {
 };
 
 // ------------------------------------------------------------------ producers
-// K: per tile, region r (dims [64r, 64r+64), 128 keys) into slot r.  Slot r
-// is used once per tile, so its phases follow the tile counter.
-__device__ __forceinline__ void role_producer_k(const AttnParams& p, const AttnMaps& m, const Ctx& c) {
+// A thread's TMA copies complete about one at a time (measured on GB300: one
+// issuing thread moves ~29-36 B/clk of 16 KB tiles from L2 into shared memory
+// whatever the number in flight, four threads ~70 B/clk), so every stream
+// of copies is spread over several lanes, each with its own slots.
+
+// K: lane r loads region r (dims [64r, 64r+64), 128 keys) of every tile into
+// slot r.  Slot r is used once per tile, so its phases follow the tile counter.
+__device__ __forceinline__ void role_producer_k(const AttnParams& p, const AttnMaps& m, const Ctx& c, int r) {
   uint32_t kt = 0;  // tiles loaded
   bool ok = true;
   for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
     const UnitGeom ug = unit_geom(un.t0, p.TQ, sg, p.S, p.W);
-    for (int j = 0; j < ug.n_tiles && ok; ++j, ++kt) {
+    for (int j = 0; j < ug.n_tiles; ++j, ++kt) {
       const int crow = logical_block_row(sg, tile_geom(ug, j, p.S, p.W).kb0);
-      for (int r = 0; r < 4; ++r) {
-        if (!(ok = mbar_wait(c.bar(B_KEMPTY + r), (kt & 1) ^ 1, c.wc, 10))) break;
-        const uint32_t fb = c.bar(B_KFULL + r);
-        mbar_expect_tx(fb, kRegionBytes);
-        tma_load_3d(c.sbase + kSmK + r * kRegionBytes, &m.k, fb, r * 64, crow, un.g);
-      }
+      if (!(ok = mbar_wait(c.bar(B_KEMPTY + r), (kt & 1) ^ 1, c.wc, 10))) break;
+      const uint32_t fb = c.bar(B_KFULL + r);
+      mbar_expect_tx(fb, kRegionBytes);
+      tma_load_3d(c.sbase + kSmK + r * kRegionBytes, &m.k, fb, r * 64, crow, un.g);
     }
   }
-  // every issued copy lands before the CTA may exit (a load that was never
-  // issued leaves its slot's previous phase complete, which passes too)
-  if (kt > 0)
-    for (int r = 0; r < 4; ++r) (void)mbar_wait_drain(c.bar(B_KFULL + r), (kt - 1) & 1, kDrainNs);
+  // every issued copy lands before the CTA may exit
+  if (kt > 0) (void)mbar_wait_drain(c.bar(B_KFULL + r), (kt - 1) & 1, kDrainNs);
 }
 
-// V^T: per tile, its 64-key chunks into a two-slot ring.
-__device__ __forceinline__ void role_producer_v(const AttnParams& p, const AttnMaps& m, const Ctx& c) {
-  uint32_t vc = 0;  // chunks loaded
+// V^T: the tiles' 64-key chunks go through a two-slot ring; lane s loads the
+// chunks that land in slot s.
+__device__ __forceinline__ void role_producer_v(const AttnParams& p, const AttnMaps& m, const Ctx& c, int s) {
+  uint32_t vc = 0;    // chunks of all tiles so far
+  uint32_t last = 0;  // 1 + index of the last chunk this lane loaded
   bool ok = true;
   for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
     const Unit un = p.units[u];
@@ -146,26 +150,41 @@ __device__ __forceinline__ void role_producer_v(const AttnParams& p, const AttnM
     for (int j = 0; j < ug.n_tiles && ok; ++j) {
       const TileGeom tg = tile_geom(ug, j, p.S, p.W);
       const int crow = logical_block_row(sg, tg.kb0);
-      for (int ch = 0; ch < n_chunks(tg.nb); ++ch) {
-        const uint32_t s = vc & 1;
+      for (int ch = 0; ch < n_chunks(tg.nb); ++ch, ++vc) {
+        if ((int)(vc & 1) != s) continue;
         if (!(ok = mbar_wait(c.bar(B_VEMPTY + s), ((vc >> 1) & 1) ^ 1, c.wc, 11))) break;
         const uint32_t fb = c.bar(B_VFULL + s);
         mbar_expect_tx(fb, kChunkBytes);
         tma_load_3d(c.sbase + kSmV + s * kChunkBytes, &m.v, fb, crow + ch * kChunkKeys, 0, un.g);
-        ++vc;
+        last = vc + 1;
       }
     }
   }
-  for (uint32_t i = 0; i < 2; ++i)
-    if (vc > i) (void)mbar_wait_drain(c.bar(B_VFULL + ((vc - 1 - i) & 1)), ((vc - 1 - i) >> 1) & 1, kDrainNs);
+  if (last > 0) (void)mbar_wait_drain(c.bar(B_VFULL + s), ((last - 1) >> 1) & 1, kDrainNs);
 }
 
-// Q of each unit (after the previous unit's last QK^T) and the K/V scales of
-// each tile (two-slot ring by tile parity).
-__device__ __forceinline__ void role_producer_q(const AttnParams& p, const AttnMaps& m, const Ctx& c) {
+// Prefetch into L2 the rows of a unit in a [tokens][HQ][256] bf16 tensor (q or
+// the output gate): per token its G heads are contiguous.
+__device__ __forceinline__ void prefetch_unit_rows(const AttnParams& p, const __nv_bfloat16* base, const Unit& un,
+                                                   const SeqGeom& sg) {
+  const int tok0 = sg.q_off + (un.t0 - sg.q_start);
+  for (int i = 0; i < p.TQ; ++i) {
+    const int tok = tok0 + i;
+    if (tok >= sg.q_off && tok < sg.q_off + sg.n_q)
+      bulk_prefetch_l2(base + ((size_t)tok * p.HQ + (size_t)un.g * p.G) * kHeadDim, (uint32_t)p.G * kHeadDim * 2);
+  }
+}
+
+// Q of each unit (after the previous unit's last QK^T): lane r loads region r.
+// Lane 0 also prefetches into L2 the unit's Q rows and the previous unit's
+// output-gate rows (both a few tiles before they are needed) and loads the
+// K/V scales of each tile (two-slot ring by tile parity).
+__device__ __forceinline__ void role_producer_q(const AttnParams& p, const AttnMaps& m, const Ctx& c, int r) {
   uint32_t ts = 0;  // tiles whose scales were loaded
   int k_unit = 0;   // units whose Q was loaded
   bool ok = true;
+  Unit prev_un{};
+  SeqGeom prev_sg{};
   for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
@@ -175,17 +194,18 @@ __device__ __forceinline__ void role_producer_q(const AttnParams& p, const AttnM
     const int tok0 = sg.q_off + (un.t0 - sg.q_start);
     if (k_unit > 0) {
       if (!(ok = mbar_wait(c.bar(B_QSOON), (k_unit - 1) & 1, c.wc, 12))) break;
-      for (int i = 0; i < p.TQ; ++i) {
-        const int tok = tok0 + i;
-        if (tok >= sg.q_off && tok < sg.q_off + sg.n_q)
-          bulk_prefetch_l2(p.q + ((size_t)tok * p.HQ + (size_t)un.g * p.G) * kHeadDim, (uint32_t)p.G * kHeadDim * 2);
+      if (r == 0) {
+        prefetch_unit_rows(p, p.q, un, sg);
+        if (p.gate) prefetch_unit_rows(p, p.gate, prev_un, prev_sg);
       }
       if (!(ok = mbar_wait(c.bar(B_QEMPTY), (k_unit - 1) & 1, c.wc, 13))) break;
     }
-    mbar_expect_tx(c.bar(B_QFULL), 4 * kRegionBytes);
-    for (int r = 0; r < 4; ++r)
-      tma_load_3d(c.sbase + kSmQ + r * kRegionBytes, &m.q, c.bar(B_QFULL), r * 64, un.g * p.G, tok0);
+    prev_un = un;
+    prev_sg = sg;
+    mbar_expect_tx(c.bar(B_QFULL), kRegionBytes);
+    tma_load_3d(c.sbase + kSmQ + r * kRegionBytes, &m.q, c.bar(B_QFULL), r * 64, un.g * p.G, tok0);
     ++k_unit;
+    if (r != 0) continue;
     for (int j = 0; j < ug.n_tiles; ++j) {
       const uint32_t s = ts & 1;
       if (!(ok = mbar_wait(c.bar(B_SCEMPTY + s), ((ts >> 1) & 1) ^ 1, c.wc, 14))) break;
@@ -536,9 +556,27 @@ __device__ __forceinline__ float q_codes_int8(const AttnParams& p, uint8_t* qs, 
   return __fdiv_rn(absmax, 127.f) * p.sm_scale_log2;
 }
 
-// out = O / l (x s_p on the u8 grid) -> bf16 (step a8), 64 columns per round.
-// O may be overwritten once the last round's TMEM loads are done, so the
-// MMA issuer is released before the last stores.
+// Eight bf16 outputs times sigmoid of their eight bf16 gate values, rounded
+// to bf16 again (the output gate, applied to the rounded attention output as
+// a separate elementwise kernel would).
+__device__ __forceinline__ uint4 gate8(uint4 v, uint4 g) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float lo = __uint_as_float(w[e] << 16) * __fdividef(1.f, 1.f + __expf(-__uint_as_float(gw[e] << 16)));
+    const float hi =
+        __uint_as_float(w[e] & 0xffff0000u) * __fdividef(1.f, 1.f + __expf(-__uint_as_float(gw[e] & 0xffff0000u)));
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    w[e] = *reinterpret_cast<uint32_t*>(&b);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// out = O / l (x s_p on the u8 grid) -> bf16 (step a8), 64 columns per round,
+// times sigmoid(gate) when the call has an output gate.  O may be overwritten
+// once the last round's TMEM loads are done, so the MMA issuer is released
+// before the last stores.
 __device__ __forceinline__ bool epilogue(const AttnParams& p, const Ctx& c, const LaneRows& lr, int k_unit,
                                          uint32_t to, const float* l_rows, const float* sp_rows, int r,
                                          uint8_t* stage, int lane) {
@@ -573,11 +611,24 @@ __device__ __forceinline__ bool epilogue(const AttnParams& p, const Ctx& c, cons
 #pragma unroll
     for (int pp = 0; pp < 8; ++pp) *swz(stage, lane, pp) = make_uint4(w[4 * pp], w[4 * pp + 1], w[4 * pp + 2], w[4 * pp + 3]);
     __syncwarp();
+    if (p.gate) {
+      uint4 g[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      if ((lr.valid >> k) & 1u)
-        *(reinterpret_cast<uint4*>(p.out + (size_t)lr.row[k] * kHeadDim + cb * 64) + pc) =
-            *swz(stage, 4 * k + (lane >> 3), pc);
+      for (int k = 0; k < 8; ++k)
+        g[k] = (lr.valid >> k) & 1u ? __ldg(reinterpret_cast<const uint4*>(p.gate + (size_t)lr.row[k] * kHeadDim + cb * 64) + pc)
+                                    : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if ((lr.valid >> k) & 1u)
+          *(reinterpret_cast<uint4*>(p.out + (size_t)lr.row[k] * kHeadDim + cb * 64) + pc) =
+              gate8(*swz(stage, 4 * k + (lane >> 3), pc), g[k]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if ((lr.valid >> k) & 1u)
+          *(reinterpret_cast<uint4*>(p.out + (size_t)lr.row[k] * kHeadDim + cb * 64) + pc) =
+              *swz(stage, 4 * k + (lane >> 3), pc);
+    }
   }
   return true;
 }
@@ -641,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(c.bar(B_PFULL + b), 8);
       mbar_init(c.bar(B_STATS + b), 8);
     }
-    mbar_init(c.bar(B_QFULL), 1);
+    mbar_init(c.bar(B_QFULL), 4);  // one arrival per Q region
     mbar_init(c.bar(B_QREADY), 4);
     mbar_init(c.bar(B_QEMPTY), 1);
     mbar_init(c.bar(B_OFULL), 1);
@@ -667,15 +718,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   c.tb = *tmem_slot;
 
-  const bool lane0 = (threadIdx.x & 31) == 0;
+  const int lane = threadIdx.x & 31;
   if (warp == 0) {
-    if (lane0) role_producer_k(p, m, c);
+    if (lane < 4) role_producer_k(p, m, c, lane);
   } else if (warp == 1) {
-    if (lane0) role_mma(p, c);
+    if (lane == 0) role_mma(p, c);
   } else if (warp == 2) {
-    if (lane0) role_producer_v(p, m, c);
+    if (lane < 2) role_producer_v(p, m, c, lane);
   } else if (warp == 3) {
-    if (lane0) role_producer_q(p, m, c);
+    if (lane < 4) role_producer_q(p, m, c, lane);
   } else if (warp < 12) {
     role_softmax(p, c, sm);
   } else {

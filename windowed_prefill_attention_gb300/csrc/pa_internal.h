@@ -52,6 +52,7 @@ struct AttnParams {
   const float* vs;
   const unsigned int* vsmax;
   __nv_bfloat16* out;         // [total_q][HQ][256]
+  const __nv_bfloat16* gate;  // [total_q][HQ][256] output gate (sigmoid), or nullptr
   int HQ, HKV, G, TQ;
   int n_tok_cap;
   int S, W;

@@ -209,6 +209,7 @@ extern "C" int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_page
   a.vs = vs;
   a.vsmax = vsmax;
   a.out = static_cast<__nv_bfloat16*>(out);
+  a.gate = nullptr;
   a.HQ = n_q_heads;
   a.HKV = n_kv_heads;
   a.G = G;
