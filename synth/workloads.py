@@ -93,6 +93,9 @@ CONFIGS = {
     "chunked_ragged": Workload("chunked_ragged", 16, 2,
                                ((1024, 2048), (6144, 2048), (30720, 2048), (12005, 2048)),
                                1, 256, seed=5, outlier_frac=0.01),
+    # Beyond the pages' benchmark (they fall back to a token path above 64k):
+    # 131072 tokens, same distributions as 32k.
+    "128k": Workload("128k", 16, 2, ((0, 131072),), 1, 256, seed=6, outlier_frac=0.01),
 }
 
 

@@ -214,3 +214,16 @@ def test_output_gate_special_values_bitwise():
     assert rc0 == rc1 == rc2 == 0
     assert np.array_equal(half, plain * 0.5)
     assert np.array_equal(one, plain)
+
+
+@pytest.mark.parametrize("n_win_blk", [256, 0], ids=["window", "window_off"])
+def test_contexts_beyond_64k_match_oracle(inputs, n_win_blk):
+    """131072-token context (beyond the pages' fallback point), sampled rows:
+    with the 256-block window, and with the window off (full causal, every
+    row up to 131072 keys; fewer sampled tokens, the oracle walks them all)."""
+    inp = inputs("128k")
+    out, rc = run_gpu(inp, W=n_win_blk)
+    assert rc == 0
+    rows = sample_rows(inp, 160 if n_win_blk else 24, seed=13, edge=4)
+    mx, mean = compare(out, inp, rows, n_win_blk=n_win_blk)
+    assert mx <= TOL_MAX and mean <= TOL_MEAN, (n_win_blk, mx, mean)
