@@ -335,6 +335,64 @@ def run_ours(args, wl):
         dist.destroy_process_group()
 
 
+def run_kv_append(args, wl):
+    """KV append (the step before the path): every query token's K and V rows of
+    the workload quantised into the pool.  HBM-bound; algorithmic bytes per
+    (token, kv head) = bf16 K and V read (2 x 512) + int8 codes written
+    (2 x 256) + fp32 scales written (2 x 4) = 1544."""
+    import torch
+
+    import windowed_prefill_attention_gb300 as pa
+    torch.cuda.set_device(0)
+    inp = make_inputs(wl)
+    dev = torch.device("cuda", 0)
+    hkv = wl.n_kv_heads
+    q_off, q_start, n_q, n_ctx = inp.seq_desc[0].tolist()
+    rng = np.random.default_rng(77)
+    kn = torch.from_numpy(rng.normal(size=(n_q, hkv, HEAD_DIM)).astype(np.float32)).to(dev).to(torch.bfloat16)
+    vn = torch.from_numpy(rng.normal(size=(n_q, hkv, HEAD_DIM)).astype(np.float32)).to(dev).to(torch.bfloat16)
+    kp, vp = torch.from_numpy(inp.k_pool).to(dev), torch.from_numpy(inp.v_pool).to(dev)
+    ks, vs = torch.from_numpy(inp.k_scale).to(dev), torch.from_numpy(inp.v_scale).to(dev)
+    bt = torch.from_numpy(np.ascontiguousarray(inp.block_table[0])).to(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    h = pa.pa_create(wl.n_q_heads, hkv, inp.k_pool.shape[0], inp.block_table.shape[1])
+    step = lambda: pa.pa_kv_append(h, kn, vn, q_start, bt, kp, vp, ks, vs)  # noqa: E731
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(0)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.2)
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record()
+        step()
+        ends[i].record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    rc = pa.pa_last_error(h)
+    pa.pa_destroy(h)
+    if rc != 0:
+        raise RuntimeError("device error: %s" % pa.pa_strerror(rc))
+    ms = float(sum(a.elapsed_time(b) for a, b in zip(starts, ends))) / args.steps
+    nbytes = n_q * hkv * 1544
+    gbs = nbytes / (ms / 1e3) / 1e9
+    peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["hbm_gbs"])
+    print(json.dumps({
+        "metric": "kv append GB/s (algorithmic bytes)", "value": gbs, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16->int8", "data": "synthetic",
+        "config": {"workload": wl.name, "op": "kv_append", "tokens": n_q, "n_kv_heads": hkv,
+                   "l2": "flushed between timed steps (256 MiB write, untimed)"},
+        "gpu_launches": args.steps, "clocks": clocks,
+        "roofline": {"bound": "hbm", "kernel": "kv_append_kernel", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                     "frac": gbs / peak, "peak_source": "measured copy bandwidth (MEASURED_PEAKS.json)",
+                     "traffic": None, "bytes_per_launch": nbytes}}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -344,10 +402,14 @@ def main():
     ap.add_argument("--config", default="32k", choices=sorted(CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gate", action="store_true", help="fuse the output gate out * sigmoid(q_gate) (extra row)")
+    ap.add_argument("--op", choices=["prefill", "kv_append"], default="prefill",
+                    help="kv_append: time the KV-append step alone (extra row)")
     args = ap.parse_args()
     wl = CONFIGS[args.config]
     if args.impl == "reference":
         run_reference(args, wl)
+    elif args.op == "kv_append":
+        run_kv_append(args, wl)
     else:
         run_ours(args, wl)
 

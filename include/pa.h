@@ -140,6 +140,28 @@ int pa_timing(pa_handle h, int reset, double* widen_ms, double* attention_ms, in
 
 const char* pa_strerror(int code);
 
+/* KV append, the step before the path ("fp16 shared-memory tiles for windowed
+ * prefill attention", "Summary": K and V live in an int8 paged pool with
+ * per-token, per-kv-head fp32 scales): the K and V rows of n_new new tokens,
+ * positions [tok_start, tok_start + n_new) of one sequence, are quantised and
+ * written into the pool.  Each (token, kv head) row of 256 values gets its own
+ * symmetric scale absmax/127 and codes rint(x/scale), half to even, clamped to
+ * [-127, 127]; all decisions in fp32 with correctly rounded divisions; an
+ * all-zero row gets scale 0 and codes 0.  Row (token t, head g) goes to page
+ * block_table_row[t / 16], slot t % 16, i.e. k_pool[page][t % 16][g][:] and
+ * k_scale[page][t % 16][g] (likewise V).
+ *   k_new, v_new     device bf16 [n_new][n_kv_heads][256], 16-byte aligned
+ *   block_table_row  device int32, the sequence's pages (>= ceil((tok_start +
+ *                    n_new) / 16) entries, at most max_pages_per_seq)
+ *   pools, scales    device, the layouts of pa_prefill; written in place
+ * Asynchronous on `stream`; no other slot is touched.  A page entry outside
+ * [0, n_pool_pages) is never dereferenced: its rows are skipped and
+ * pa_last_error reports PA_EBADPAGE.  PA_EINVAL for bad pointers, alignment or
+ * a range past max_pages_per_seq pages.  Inputs must be finite. */
+int pa_kv_append(pa_handle h, const void* k_new, const void* v_new, int n_new, int tok_start,
+                 const int32_t* block_table_row, int8_t* k_pool, int8_t* v_pool, float* k_scale, float* v_scale,
+                 void* stream);
+
 /* Host-only planning, no GPU needed: the work units of a call in launch order
  * (longest first).  units_out (may be NULL) receives up to cap entries of
  * int32[4] = {sequence, kv head, first token, key tiles}.  Outputs: unit

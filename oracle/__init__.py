@@ -120,6 +120,40 @@ def gate(out_rows: np.ndarray, gate_rows: np.ndarray) -> np.ndarray:
         return np.asarray(out_rows, dtype=np.float64) * (1.0 / (1.0 + np.exp(-g)))
 
 
+def kv_quantize(x_bits: np.ndarray):
+    """The pool's quantisation of K/V rows ("fp16 shared-memory tiles for
+    windowed prefill attention", "Summary": int8 pages, per-token per-kv-head
+    fp32 scales): for each row of 256 bf16 values (bit patterns, last axis),
+    scale = absmax / 127 and code = rint(x / scale), half to even, clamped to
+    [-127, 127], decided in fp32 (IEEE-rounded division); scale 0 and codes 0
+    for an all-zero row.  Returns (int8 codes, float32 scales)."""
+    x = (np.asarray(x_bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+    absmax = np.abs(x).max(axis=-1)
+    scale = np.divide(absmax, np.float32(127.0), dtype=np.float32)
+    codes = np.zeros(x.shape, dtype=np.int8)
+    nz = scale > 0
+    q = np.divide(x[nz], scale[nz][:, None], dtype=np.float32)
+    codes[nz] = np.clip(np.rint(q), -127, 127).astype(np.int8)
+    return codes, scale
+
+
+def kv_append(k_pool, v_pool, k_scale, v_scale, bt_row, tok_start, k_new_bits, v_new_bits):
+    """KV append on host copies of the pool: the new tokens' rows quantised
+    (kv_quantize) and placed at page bt_row[t // 16], slot t % 16, kv head g.
+    Returns the updated (k_pool, v_pool, k_scale, v_scale)."""
+    k_pool, v_pool, k_scale, v_scale = (np.array(a, copy=True) for a in (k_pool, v_pool, k_scale, v_scale))
+    kc, ks = kv_quantize(k_new_bits)
+    vc, vs = kv_quantize(v_new_bits)
+    for i in range(kc.shape[0]):
+        t = tok_start + i
+        page, slot = int(bt_row[t // 16]), t % 16
+        k_pool[page, slot] = kc[i]
+        v_pool[page, slot] = vc[i]
+        k_scale[page, slot] = ks[i]
+        v_scale[page, slot] = vs[i]
+    return k_pool, v_pool, k_scale, v_scale
+
+
 def method(prob: Problem, rows: np.ndarray, q_mode: int, p_mode: int, tile: int = 64,
            n_threads: int = 0) -> np.ndarray:
     """The pages' quantised steps for the given rows (see pa_oracle.c)."""

@@ -1,0 +1,105 @@
+"""GPU: KV append (the step before the path) through the C ABI.
+
+The new tokens' K/V rows are quantised per (token, kv head) and written into
+the paged pool through the block table.  Codes and scales are integer / fp32
+decisions taken in the same precision on both sides, so the pool the kernel
+writes must equal the oracle's bit for bit, every other slot unchanged.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+from pa_testutil import TOL_MAX, TOL_MEAN, norm_errors, run_gpu, sample_rows
+from synth import CONFIGS, make_inputs
+from synth.workloads import Inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _bf16_bits(x):
+    b = np.asarray(x, dtype=np.float32).view(np.uint32)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def _new_rows(n_new, hkv, seed, outliers=True):
+    rng = np.random.default_rng(seed)
+    x = rng.normal(size=(n_new, hkv, 256)).astype(np.float32)
+    if outliers:  # a few x8 tokens and an all-zero row
+        x[rng.choice(n_new, size=max(1, n_new // 100), replace=False)] *= 8
+        x[n_new // 2, 0] = 0.0
+    return _bf16_bits(x)
+
+
+def _append_gpu(inp, seq, tok_start, kn_bits, vn_bits, bt_row=None):
+    import torch
+
+    import windowed_prefill_attention_gb300 as pa
+    wl = inp.wl
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    kp, vp, ks, vs = dev(inp.k_pool), dev(inp.v_pool), dev(inp.k_scale), dev(inp.v_scale)
+    bt = dev(inp.block_table[seq] if bt_row is None else bt_row)
+    kn = dev(kn_bits.view(np.int16)).view(torch.bfloat16)
+    vn = dev(vn_bits.view(np.int16)).view(torch.bfloat16)
+    h = pa.pa_create(wl.n_q_heads, wl.n_kv_heads, inp.k_pool.shape[0], inp.block_table.shape[1])
+    try:
+        pa.pa_kv_append(h, kn, vn, tok_start, bt, kp, vp, ks, vs)
+        rc = pa.pa_last_error(h)
+    finally:
+        pa.pa_destroy(h)
+    return [t.cpu().numpy() for t in (kp, vp, ks, vs)], rc
+
+
+@pytest.mark.parametrize("seq,tok_start,n_new", [(3, 12005, 2048), (0, 1024, 2048), (1, 6144, 1), (2, 30720, 17)],
+                         ids=["ragged_start", "aligned", "one_token", "short"])
+def test_kv_append_is_bit_exact(seq, tok_start, n_new):
+    inp = make_inputs(CONFIGS["chunked_ragged"])
+    hkv = inp.wl.n_kv_heads
+    kn, vn = _new_rows(n_new, hkv, 100 + seq), _new_rows(n_new, hkv, 200 + seq)
+    (kp, vp, ks, vs), rc = _append_gpu(inp, seq, tok_start, kn, vn)
+    assert rc == 0
+    want = oracle.kv_append(inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale, inp.block_table[seq], tok_start, kn, vn)
+    for got, ref in zip((kp, vp, ks, vs), want):
+        assert np.array_equal(got.view(np.uint8) if got.dtype == np.int8 else got.view(np.uint32),
+                              ref.view(np.uint8) if ref.dtype == np.int8 else ref.view(np.uint32))
+
+
+def test_append_then_prefill_matches_oracle():
+    """A fresh chunk appended on the GPU, then prefilled over the pool it wrote:
+    against the fp64 definition on the oracle's own appended pool."""
+    inp = make_inputs(CONFIGS["chunked_ragged"])
+    seq, (q_off, q_start, n_q, n_ctx) = 3, inp.seq_desc[3].tolist()
+    hkv = inp.wl.n_kv_heads
+    kn, vn = _new_rows(n_q, hkv, 300), _new_rows(n_q, hkv, 301)
+    (kp, vp, ks, vs), rc = _append_gpu(inp, seq, q_start, kn, vn)
+    assert rc == 0
+    new = dataclasses.replace(inp, k_pool=kp, v_pool=vp, k_scale=ks, v_scale=vs)
+    out, rc = run_gpu(new)
+    assert rc == 0
+    kp2, vp2, ks2, vs2 = oracle.kv_append(inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale, inp.block_table[seq],
+                                          q_start, kn, vn)
+    ref_inp = Inputs(inp.wl, inp.q, kp2, vp2, ks2, vs2, inp.block_table, inp.seq_desc)
+    rows = sample_rows(ref_inp, 128, seed=17)
+    rows = rows[(rows[:, 0] >= q_off) & (rows[:, 0] < q_off + n_q)]
+    ref = oracle.exact(oracle.Problem.from_inputs(ref_inp), rows)
+    mx, mean = norm_errors(out[rows[:, 0], rows[:, 1]].astype(np.float64), ref)
+    assert mx <= TOL_MAX and mean <= TOL_MEAN, (mx, mean)
+
+
+def test_kv_append_bad_page_is_reported_and_skipped():
+    import windowed_prefill_attention_gb300 as pa
+    inp = make_inputs(CONFIGS["chunked_ragged"])
+    hkv = inp.wl.n_kv_heads
+    bt = inp.block_table[0].copy()
+    bt[(1024 + 20) // 16] = inp.k_pool.shape[0] + 5  # the page of tokens 1040..1055: outside the pool
+    kn, vn = _new_rows(64, hkv, 400), _new_rows(64, hkv, 401)
+    (kp, vp, ks, vs), rc = _append_gpu(inp, 0, 1024, kn, vn, bt_row=bt)
+    assert rc == pa.PA_EBADPAGE
+    want = oracle.kv_append(inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale, inp.block_table[0], 1024, kn, vn)
+    bits = lambda a: a.view(np.uint8) if a.dtype == np.int8 else a.view(np.uint32)  # noqa: E731 (NaN-safe)
+    for got, ref, orig in zip((kp, vp, ks, vs), want, (inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale)):
+        good = np.ones(got.shape[:2], dtype=bool)
+        good[inp.block_table[0][(1024 + 20) // 16]] = False  # the slots the bad entry stood for keep old values
+        assert np.array_equal(bits(got)[good], bits(ref)[good])
+        assert np.array_equal(bits(got)[~good], bits(orig)[~good])

@@ -281,3 +281,65 @@ def test_gate_against_library_sigmoid_and_special_values():
     np.testing.assert_allclose(oracle.gate(out, np.full_like(g, 40.0)), out, rtol=1e-15)
     assert np.all(np.abs(oracle.gate(out, np.full_like(g, -800.0))) == 0.0)
     np.testing.assert_allclose(oracle.gate(out, g) + oracle.gate(out, -g), out, rtol=1e-13, atol=1e-15)
+
+
+def _bf16_bits(x):
+    x = np.asarray(x, dtype=np.float32)
+    b = x.view(np.uint32)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)  # round to nearest even
+
+
+def test_kv_quantize_golden_row():
+    """A hand-derived row (scale 2 exactly, values on and between the code
+    grid, half-way cases rounded to even) gives the codes written out by hand."""
+    with open(os.path.join(GOLDEN, "kv_codes.json")) as f:
+        gold = json.load(f)
+    codes, scale = oracle.kv_quantize(_bf16_bits(gold["values"])[None, :])
+    assert scale[0] == np.float32(gold["scale"])
+    assert codes[0, :16].tolist() == gold["codes_first16"]
+    assert not codes[0, 16:].any()
+
+
+def test_kv_quantize_properties():
+    """On random rows: the largest magnitude maps to +-127, every value is
+    reconstructed within half a step (up to the fp32 rounding of x / scale, in
+    which a value a hair above a half-way point can round to the tie), an
+    all-zero row gets scale 0 and codes 0."""
+    rng = np.random.default_rng(9)
+    x = rng.normal(size=(500, 256)).astype(np.float32) * rng.uniform(0.01, 50, size=(500, 1)).astype(np.float32)
+    x[7] = 0.0
+    bits = _bf16_bits(x)
+    xf = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    codes, scale = oracle.kv_quantize(bits)
+    assert scale[7] == 0 and not codes[7].any()
+    live = np.arange(500) != 7
+    s = scale[live].astype(np.float64)[:, None]
+    # half a step, plus the fp32 rounding of the quotient x / scale (<= 127 * 2^-24 steps)
+    assert np.all(np.abs(xf[live] - codes[live] * s) <= (0.5 + 1e-5) * s)
+    top = np.abs(xf[live]).argmax(axis=1)
+    assert np.all(np.abs(codes[live][np.arange(live.sum()), top]) == 127)
+
+
+def test_kv_append_places_rows_through_the_block_table():
+    """Rows land at page bt[t // 16], slot t % 16; every other slot is untouched."""
+    rng = np.random.default_rng(10)
+    n_pool, hkv = 9, 2
+    kp = rng.integers(-127, 128, size=(n_pool, 16, hkv, 256), dtype=np.int8)
+    vp = rng.integers(-127, 128, size=(n_pool, 16, hkv, 256), dtype=np.int8)
+    ks = rng.uniform(0.1, 1, size=(n_pool, 16, hkv)).astype(np.float32)
+    vs = rng.uniform(0.1, 1, size=(n_pool, 16, hkv)).astype(np.float32)
+    bt = np.array([4, 0, 7, 2], dtype=np.int32)
+    tok_start, n_new = 13, 30  # tokens 13..42: pages bt[0..2], slots 13.. and 0..10
+    kn = _bf16_bits(rng.normal(size=(n_new, hkv, 256)))
+    vn = _bf16_bits(rng.normal(size=(n_new, hkv, 256)))
+    k2, v2, ks2, vs2 = oracle.kv_append(kp, vp, ks, vs, bt, tok_start, kn, vn)
+    kc, kq = oracle.kv_quantize(kn)
+    vc, vq = oracle.kv_quantize(vn)
+    touched = np.zeros((n_pool, 16), dtype=bool)
+    for i in range(n_new):
+        t = tok_start + i
+        page, slot = bt[t // 16], t % 16
+        touched[page, slot] = True
+        assert np.array_equal(k2[page, slot], kc[i]) and np.array_equal(v2[page, slot], vc[i])
+        assert np.array_equal(ks2[page, slot], kq[i]) and np.array_equal(vs2[page, slot], vq[i])
+    assert np.array_equal(k2[~touched], kp[~touched]) and np.array_equal(vs2[~touched], vs[~touched])

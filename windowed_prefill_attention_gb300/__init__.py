@@ -28,7 +28,7 @@ PA_Q_BF16, PA_Q_INT8 = 0, 1
 PA_P_F16, PA_P_U8 = 0, 1
 
 EXPORTED = ("pa_default_options", "pa_create", "pa_destroy", "pa_prefill", "pa_prefill_batch",
-            "pa_prefill_batch_gated", "pa_prefill_host",
+            "pa_prefill_batch_gated", "pa_prefill_host", "pa_kv_append",
             "pa_last_error", "pa_timing", "pa_strerror", "pa_plan", "pa_debug_gather", "pa_debug_maskset",
             "pa_prefill_noalloc")
 
@@ -52,6 +52,7 @@ _lib.pa_prefill.argtypes = [_vp] + [_vp] * 6 + [_i] * 5 + [_f, _vp, _vp]
 _lib.pa_prefill_batch.argtypes = [_vp, _i, C.POINTER(pa_seq)] + [_vp] * 6 + [_i, _i, _f, _vp, _vp]
 _lib.pa_prefill_host.argtypes = _lib.pa_prefill_batch.argtypes
 _lib.pa_prefill_batch_gated.argtypes = [_vp, _i, C.POINTER(pa_seq)] + [_vp] * 7 + [_i, _i, _f, _vp, _vp]
+_lib.pa_kv_append.argtypes = [_vp, _vp, _vp, _i, _i] + [_vp] * 6
 _lib.pa_last_error.argtypes = [_vp, _vp]
 _lib.pa_timing.argtypes = [_vp, _i, C.POINTER(C.c_double), C.POINTER(C.c_double), C.POINTER(_i)]
 _lib.pa_strerror.argtypes = [_i]
@@ -166,6 +167,18 @@ def pa_prefill_batch(h, seqs, q, k_pool, v_pool, k_scale, v_scale, block_table, 
         _check(_lib.pa_prefill_batch_gated(h, len(s), s, args[0], _dev(q_gate, torch.bfloat16, "q_gate"), *args[1:],
                                            n_sink_blk, n_win_blk, float(sm_scale), _dev(out, torch.bfloat16, "out"),
                                            _stream(stream)), "pa_prefill_batch_gated")
+
+
+def pa_kv_append(h, k_new, v_new, tok_start, block_table_row, k_pool, v_pool, k_scale, v_scale,
+                 stream=None) -> None:
+    """Quantise the new tokens' K/V rows (bf16 [n_new, HKV, 256]) into the pool."""
+    import torch
+    n_new = int(k_new.shape[0])
+    _check(_lib.pa_kv_append(h, _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"), n_new,
+                             int(tok_start), _dev(block_table_row, torch.int32, "block_table_row"),
+                             _dev(k_pool, torch.int8, "k_pool"), _dev(v_pool, torch.int8, "v_pool"),
+                             _dev(k_scale, torch.float32, "k_scale"), _dev(v_scale, torch.float32, "v_scale"),
+                             _stream(stream)), "pa_kv_append")
 
 
 def pa_prefill_host(h, seqs, q, k_pool, v_pool, k_scale, v_scale, block_table, n_sink_blk, n_win_blk, sm_scale,

@@ -593,6 +593,33 @@ int pa_debug_gather(pa_handle h, int n_seq, const pa_seq* seqs, const int8_t* k_
   return pa_last_error(h, stream);
 }
 
+int pa_kv_append(pa_handle h, const void* k_new, const void* v_new, int n_new, int tok_start,
+                 const int32_t* block_table_row, int8_t* k_pool, int8_t* v_pool, float* k_scale, float* v_scale,
+                 void* stream) {
+  if (!h || n_new < 0 || tok_start < 0) return PA_EINVAL;
+  if (n_new == 0) return PA_OK;
+  if (!k_new || !v_new || !block_table_row || !k_pool || !v_pool || !k_scale || !v_scale) return PA_EINVAL;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+      !aligned(k_scale, 4) || !aligned(v_scale, 4) || !aligned(block_table_row, 4))
+    return PA_EINVAL;
+  if ((long long)tok_start + n_new > (long long)h->max_pages * kPage) return PA_EINVAL;
+  KvAppendParams p{};
+  p.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  p.n_new = n_new;
+  p.tok_start = tok_start;
+  p.HKV = h->HKV;
+  p.n_pool = h->n_pool;
+  p.bt_row = block_table_row;
+  p.k_pool = k_pool;
+  p.v_pool = v_pool;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.err = h->d_err;
+  PA_CUDA(launch_kv_append(p, static_cast<cudaStream_t>(stream)));
+  return PA_OK;
+}
+
 int pa_debug_maskset(pa_handle h, int n_seq, const pa_seq* seqs, int n_sink_blk, int n_win_blk,
                      int32_t* row_counts, int32_t* unit_blocks, int cap, int32_t* units_out, int units_cap,
                      int* n_units, void* stream) {

@@ -72,6 +72,20 @@ struct AttnMaps {
 
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_widen(const WidenParams& p, cudaStream_t st);
+
+// KV append: the new tokens' K/V rows quantised into the pool.
+struct KvAppendParams {
+  const __nv_bfloat16* k_new;  // [n_new][HKV][256]
+  const __nv_bfloat16* v_new;  // [n_new][HKV][256]
+  int n_new, tok_start, HKV, n_pool;
+  const int32_t* bt_row;       // pool page of each 16-token block of the sequence
+  int8_t* k_pool;
+  int8_t* v_pool;
+  float* k_scale;
+  float* v_scale;
+  int* err;
+};
+cudaError_t launch_kv_append(const KvAppendParams& p, cudaStream_t st);
 cudaError_t launch_attention(const AttnParams& p, const AttnMaps& m, int n_sm, cudaStream_t st);
 
 // Debug exports (tests only).

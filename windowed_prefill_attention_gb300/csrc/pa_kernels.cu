@@ -99,6 +99,98 @@ cudaError_t launch_widen(const WidenParams& p, cudaStream_t st) {
 }
 
 // ======================================================================
+// KV append: the step before the path.  Each new (token, kv head) row of K
+// and of V is quantised symmetrically on its own (scale = absmax / 127, code
+// = rint(x / scale) half to even, clamped to [-127, 127], all in fp32 with
+// correctly rounded divisions; an all-zero row gets scale 0) and written into
+// its pool slot: page bt_row[tok / 16], slot tok % 16.
+// One warp per new token: its 2 x HKV rows (K and V of every kv head), 8
+// values per lane per row, all rows' loads in flight before any reduction.
+constexpr int kAppendWarps = 8;
+
+__device__ __forceinline__ uint2 quantise_row8(const uint4 raw, float& scale_out) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  float x[8];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    x[2 * e] = __uint_as_float(w[e] << 16);
+    x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+  }
+  float am = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(x[e]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+  const float scale = __fdiv_rn(am, 127.f);
+  // code = rint(x / scale) on the IEEE-rounded quotient.  x * (1/scale) is
+  // within 2.3e-5 of that quotient (|quotient| <= 127.5; two roundings of
+  // 2^-24 relative each), so away from the half-integers (farther than 1e-4)
+  // both round the same way; near them the division itself decides.
+  const float rcp = scale > 0.f ? __frcp_rn(scale) : 0.f;
+  uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    float qv = x[e] * rcp;
+    if (fabsf(qv - floorf(qv) - 0.5f) < 1e-4f && scale > 0.f) qv = __fdiv_rn(x[e], scale);
+    const int code = scale > 0.f ? (int)fminf(127.f, fmaxf(-127.f, rintf(qv))) : 0;
+    packed[e >> 2] |= ((uint32_t)code & 0xffu) << (8 * (e & 3));
+  }
+  scale_out = scale;
+  return make_uint2(packed[0], packed[1]);
+}
+
+template <int HKV>
+__global__ void __launch_bounds__(kAppendWarps * 32) kv_append_kernel(const KvAppendParams p) {
+  const int i = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);  // new token
+  const int lane = threadIdx.x & 31;
+  if (i >= p.n_new) return;
+  const int tok = p.tok_start + i;
+  // the rows' loads go out with the block-table read, not after it
+  const int phys = p.bt_row[tok / kPage];
+  const size_t row0 = (size_t)i * HKV;
+  uint4 rk[HKV], rv[HKV];
+#pragma unroll
+  for (int g = 0; g < HKV; ++g) {
+    rk[g] = reinterpret_cast<const uint4*>(p.k_new + (row0 + g) * kHeadDim)[lane];
+    rv[g] = reinterpret_cast<const uint4*>(p.v_new + (row0 + g) * kHeadDim)[lane];
+  }
+  if (phys < 0 || phys >= p.n_pool) {  // never dereferenced
+    if (lane == 0) atomicCAS(p.err, 0, DEV_ERR_BAD_PAGE);
+    return;
+  }
+  const size_t slot0 = ((size_t)phys * kPage + tok % kPage) * HKV;
+#pragma unroll
+  for (int g = 0; g < HKV; ++g) {
+      float sk, sv;
+      const uint2 ck = quantise_row8(rk[g], sk);
+      const uint2 cv = quantise_row8(rv[g], sv);
+      reinterpret_cast<uint2*>(p.k_pool + (slot0 + g) * kHeadDim)[lane] = ck;
+      reinterpret_cast<uint2*>(p.v_pool + (slot0 + g) * kHeadDim)[lane] = cv;
+      if (lane == 0) {
+        p.k_scale[slot0 + g] = sk;
+        p.v_scale[slot0 + g] = sv;
+      }
+    }
+}
+
+cudaError_t launch_kv_append(const KvAppendParams& p, cudaStream_t st) {
+  if (p.n_new <= 0) return cudaSuccess;
+  const int grid = (p.n_new + kAppendWarps - 1) / kAppendWarps;
+  switch (p.HKV) {
+    case 1: kv_append_kernel<1><<<grid, kAppendWarps * 32, 0, st>>>(p); break;
+    case 2: kv_append_kernel<2><<<grid, kAppendWarps * 32, 0, st>>>(p); break;
+    case 3: kv_append_kernel<3><<<grid, kAppendWarps * 32, 0, st>>>(p); break;
+    case 4: kv_append_kernel<4><<<grid, kAppendWarps * 32, 0, st>>>(p); break;
+    case 5: kv_append_kernel<5><<<grid, kAppendWarps * 32, 0, st>>>(p); break;
+    case 6: kv_append_kernel<6><<<grid, kAppendWarps * 32, 0, st>>>(p); break;
+    case 7: kv_append_kernel<7><<<grid, kAppendWarps * 32, 0, st>>>(p); break;
+    case 8: kv_append_kernel<8><<<grid, kAppendWarps * 32, 0, st>>>(p); break;
+    default: return cudaErrorInvalidValue;  // the handle accepts 1..8 kv heads
+  }
+  return cudaGetLastError();
+}
+
+// ======================================================================
 // Debug exports (tests only): the same geometry helpers as the kernels.
 // ======================================================================
 __global__ void debug_gather_kernel(const WidenParams p, int seq, int8_t* k_out, int8_t* v_out, float* ks_out,
