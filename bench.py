@@ -34,6 +34,8 @@ UNIT = "TOPS"
 HEAD_DIM = 256
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
+PAGE = 16
+N_DECODE_SEQS = 64  # decode batch of the --op decode row
 
 
 def visible_pairs(q_start, n_q, S, W, page=16):
@@ -393,6 +395,84 @@ def run_kv_append(args, wl):
                      "traffic": None, "bytes_per_launch": nbytes}}), flush=True)
 
 
+def run_decode(args, wl):
+    """Split-KV decode: one new token for each of N_DECODE_SEQS sequences whose
+    context is the workload's (the 32k workload: 64 x 32768 tokens, GQA 16:2,
+    1 sink block + 256-block window).  HBM-bound; algorithmic bytes per step =
+    every visible key's K and V codes (2 x 256 per kv head) and scales (2 x 4)
+    + the query and output rows.  The pool is drawn on the device (uniform
+    codes, scales in [1e-3, 2e-2], a random page permutation): only bandwidth
+    is measured here; the decode tests check the values."""
+    import torch
+
+    import windowed_prefill_attention_gb300 as pa
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev).manual_seed(99)
+    n_seq, ctx = N_DECODE_SEQS, wl.seqs[0][0] + wl.seqs[0][1]
+    hq, hkv = wl.n_q_heads, wl.n_kv_heads
+    pages = (ctx + PAGE - 1) // PAGE
+    n_pool = n_seq * pages
+    kp = torch.randint(-127, 128, (n_pool, PAGE, hkv, HEAD_DIM), dtype=torch.int8, device=dev, generator=gen)
+    vp = torch.randint(-127, 128, (n_pool, PAGE, hkv, HEAD_DIM), dtype=torch.int8, device=dev, generator=gen)
+    ks = torch.rand((n_pool, PAGE, hkv), device=dev, generator=gen) * 0.019 + 0.001
+    vs = torch.rand((n_pool, PAGE, hkv), device=dev, generator=gen) * 0.019 + 0.001
+    bt = torch.randperm(n_pool, device=dev, generator=gen).to(torch.int32).view(n_seq, pages).contiguous()
+    q = torch.randn((n_seq, hq, HEAD_DIM), device=dev, generator=gen).to(torch.bfloat16)
+    out = torch.empty_like(q)
+    seqs = np.array([(s, ctx - 1, 1, ctx) for s in range(n_seq)], dtype=np.int32)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    h = pa.pa_create(hq, hkv, n_pool, pages)
+    S, W = wl.n_sink_blk, wl.n_win_blk
+    step = lambda: pa.pa_decode(h, seqs, q, kp, vp, ks, vs, bt, S, W, wl.sm_scale, out)  # noqa: E731
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(0)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.2)
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record()
+        step()
+        ends[i].record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    rc = pa.pa_last_error(h)
+    pa.pa_destroy(h)
+    if rc != 0:
+        raise RuntimeError("device error: %s" % pa.pa_strerror(rc))
+    ms = float(sum(a.elapsed_time(b) for a, b in zip(starts, ends))) / args.steps
+    keys = _row_count_decode(ctx, S, W)
+    nbytes = n_seq * hkv * keys * (2 * HEAD_DIM + 8) + 2 * n_seq * hq * HEAD_DIM * 2
+    gbs = nbytes / (ms / 1e3) / 1e9
+    peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["hbm_gbs"])
+    print(json.dumps({
+        "metric": "decode GB/s (visible K/V read)", "value": gbs, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8 codes, fp16/fp32 arithmetic", "data": "synthetic",
+        "config": {"workload": wl.name, "op": "decode", "n_seq": n_seq, "context": ctx, "n_q_heads": hq,
+                   "n_kv_heads": hkv, "n_sink_blk": S, "n_win_blk": W, "visible_keys_per_seq": keys,
+                   "l2": "flushed between timed steps (256 MiB write, untimed)"},
+        "tokens_per_s": n_seq / (ms / 1e3), "gpu_launches": 2 * args.steps, "clocks": clocks,
+        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel + decode_combine_kernel", "achieved": gbs,
+                     "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "peak_source": "measured copy bandwidth (MEASURED_PEAKS.json)", "traffic": None,
+                     "bytes_per_step": nbytes}}), flush=True)
+
+
+def _row_count_decode(ctx, S, W):
+    """Visible keys of a context's last token: the mask's closed form."""
+    t = ctx - 1
+    if W <= 0:
+        return t + 1
+    lo = max(0, t // PAGE + 1 - W)
+    return min(S, lo) * PAGE + (t + 1 - lo * PAGE)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -402,14 +482,16 @@ def main():
     ap.add_argument("--config", default="32k", choices=sorted(CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gate", action="store_true", help="fuse the output gate out * sigmoid(q_gate) (extra row)")
-    ap.add_argument("--op", choices=["prefill", "kv_append"], default="prefill",
-                    help="kv_append: time the KV-append step alone (extra row)")
+    ap.add_argument("--op", choices=["prefill", "kv_append", "decode"], default="prefill",
+                    help="kv_append / decode: time that step alone (extra rows)")
     args = ap.parse_args()
     wl = CONFIGS[args.config]
     if args.impl == "reference":
         run_reference(args, wl)
     elif args.op == "kv_append":
         run_kv_append(args, wl)
+    elif args.op == "decode":
+        run_decode(args, wl)
     else:
         run_ours(args, wl)
 

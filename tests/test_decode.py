@@ -1,0 +1,87 @@
+"""GPU: split-KV decode (one new token per sequence) through the C ABI,
+against the fp64 definition.
+
+A decode call is an attention call whose every sequence has one query row,
+the context's last token, so the workloads and the oracle are the prefill's:
+sequences (q_start, n_q) = (n_ctx - 1, 1).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from pa_testutil import TOL_MAX, TOL_MEAN, norm_errors, to_device
+from synth import make_inputs
+from synth.workloads import Workload
+
+pytestmark = pytest.mark.gpu
+
+
+def _decode_wl(name, hq, hkv, ctxs, S, W, seed, outliers=0.01):
+    return Workload(name, hq, hkv, tuple((c - 1, 1) for c in ctxs), S, W, seed=seed, outlier_frac=outliers)
+
+
+def run_decode(inp, S=None, W=None, bt=None):
+    import torch
+
+    import windowed_prefill_attention_gb300 as pa
+    wl = inp.wl
+    d = to_device(inp)
+    if bt is not None:
+        d["block_table"] = torch.from_numpy(bt).cuda()
+    out = torch.full_like(d["q"], float("nan"))
+    h = pa.pa_create(wl.n_q_heads, wl.n_kv_heads, inp.k_pool.shape[0], inp.block_table.shape[1])
+    try:
+        pa.pa_decode(h, inp.seq_desc, d["q"], d["k_pool"], d["v_pool"], d["k_scale"], d["v_scale"], d["block_table"],
+                     wl.n_sink_blk if S is None else S, wl.n_win_blk if W is None else W, wl.sm_scale, out)
+        rc = pa.pa_last_error(h)
+    finally:
+        pa.pa_destroy(h)
+    return out.float().cpu().numpy(), rc
+
+
+CASES = {
+    # contexts around split (256 keys) and window (4096 keys) edges, one-block and one-token contexts
+    "mixed": _decode_wl("dec_mixed", 16, 2, (4096, 32000, 17, 1, 12005, 256, 257, 4112, 65536), 1, 256, 41),
+    "window_off": _decode_wl("dec_nowin", 16, 2, (300, 5000, 16, 4097), 1, 0, 42),
+    "no_sink": _decode_wl("dec_nosink", 16, 2, (9000, 4096, 100), 0, 64, 43),
+    "sink_in_window": _decode_wl("dec_sinkwin", 16, 2, (200, 1000), 4, 10, 44),
+    "gqa1": _decode_wl("dec_g1", 4, 4, (3000, 700), 1, 128, 45),
+    "gqa2": _decode_wl("dec_g2", 8, 4, (2049, 33), 2, 32, 46),
+    "gqa4": _decode_wl("dec_g4", 8, 2, (6000,), 1, 256, 47),
+    "many": _decode_wl("dec_many", 16, 2, tuple(int(x) for x in np.random.default_rng(48).integers(1, 20000, 40)),
+                       1, 256, 48),
+}
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_decode_matches_oracle(case):
+    inp = make_inputs(CASES[case])
+    out, rc = run_decode(inp)
+    assert rc == 0
+    rows = oracle.all_rows(inp)
+    ref = oracle.exact(oracle.Problem.from_inputs(inp), rows)
+    got = out[rows[:, 0], rows[:, 1]].astype(np.float64)
+    assert np.isfinite(got).all()
+    mx, mean = norm_errors(got, ref)
+    assert mx <= TOL_MAX and mean <= TOL_MEAN, (case, mx, mean)
+
+
+def test_decode_rejects_prefill_shaped_sequences_and_wide_groups():
+    import windowed_prefill_attention_gb300 as pa
+    inp = make_inputs(CASES["window_off"])
+    bad = inp.seq_desc.copy()
+    bad[0, 1] -= 1  # not the context's last token
+    with pytest.raises(pa.PAError):
+        run_decode(type(inp)(inp.wl, inp.q, inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale, inp.block_table, bad))
+    wide = make_inputs(_decode_wl("dec_g16", 32, 2, (100,), 1, 8, 49))
+    with pytest.raises(pa.PAError):
+        run_decode(wide)
+
+
+def test_decode_bad_page_is_reported():
+    import windowed_prefill_attention_gb300 as pa
+    inp = make_inputs(CASES["no_sink"])
+    bt = inp.block_table.copy()
+    bt[0, (inp.seq_desc[0, 3] - 1) // 16] = inp.k_pool.shape[0] + 9  # the query's own block: always visible
+    _, rc = run_decode(inp, bt=bt)
+    assert rc == pa.PA_EBADPAGE

@@ -28,7 +28,7 @@ PA_Q_BF16, PA_Q_INT8 = 0, 1
 PA_P_F16, PA_P_U8 = 0, 1
 
 EXPORTED = ("pa_default_options", "pa_create", "pa_destroy", "pa_prefill", "pa_prefill_batch",
-            "pa_prefill_batch_gated", "pa_prefill_host", "pa_kv_append",
+            "pa_prefill_batch_gated", "pa_prefill_host", "pa_kv_append", "pa_decode",
             "pa_last_error", "pa_timing", "pa_strerror", "pa_plan", "pa_debug_gather", "pa_debug_maskset",
             "pa_prefill_noalloc")
 
@@ -53,6 +53,7 @@ _lib.pa_prefill_batch.argtypes = [_vp, _i, C.POINTER(pa_seq)] + [_vp] * 6 + [_i,
 _lib.pa_prefill_host.argtypes = _lib.pa_prefill_batch.argtypes
 _lib.pa_prefill_batch_gated.argtypes = [_vp, _i, C.POINTER(pa_seq)] + [_vp] * 7 + [_i, _i, _f, _vp, _vp]
 _lib.pa_kv_append.argtypes = [_vp, _vp, _vp, _i, _i] + [_vp] * 6
+_lib.pa_decode.argtypes = _lib.pa_prefill_batch.argtypes
 _lib.pa_last_error.argtypes = [_vp, _vp]
 _lib.pa_timing.argtypes = [_vp, _i, C.POINTER(C.c_double), C.POINTER(C.c_double), C.POINTER(_i)]
 _lib.pa_strerror.argtypes = [_i]
@@ -167,6 +168,16 @@ def pa_prefill_batch(h, seqs, q, k_pool, v_pool, k_scale, v_scale, block_table, 
         _check(_lib.pa_prefill_batch_gated(h, len(s), s, args[0], _dev(q_gate, torch.bfloat16, "q_gate"), *args[1:],
                                            n_sink_blk, n_win_blk, float(sm_scale), _dev(out, torch.bfloat16, "out"),
                                            _stream(stream)), "pa_prefill_batch_gated")
+
+
+def pa_decode(h, seqs, q, k_pool, v_pool, k_scale, v_scale, block_table, n_sink_blk, n_win_blk, sm_scale, out,
+              stream=None) -> None:
+    """One new token per sequence (seqs rows (q_off, n_ctx - 1, 1, n_ctx))."""
+    import torch
+    s = _seqs(seqs)
+    args = _dev_inputs(q, k_pool, v_pool, k_scale, v_scale, block_table)
+    _check(_lib.pa_decode(h, len(s), s, *args, n_sink_blk, n_win_blk, float(sm_scale),
+                          _dev(out, torch.bfloat16, "out"), _stream(stream)), "pa_decode")
 
 
 def pa_kv_append(h, k_new, v_new, tok_start, block_table_row, k_pool, v_pool, k_scale, v_scale,

@@ -5,7 +5,7 @@ import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
-SOURCES = [os.path.join(CSRC, f) for f in ("pa_api.cu", "pa_kernels.cu", "pa_attention.cu", "pa_noalloc.cu")]
+SOURCES = [os.path.join(CSRC, f) for f in ("pa_api.cu", "pa_kernels.cu", "pa_attention.cu", "pa_noalloc.cu", "pa_decode.cu")]
 HEADERS = [os.path.join(CSRC, f) for f in ("pa_internal.h", "pa_ptx.cuh", "pa_tiles.cuh")] + [
     os.path.join(HERE, "..", "include", "pa.h")]
 LIB = os.path.join(HERE, "libpa.so")

@@ -125,6 +125,16 @@ struct pa_ctx {
   int kv_rows = -1;
   int kv_cap = -1;
 
+  // decode: per-sequence table (pinned staging, like the plan) and partials
+  DecSeq* d_dec = nullptr;
+  int dec_cap = 0;
+  float* d_part = nullptr;
+  int part_cap = 0;
+  void* h_dec = nullptr;
+  size_t h_dec_cap = 0;
+  cudaEvent_t dec_done = nullptr;
+  bool dec_recorded = false;
+
   // host-buffer path staging
   void* hb[7] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
   size_t hb_cap[7] = {0, 0, 0, 0, 0, 0, 0};
@@ -450,13 +460,16 @@ int pa_create(pa_handle* out, int n_q_heads, int n_kv_heads, int head_dim, int p
 void pa_destroy(pa_handle h) {
   if (!h) return;
   cudaDeviceSynchronize();
-  void* ptrs[] = {h->kw, h->vt, h->ks, h->vs, h->vsmax, h->d_seqs, h->d_units, h->d_err, h->d_counter};
+  void* ptrs[] = {h->kw, h->vt, h->ks, h->vs, h->vsmax, h->d_seqs, h->d_units, h->d_err, h->d_counter, h->d_dec,
+                  h->d_part};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (int i = 0; i < 7; ++i)
     if (h->hb[i]) cudaFree(h->hb[i]);
   if (h->h_stage) cudaFreeHost(h->h_stage);
   if (h->upload_done) cudaEventDestroy(h->upload_done);
+  if (h->h_dec) cudaFreeHost(h->h_dec);
+  if (h->dec_done) cudaEventDestroy(h->dec_done);
   for (cudaEvent_t e : h->ev_free) cudaEventDestroy(e);
   for (cudaEvent_t e : h->ev_pending) cudaEventDestroy(e);
   delete h;
@@ -617,6 +630,69 @@ int pa_kv_append(pa_handle h, const void* k_new, const void* v_new, int n_new, i
   p.v_scale = v_scale;
   p.err = h->d_err;
   PA_CUDA(launch_kv_append(p, static_cast<cudaStream_t>(stream)));
+  return PA_OK;
+}
+
+int pa_decode(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* k_pool, const int8_t* v_pool,
+              const float* k_scale, const float* v_scale, const int32_t* block_table, int n_sink_blk, int n_win_blk,
+              float sm_scale, void* out, void* stream) {
+  int rc = check_inputs(h, q, k_pool, v_pool, k_scale, v_scale, block_table, out);
+  if (rc) return rc;
+  if (n_seq <= 0 || !seqs || h->G > 8 || !(sm_scale == sm_scale) || sm_scale < 0.f) return PA_EINVAL;
+  std::vector<DecSeq> tab((size_t)n_seq);
+  int max_splits = 1;
+  for (int s = 0; s < n_seq; ++s) {
+    const pa_seq& q1 = seqs[s];
+    if (q1.n_q != 1 || q1.q_off < 0 || q1.n_ctx < 1 || q1.q_start != q1.n_ctx - 1) return PA_EINVAL;
+    if ((q1.n_ctx + kPage - 1) / kPage > h->max_pages) return PA_EINVAL;
+    DecSeq& d = tab[(size_t)s];
+    d.q_row = q1.q_off;
+    d.t = q1.n_ctx - 1;
+    d.bt_row = s;
+    const int last = d.t / kPage;
+    d.lo = n_win_blk > 0 ? std::max(0, last + 1 - n_win_blk) : 0;
+    d.n_sink = n_win_blk > 0 ? std::min(std::max(n_sink_blk, 0), d.lo) : 0;
+    d.n_vis = d.n_sink + (last - d.lo + 1);
+    d.n_splits = (d.n_vis + kDecSplitBlocks - 1) / kDecSplitBlocks;
+    d.per_split = kDecSplitBlocks;
+    max_splits = std::max(max_splits, d.n_splits);
+  }
+  if ((rc = grow(h->d_dec, h->dec_cap, (size_t)n_seq))) return rc;
+  if ((rc = grow(h->d_part, h->part_cap, (size_t)n_seq * h->HQ * max_splits * kDecPartStride))) return rc;
+  const size_t bytes = tab.size() * sizeof(DecSeq);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!h->dec_done) PA_CUDA(cudaEventCreateWithFlags(&h->dec_done, cudaEventDisableTiming));
+  if (h->dec_recorded) PA_CUDA(cudaEventSynchronize(h->dec_done));  // never overwrite staging a copy may read
+  if (h->h_dec_cap < bytes) {
+    if (h->h_dec) cudaFreeHost(h->h_dec);
+    h->h_dec = nullptr;
+    h->h_dec_cap = 0;
+    PA_CUDA(cudaMallocHost(&h->h_dec, bytes));
+    h->h_dec_cap = bytes;
+  }
+  std::memcpy(h->h_dec, tab.data(), bytes);
+  PA_CUDA(cudaMemcpyAsync(h->d_dec, h->h_dec, bytes, cudaMemcpyHostToDevice, st));
+  PA_CUDA(cudaEventRecord(h->dec_done, st));
+  h->dec_recorded = true;
+  DecodeParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.k_pool = k_pool;
+  p.v_pool = v_pool;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.block_table = block_table;
+  p.bt_stride = h->max_pages;
+  p.n_pool = h->n_pool;
+  p.seqs = h->d_dec;
+  p.HQ = h->HQ;
+  p.HKV = h->HKV;
+  p.G = h->G;
+  p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  p.part = h->d_part;
+  p.max_splits = max_splits;
+  p.err = h->d_err;
+  PA_CUDA(launch_decode(p, n_seq, st));
   return PA_OK;
 }
 

@@ -86,6 +86,37 @@ struct KvAppendParams {
   int* err;
 };
 cudaError_t launch_kv_append(const KvAppendParams& p, cudaStream_t st);
+
+// Decode: one query token per sequence, split over its visible blocks.
+constexpr int kDecSplitBlocks = 64;  // 16-token blocks per split (one CTA)
+constexpr int kDecPartStride = 260;  // floats per partial: row max (log2), row sum, 2 pad, O[256]
+struct DecSeq {
+  int q_row;     // row of the query token in q / out
+  int t;         // its position in the context (n_ctx - 1)
+  int bt_row;    // block-table row
+  int n_sink;    // sink blocks listed ahead of the window run
+  int lo;        // first block of the window run (0 with the window off)
+  int n_vis;     // visible blocks
+  int n_splits;  // ceil(n_vis / kDecSplitBlocks)
+  int per_split; // blocks per split (the last split may have fewer)
+};
+struct DecodeParams {
+  const __nv_bfloat16* q;  // [rows][HQ][256]
+  __nv_bfloat16* out;      // [rows][HQ][256]
+  const int8_t* k_pool;
+  const int8_t* v_pool;
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* block_table;
+  int bt_stride, n_pool;
+  const DecSeq* seqs;
+  int HQ, HKV, G;
+  float sm_scale_log2;
+  float* part;  // [n_seq][HQ][max_splits][kDecPartStride]
+  int max_splits;
+  int* err;
+};
+cudaError_t launch_decode(const DecodeParams& p, int n_seq, cudaStream_t st);
 cudaError_t launch_attention(const AttnParams& p, const AttnMaps& m, int n_sm, cudaStream_t st);
 
 // Debug exports (tests only).
