@@ -351,33 +351,30 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
         okl = c.warp_wait(B_SCFULL + (t & 1), (t >> 1) & 1, 32);
         tmem_wait_ld(sa);
         reg_fence(sb);
-        // y = S * k_scale (masked: -inf), and this half's row maximum
+        // y = S * k_scale (masked: -inf), and this half's row maximum; the
+        // products in fp32 pairs, the maximum three operands at a time
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (!tg.needs_mask && tg.nb == kTileBlocks) {  // full tile, every row sees every key
+        const bool full = !tg.needs_mask && tg.nb == kTileBlocks;  // every row sees every key
+        const unsigned long long vis = full ? ~0ull : visible_columns(tg, t_row, p.S, p.W, h);
 #pragma unroll
-          for (int q4 = 0; q4 < 16; ++q4) {
-            const float4 k4 = ks4[q4];
-            const float kq[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int q = 4 * q4 + e;
-              y[q] = __uint_as_float(q < 32 ? sa[q] : sb[q - 32]) * kq[e];
-              m4[e] = fmaxf(m4[e], y[q]);
-            }
+        for (int q4 = 0; q4 < 16; ++q4) {
+          const float4 k4 = ks4[q4];
+          const int q = 4 * q4;
+          const uint32_t* src = q < 32 ? sa + q : sb + (q - 32);
+          float2 y01 = mul2(make_float2(__uint_as_float(src[0]), __uint_as_float(src[1])), make_float2(k4.x, k4.y));
+          float2 y23 = mul2(make_float2(__uint_as_float(src[2]), __uint_as_float(src[3])), make_float2(k4.z, k4.w));
+          if (!full) {
+            y01.x = ((vis >> q) & 1ull) ? y01.x : -INFINITY;
+            y01.y = ((vis >> (q + 1)) & 1ull) ? y01.y : -INFINITY;
+            y23.x = ((vis >> (q + 2)) & 1ull) ? y23.x : -INFINITY;
+            y23.y = ((vis >> (q + 3)) & 1ull) ? y23.y : -INFINITY;
           }
-        } else {
-          const unsigned long long vis = visible_columns(tg, t_row, p.S, p.W, h);
-#pragma unroll
-          for (int q4 = 0; q4 < 16; ++q4) {
-            const float4 k4 = ks4[q4];
-            const float kq[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int q = 4 * q4 + e;
-              y[q] = ((vis >> q) & 1ull) ? __uint_as_float(q < 32 ? sa[q] : sb[q - 32]) * kq[e] : -INFINITY;
-              m4[e] = fmaxf(m4[e], y[q]);
-            }
-          }
+          y[q] = y01.x;
+          y[q + 1] = y01.y;
+          y[q + 2] = y23.x;
+          y[q + 3] = y23.y;
+          m4[2 * (q4 & 1)] = max3(m4[2 * (q4 & 1)], y01.x, y01.y);
+          m4[2 * (q4 & 1) + 1] = max3(m4[2 * (q4 & 1) + 1], y23.x, y23.y);
         }
         my = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c_row;  // log2 units
       } else {
@@ -404,20 +401,28 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
         }
       }
       const float mref = m_run == -INFINITY ? 0.f : m_run + ev;
-      // p = 2^(y c - mref); P' = p * v_scale (V scale folded into P)
-      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+      // p = 2^(y c - mref); P' = p * v_scale (V scale folded into P).  Column
+      // q adds into partial sum q mod 4; (s01, s23) hold the four partials.
+      float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
+      const float2 c2 = make_float2(c_row, c_row), nm2 = make_float2(-mref, -mref);
 #pragma unroll
       for (int q4 = 0; q4 < 16; ++q4) {
         const float4 v4 = vs4[q4];
-        const float vq[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int q = 4 * q4 + e;
-          const float pj = ex2_approx(fmaf(y[q], c_row, -mref));
-          s4[e] += pj;
-          y[q] = pj * vq[e];
-        }
+        const int q = 4 * q4;
+        const float2 a01 = fma2(make_float2(y[q], y[q + 1]), c2, nm2);
+        const float2 a23 = fma2(make_float2(y[q + 2], y[q + 3]), c2, nm2);
+        const float2 p01 = make_float2(ex2_approx(a01.x), ex2_approx(a01.y));
+        const float2 p23 = make_float2(ex2_approx(a23.x), ex2_approx(a23.y));
+        s01 = add2(s01, p01);
+        s23 = add2(s23, p23);
+        const float2 w01 = mul2(p01, make_float2(v4.x, v4.y));
+        const float2 w23 = mul2(p23, make_float2(v4.z, v4.w));
+        y[q] = w01.x;
+        y[q + 1] = w01.y;
+        y[q + 2] = w23.x;
+        y[q + 3] = w23.y;
       }
+      const float s4[4] = {s01.x, s01.y, s23.x, s23.y};
       // this warp is done with the tile's scales
       __syncwarp();
       if (okl && lane == 0) mbar_arrive(c.bar(B_SCEMPTY + (t & 1)));
@@ -456,7 +461,11 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
           tmem_ld32(oa, o);
           tmem_wait_ld(o);
 #pragma unroll
-          for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * corr);
+          for (int q = 0; q < 32; q += 2) {
+            const float2 v = mul2(make_float2(__uint_as_float(o[q]), __uint_as_float(o[q + 1])), make_float2(corr, corr));
+            o[q] = __float_as_uint(v.x);
+            o[q + 1] = __float_as_uint(v.y);
+          }
           tmem_st32(oa, o);
         }
       }

@@ -27,6 +27,47 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- fp32 pairs
+// Packed two-lane fp32 arithmetic (sm_100 and later): one instruction does the
+// work of two, with the same IEEE round-to-nearest results as the scalar forms.
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ta, tb, td;\n\t"
+      "mov.b64 ta, {%2, %3};\n\tmov.b64 tb, {%4, %5};\n\t"
+      "mul.rn.f32x2 td, ta, tb;\n\t"
+      "mov.b64 {%0, %1}, td;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ta, tb, td;\n\t"
+      "mov.b64 ta, {%2, %3};\n\tmov.b64 tb, {%4, %5};\n\t"
+      "add.rn.f32x2 td, ta, tb;\n\t"
+      "mov.b64 {%0, %1}, td;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+// a * b + c, each lane rounded once
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ta, tb, tc, td;\n\t"
+      "mov.b64 ta, {%2, %3};\n\tmov.b64 tb, {%4, %5};\n\tmov.b64 tc, {%6, %7};\n\t"
+      "fma.rn.f32x2 td, ta, tb, tc;\n\t"
+      "mov.b64 {%0, %1}, td;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+// max of three (sm_100 and later), as fmaxf(fmaxf(a, b), c)
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
