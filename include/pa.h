@@ -179,6 +179,13 @@ int pa_decode(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const i
               const float* k_scale, const float* v_scale, const int32_t* block_table, int n_sink_blk, int n_win_blk,
               float sm_scale, void* out, void* stream);
 
+/* Query rows per work unit: the G = n_q_heads / n_kv_heads q heads of one kv
+ * head times PA_UNIT_ROWS / G consecutive tokens starting on a multiple of
+ * PA_UNIT_ROWS / G.  One unit is one 256-row tensor-core tile computed by a
+ * pair of SMs (128 rows each), so every row of a unit shares the keys its
+ * tiles visit: the union of the visible key blocks of the unit's query blocks. */
+#define PA_UNIT_ROWS 256
+
 /* Host-only planning, no GPU needed: the work units of a call in launch order
  * (longest first).  units_out (may be NULL) receives up to cap entries of
  * int32[4] = {sequence, kv head, first token, key tiles}.  Outputs: unit
@@ -198,7 +205,8 @@ int pa_debug_gather(pa_handle h, int n_seq, const pa_seq* seqs, const int8_t* k_
 
 /* Debug (tests): for every work unit, the key blocks its tiles visit
  * (unit_blocks int32 [n_units][cap], -1 padded) and per row the number of keys
- * the kernel's mask admits (row_counts int32 [n_units][128]); device pointers.
+ * the kernel's mask admits (row_counts int32 [n_units][PA_UNIT_ROWS]); device
+ * pointers.
  * units_out (host int32 [n_units][4], as pa_plan) names each unit.  Synchronous. */
 int pa_debug_maskset(pa_handle h, int n_seq, const pa_seq* seqs, int n_sink_blk, int n_win_blk,
                      int32_t* row_counts, int32_t* unit_blocks, int cap, int32_t* units_out, int units_cap,

@@ -40,6 +40,14 @@ def test_library_exports_every_declared_symbol(pa):
     assert set(pa.EXPORTED) == set(names)
 
 
+def test_binding_constants_match_the_header(pa):
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    assert int(re.search(r"#define PA_UNIT_ROWS (\d+)", text).group(1)) == pa.UNIT_ROWS
+    csrc = open(os.path.join(ROOT, "windowed_prefill_attention_gb300", "csrc", "pa_tiles.cuh")).read()
+    assert "constexpr int kUnitRows = 2 * kRows;" in csrc and "constexpr int kRows = 128;" in csrc
+    assert pa.UNIT_ROWS == 2 * 128
+
+
 def test_strerror_and_defaults(pa):
     assert pa.pa_strerror(0) == "ok"
     assert "timed out" in pa.pa_strerror(pa.PA_ETIMEOUT)
@@ -106,7 +114,7 @@ def test_plan_covers_rows_once_with_mask_tiles(pa, case):
     _, HQ, HKV, seqs, S, W = case
     units, n_tiles, n_rows = pa.pa_plan(HQ, HKV, seqs, S, W)
     G = HQ // HKV
-    TQ = 128 // G
+    TQ = pa.UNIT_ROWS // G  # tokens per unit
     covered = {}
     lists_of = {s: oracle.block_lists(q_start, n_q, S, W, cap=4096)
                 for s, (_, q_start, n_q, _) in enumerate(seqs)}

@@ -71,7 +71,7 @@ def test_maskset_is_bit_exact(case):
     import windowed_prefill_attention_gb300 as pa
     wl = MASK_CASES[case]
     G = wl.n_q_heads // wl.n_kv_heads
-    TQ = 128 // G
+    TQ = pa.UNIT_ROWS // G  # tokens per unit
     seq_desc = make_inputs(wl).seq_desc if wl.total_q < 20000 else None
     if seq_desc is None:
         seq_desc = np.array([(0, qs, nq, qs + nq) for qs, nq in wl.seqs], np.int32)
@@ -98,7 +98,7 @@ def test_maskset_is_bit_exact(case):
         visited = blocks[u][blocks[u] >= 0].tolist()
         assert sorted(visited) == sorted(union), (case, u)
         assert len(visited) == len(set(visited)), "a block visited twice"
-        for r in range(128):
+        for r in range(pa.UNIT_ROWS):
             t = t0 + r // G
             if q_start <= t < q_start + n_q:
                 assert counts[u, r] == oracle.visible_count(t, wl.n_sink_blk, wl.n_win_blk), (case, u, r)

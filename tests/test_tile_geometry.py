@@ -32,8 +32,7 @@ static bool sees(int t, int j, int S, int W) {
 }
 int main() {
   long checked = 0;
-  for (int G : {1, 2, 4, 8, 16}) {
-    const int TQ = kRows / G;
+  for (int G : {1, 2, 4, 8, 16}) for (int TQ : {kRows / G, kUnitRows / G}) {
     for (int S : {0, 1, 2, 5}) for (int W : {0, 1, 3, 4, 7, 16}) for (int q_start : {0, 5, 48, 300}) for (int n_q : {1, 17, 130, 333}) {
       SeqGeom sg{};
       sg.q_start = q_start; sg.n_q = n_q; sg.n_ctx = q_start + n_q;

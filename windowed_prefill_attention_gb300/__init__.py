@@ -24,6 +24,8 @@ _lib = C.CDLL(_LIB_PATH)
 
 PA_OK, PA_EINVAL, PA_EARCH, PA_ECUDA, PA_ETIMEOUT, PA_EBADPAGE, PA_ENOMEM, PA_ENOSCRATCH = 0, -1, -2, -3, -4, -5, -6, -7
 PA_NOALLOC_SCRATCH_BYTES = 32 << 20
+# query rows per work unit (PA_UNIT_ROWS in include/pa.h)
+UNIT_ROWS = 256
 PA_Q_BF16, PA_Q_INT8 = 0, 1
 PA_P_F16, PA_P_U8 = 0, 1
 
@@ -267,7 +269,7 @@ def pa_debug_maskset(h, seqs, n_sink_blk, n_win_blk, units_cap, cap, stream=None
     """Per unit: visited key blocks and per-row admitted key counts (see include/pa.h)."""
     import torch
     s = _seqs(seqs)
-    counts = torch.empty((units_cap, 128), dtype=torch.int32, device="cuda")
+    counts = torch.empty((units_cap, UNIT_ROWS), dtype=torch.int32, device="cuda")
     blocks = torch.empty((units_cap, cap), dtype=torch.int32, device="cuda")
     units = np.zeros((units_cap, 4), dtype=np.int32)
     n = C.c_int()

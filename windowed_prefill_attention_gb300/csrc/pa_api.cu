@@ -52,7 +52,7 @@ int build_plan(int HQ, int HKV, int n_seq, const pa_seq* seqs, int S, int W, int
   const int G = HQ / HKV;
   if (G > kRows || kRows % G != 0) return PA_EINVAL;
   if (n_seq <= 0 || seqs == nullptr || S < 0) return PA_EINVAL;
-  const int TQ = kRows / G;
+  const int UT = kUnitRows / G;  // tokens per unit
   P = Plan();
   int tok_off = 0;
   for (int s = 0; s < n_seq; ++s) {
@@ -72,9 +72,9 @@ int build_plan(int HQ, int HKV, int n_seq, const pa_seq* seqs, int S, int W, int
     if (tok_off > (1 << 30)) return PA_EINVAL;
     P.seqs.push_back(g);
     P.total_q = std::max(P.total_q, q.q_off + q.n_q);
-    const int t_first = (q.q_start / TQ) * TQ;
-    for (int t0 = t_first; t0 < q.q_start + q.n_q; t0 += TQ) {
-      const UnitGeom ug = unit_geom(t0, TQ, g, S, W);
+    const int t_first = (q.q_start / UT) * UT;
+    for (int t0 = t_first; t0 < q.q_start + q.n_q; t0 += UT) {
+      const UnitGeom ug = unit_geom(t0, UT, g, S, W);
       for (int kv = 0; kv < HKV; ++kv) {
         P.units.push_back(Unit{s, kv, t0, ug.n_tiles});
         P.n_tiles += ug.n_tiles;
@@ -320,13 +320,13 @@ int run(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t*
   if (h->kw != h->kv_ptr || P.n_tok_total != h->kv_rows || h->n_tok_cap != h->kv_cap) {
     const uint64_t kd[3] = {(uint64_t)kHeadDim, (uint64_t)P.n_tok_total, (uint64_t)h->HKV};
     const uint64_t kst[2] = {(uint64_t)kHeadDim * 2, (uint64_t)h->n_tok_cap * kHeadDim * 2};
-    const uint32_t kbox[3] = {64, (uint32_t)kTileKeys, 1};
+    const uint32_t kbox[3] = {64, (uint32_t)kTileKeys / 2, 1};  // one CTA's half of a tile
     if ((rc = encode(&h->maps.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, h->kw, kd, kst, kbox,
                      CU_TENSOR_MAP_SWIZZLE_128B)))
       return rc;
     const uint64_t vd[3] = {(uint64_t)P.n_tok_total, (uint64_t)kHeadDim, (uint64_t)h->HKV};
     const uint64_t vst[2] = {(uint64_t)h->n_tok_cap * 2, (uint64_t)h->n_tok_cap * kHeadDim * 2};
-    const uint32_t vbox[3] = {(uint32_t)kChunkKeys, (uint32_t)kHeadDim, 1};
+    const uint32_t vbox[3] = {(uint32_t)kChunkKeys, (uint32_t)kHeadDim / 2, 1};  // one CTA's half of the dims
     if ((rc = encode(&h->maps.v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, h->vt, vd, vst, vbox,
                      CU_TENSOR_MAP_SWIZZLE_128B)))
       return rc;
@@ -352,7 +352,9 @@ int run(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t*
     PA_CUDA(cudaEventRecord(e0, st));
   }
   PA_CUDA(cudaMemsetAsync(h->vsmax, 0, sizeof(unsigned int) * n_seq * h->HKV, st));
-  PA_CUDA(launch_widen(widen_params(h, kp, vp, ksc, vsc, bt, n_seq), st));
+  WidenParams wp = widen_params(h, kp, vp, ksc, vsc, bt, n_seq);
+  wp.k_mult = sm_scale * 1.4426950408889634f;  // the softmax's sm_scale * log2(e), folded into the K scales
+  PA_CUDA(launch_widen(wp, st));
   if (e1) PA_CUDA(cudaEventRecord(e1, st));
   AttnParams a{};
   a.q = static_cast<const __nv_bfloat16*>(q);
@@ -712,7 +714,7 @@ int pa_debug_maskset(pa_handle h, int n_seq, const pa_seq* seqs, int n_sink_blk,
     units_out[4 * i + 2] = P.units[i].t0;
     units_out[4 * i + 3] = P.units[i].n_tiles;
   }
-  PA_CUDA(launch_debug_maskset(h->d_seqs, h->d_units, (int)P.units.size(), h->TQ, h->G, n_sink_blk, n_win_blk,
+  PA_CUDA(launch_debug_maskset(h->d_seqs, h->d_units, (int)P.units.size(), 2 * h->TQ, h->G, n_sink_blk, n_win_blk,
                                row_counts, unit_blocks, cap, st));
   return pa_last_error(h, stream);
 }

@@ -11,23 +11,31 @@
 // (tcgen05.mma kind::f16), which hold them exactly: K in bf16 against the bf16
 // query, V in fp16 against P' in fp16.
 //
-// One CTA per SM walks the longest-first unit list with stride gridDim.x.  A
-// unit is 128 query rows of one kv head; key tiles are 128 keys (pa_tiles.cuh).
-// With N = 128 a QK^T instruction runs at the tensor core's full rate (at
-// N = 64 it does not), which sets the memory plan:
-//   TMEM (512 columns)   O fp32 [0,256), S0 [256,384), S1 [384,512); P (fp16
-//                        pairs) of warp half h overwrites S columns [64h, 64h+32)
-//   shared memory        Q (64 KB, bf16, TMA), K as four 16 KB slots, one per
-//                        64-dim region of a tile, V^T as two 32 KB slots of 64
-//                        keys, the tiles' K/V scales in two 1 KB slots
-// Each K region slot is released by the commit after the four k-steps that
-// read it, so region r of the next tile loads while this tile's later regions
-// are multiplied.  Roles:
-//   warp 0        TMA producer of the K regions (one lane per region)
-//   warp 1        TMEM allocator and the single MMA-issuing thread; QK^T(j+1)
-//                 is issued before PV(j), so the tensor core works on the next
-//                 scores while the softmax handles the current ones
-//   warp 2        TMA producer of the V^T chunks (one lane per slot)
+// Pairs of SMs (clusters of two CTAs, one per SM) walk the longest-first
+// unit list with stride = the number of pairs.  A unit is 256 query rows of
+// one kv head (pa_tiles.cuh), 128 in each CTA; one 256-row tcgen05 MMA
+// (cta_group::2, issued by the even CTA) covers both, with the B operand (K
+// keys for QK^T, V^T dims for PV) split between the two CTAs' shared memory,
+// so each SM stores and reads only half of every K/V tile.  Key tiles are
+// 128 keys; with N = 128 a QK^T instruction runs at the tensor core's full
+// rate (at N = 64 it does not), which sets the memory plan, per CTA:
+//   TMEM (512 columns)   O fp32 [0,256), S0 [256,384), S1 [384,512) for the
+//                        CTA's 128 rows; P' (fp16 pairs) of softmax half h
+//                        overwrites S columns [64h, 64h+32)
+//   shared memory        Q (64 KB, bf16, TMA), K as 2 x 4 slots of 8 KB (tile
+//                        parity x 64-dim region; this CTA's 64 keys), V^T as
+//                        2 x 2 slots of 16 KB (tile parity x 64-key chunk;
+//                        this CTA's 128 dims), the tiles' K/V scales in two
+//                        1 KB slots
+// K and V^T are double-buffered by tile parity, so the MMA issuer waits once
+// per operand per tile.  Roles (both CTAs unless noted):
+//   warp 0        TMA producer of K (one lane per slot); the odd CTA's copies
+//                 complete on the even CTA's barrier
+//   warp 1        TMEM allocator (for the pair); in the even CTA the single
+//                 MMA-issuing thread; QK^T(j+1) is issued before PV(j), so the
+//                 tensor core works on the next scores while the softmax
+//                 handles the current ones
+//   warp 2        TMA producer of V^T (one lane per slot), as warp 0
 //   warp 3        producer of Q (TMA, one lane per region, after an L2
 //                 prefetch) and of the scales
 //   warps 4-11    softmax: one query row per thread (TMEM lane = row), two
@@ -45,22 +53,51 @@
 namespace pa {
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kRegionBytes = kTileKeys * 128;           // 16 KB: 128 rows x 64 dims (bf16)
-constexpr int kChunkBytes = kHeadDim * kChunkKeys * 2;  // 32 KB: 256 dims x 64 keys (fp16)
-// Shared memory, offsets from a 1024-byte aligned base.
-constexpr int kSmQ = 0;                                 // 4 regions of 128 rows x 128 B
-constexpr int kSmK = kSmQ + 4 * kRegionBytes;           // 4 region slots
-constexpr int kSmV = kSmK + 4 * kRegionBytes;           // 2 chunk slots
-constexpr int kSmScale = kSmV + 2 * kChunkBytes;        // 2 slots: ks[128], vs[128]
-constexpr int kSmRows = kSmScale + 2 * 1024;            // c[2][128], l[2][2][128], sp[2][128] floats
-constexpr int kSmXchg = kSmRows + 8 * kRows * 4;        // softmax pair exchange: 2 x [2][2][128] floats
-constexpr int kSmStage = kSmXchg + 8 * kRows * 4;       // epilogue: 4 x [32 rows][128 B]
+constexpr int kSlices = 2;                              // softmax warps per TMEM lane quadrant
+constexpr int kSoftmaxWarps = 4 * kSlices;             // warps 4 .. 11
+constexpr int kThreads = 32 * (4 + kSoftmaxWarps + 4);  // + producers/MMA (0-3) and epilogue (12-15)
+constexpr int kRegionBytes = kRows * 128;                 // 16 KB: Q, 128 rows x 64 dims (bf16)
+constexpr int kKSlotBytes = (kTileKeys / 2) * 128;        // 8 KB: this CTA's 64 keys x 64 dims (bf16)
+constexpr int kVSlotBytes = (kHeadDim / 2) * kChunkKeys * 2;  // 16 KB: this CTA's 128 dims x 64 keys (fp16)
+constexpr int kKSlots = 8;                                // [tile parity][64-dim region]
+constexpr int kVSlots = 4;                                // [tile parity][64-key chunk]
+// Shared memory, offsets from a 1024-byte aligned base (the same in both CTAs).
+constexpr int kSmQ = 0;                                   // 4 regions of 128 rows x 128 B
+constexpr int kSmK = kSmQ + 4 * kRegionBytes;             // K slots
+constexpr int kSmV = kSmK + kKSlots * kKSlotBytes;        // V^T slots
+constexpr int kSmScale = kSmV + kVSlots * kVSlotBytes;    // 2 slots: k'[128], vs[128]
+constexpr int kSmRows = kSmScale + 2 * 1024;              // c[2][128], l[2][kSlices][128], sp[2][128] floats
+constexpr int kSmXchg = kSmRows + (4 + 2 * kSlices) * kRows * 4;  // softmax slice exchange: 2 x [2][kSlices][128] floats
+constexpr int kSmStage = kSmXchg + 4 * kSlices * kRows * 4;  // epilogue: 4 x [32 rows][128 B]
 constexpr int kSmBars = kSmStage + 4 * 4096;
+// Barriers.  "Pair" barriers are waited on by the even CTA's MMA issuer and
+// count arrivals from both CTAs (the odd CTA arrives through the cluster);
+// "both" barriers are arrived on in both CTAs by one multicast MMA commit.
+//
+// Every K tile and V^T tile has one "full" barrier (by tile parity), so the
+// MMA issuer waits once per operand per tile: a wait or a commit between two
+// MMAs leaves the tensor pipe idle for tens of cycles, and the issuer's
+// waits and commits add up on the critical path.  QK^T(t) done (S full) also
+// frees the K slots of tile t.
 enum : int {
-  B_KFULL = 0, B_KEMPTY = 4, B_VFULL = 8, B_VEMPTY = 10, B_SCFULL = 12, B_SCEMPTY = 14, B_SFULL = 16,
-  B_PFULL = 18, B_QFULL = 20, B_QREADY = 21, B_QEMPTY = 22, B_OFULL = 23, B_OEMPTY = 24,
-  B_STATS = 25 /* two, by unit parity */, B_STALL = 27, B_DRAIN = 28, B_QSOON = 29, kNumBars = 30
+  B_KFULL = 0,      // [2] by tile parity, pair: the tile's K landed in both CTAs
+  B_VFULL = 2,      // [2] by tile parity, pair: the tile's V^T chunks landed in both CTAs
+  B_VEMPTY = 4,     // [2] by tile parity, both: the tile's PV is done (V^T slots free)
+  B_SCFULL = 6,     // [2] the tile's scales landed (each CTA loads its own copy)
+  B_SCEMPTY = 8,    // [2] every softmax warp read them
+  B_SFULL = 10,     // [2] both: S of a tile is in TMEM (and its K slots are free)
+  B_PFULL = 12,     // [2] pair: P of a tile is in TMEM (every softmax warp of both CTAs)
+  B_QFULL = 14,     // Q landed (in the even CTA: in both CTAs)
+  B_QREADY = 15,    // this CTA's Q codes on the int8 grid are written
+  B_QREADY2 = 16,   // pair: both CTAs' Q codes are written
+  B_QEMPTY = 17,    // both: the unit's last QK^T is done
+  B_OFULL = 18,     // both: the unit's last PV is done
+  B_OEMPTY = 19,    // pair: the epilogue of both CTAs has read O
+  B_STATS = 20,     // [2] by unit parity: the softmax's row sums are written
+  B_STALL = 22,     // test hook: nothing arrives
+  B_DRAIN = 23,     // both: every MMA is done
+  B_QSOON = 24,     // the unit's Q may be prefetched
+  kNumBars = 25
 };
 constexpr int kSmTmemSlot = kSmBars + kNumBars * 8;
 constexpr int kAttnSmem = kSmTmemSlot + 16 + 1024;  // + alignment slack
@@ -97,16 +134,40 @@ __device__ __forceinline__ int pow2_ceil_exp(float x) {
 __device__ __forceinline__ int n_chunks(int nb) { return (nb + 3) / 4; }
 
 struct Ctx {
-  uint32_t sbase;  // shared address of the aligned base
-  uint32_t tb;     // TMEM base address
+  uint32_t sbase;    // shared address of the aligned base
+  uint32_t tb;       // TMEM base address (the same in both CTAs)
+  uint32_t rank;     // 0: the even CTA of the pair (issues the MMAs), 1: the odd one
+  int pair, n_pairs; // this pair's index and the number of pairs (units are strided over pairs)
   WaitCtl wc;
   __device__ uint32_t bar(int i) const { return sbase + kSmBars + 8 * i; }
-  // Bounded wait by all 32 lanes of a warp with one outcome for the warp, so
-  // that the warp-collective tcgen05.ld/st and __syncwarp that follow never
-  // see a diverged warp, also when a wait runs out.
+  // Bounded wait.  Phases completed by the other CTA of the pair hand over
+  // data that TMA copies or tcgen05 operations wrote (the copy's complete_tx,
+  // the MMA commit, or tcgen05.wait + fence before the arrival order it), so
+  // an acquire at CTA scope suffices; a cluster-scope acquire costs the MMA
+  // issuer ~100 cycles more per wait.
+  __device__ bool wait(int i, uint32_t parity, int site) const { return mbar_wait(bar(i), parity, wc, site); }
+  // Bounded wait acquiring at cluster scope: for a phase that publishes the
+  // other CTA's generic-proxy shared-memory writes (the int8 Q codes).
+  __device__ bool wait_cluster(int i, uint32_t parity, int site) const {
+    return mbar_wait_cluster(bar(i), parity, wc, site);
+  }
+  // The same by all 32 lanes of a warp with one outcome for the warp, so that
+  // the warp-collective tcgen05.ld/st and __syncwarp that follow never see a
+  // diverged warp, also when a wait runs out.
   __device__ bool warp_wait(int i, uint32_t parity, int site) const {
-    const bool r = mbar_wait(bar(i), parity, wc, site);
-    return __all_sync(0xffffffffu, r);
+    return __all_sync(0xffffffffu, wait(i, parity, site));
+  }
+  // Arrive on a pair barrier (in the even CTA), publishing this thread's
+  // generic-proxy writes to the other CTA.
+  __device__ void arrive_pair(int i) const {
+    if (rank == 0) mbar_arrive(bar(i));
+    else mbar_arrive_cluster(cluster_addr(bar(i), 0));
+  }
+  // The same for a tensor-memory hand-off (the caller has waited for its
+  // tcgen05.st/ld and fenced with tcgen05.fence::before_thread_sync).
+  __device__ void arrive_pair_tmem(int i) const {
+    if (rank == 0) mbar_arrive(bar(i));
+    else mbar_arrive_remote(cluster_addr(bar(i), 0));
   }
 };
 
@@ -115,187 +176,240 @@ struct Ctx {
 // issuing thread moves ~29-36 B/clk of 16 KB tiles from L2 into shared memory
 // whatever the number in flight, four threads ~70 B/clk), so every stream
 // of copies is spread over several lanes, each with its own slots.
+//
+// Each CTA loads its own half of every K tile and V^T chunk into its own
+// shared memory; both copies complete their bytes on the even CTA's barrier
+// (the odd CTA's through the pair form of the TMA load), which expects both
+// halves, so its phase means "both halves landed" to the MMA issuer.
 
-// K: lane r loads region r (dims [64r, 64r+64), 128 keys) of every tile into
-// slot r.  Slot r is used once per tile, so its phases follow the tile counter.
-__device__ __forceinline__ void role_producer_k(const AttnParams& p, const AttnMaps& m, const Ctx& c, int r) {
-  uint32_t kt = 0;  // tiles loaded
+// K: lane s loads region r = s % 4 (dims [64 r, 64 r + 64)) of the tiles of
+// parity s / 4 into slot s: this CTA's N/2 keys of the tile, from key
+// rank * N/2 on, N = 16 nb (the MMA takes N/2 rows from each CTA's slot).  The
+// slot is free again once QK^T of the tile two before is done (S full).
+__device__ __forceinline__ void role_producer_k(const AttnParams& p, const AttnMaps& m, const Ctx& c, int s) {
+  const int r = s & 3, par = s >> 2;
+  uint32_t uses = 0, tc = 0;  // tiles this slot held; tiles so far
   bool ok = true;
-  for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+  for (int u = c.pair; u < p.n_units && ok; u += c.n_pairs) {
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
-    const UnitGeom ug = unit_geom(un.t0, p.TQ, sg, p.S, p.W);
-    for (int j = 0; j < ug.n_tiles; ++j, ++kt) {
-      const int crow = logical_block_row(sg, tile_geom(ug, j, p.S, p.W).kb0);
-      if (!(ok = mbar_wait(c.bar(B_KEMPTY + r), (kt & 1) ^ 1, c.wc, 10))) break;
-      const uint32_t fb = c.bar(B_KFULL + r);
-      mbar_expect_tx(fb, kRegionBytes);
-      tma_load_3d(c.sbase + kSmK + r * kRegionBytes, &m.k, fb, r * 64, crow, un.g);
+    const UnitGeom ug = unit_geom(un.t0, 2 * p.TQ, sg, p.S, p.W);
+    for (int j = 0; j < ug.n_tiles; ++j) {
+      if ((int)((tc + j) & 1) != par) continue;
+      const TileGeom tg = tile_geom(ug, j, p.S, p.W);
+      const int row = logical_block_row(sg, tg.kb0) + (int)c.rank * tg.nb * (kPage / 2);
+      if (!(ok = c.wait(B_SFULL + par, (uses & 1) ^ 1, 10))) break;
+      const uint32_t fb = c.bar(B_KFULL + par);
+      if (c.rank == 0) {
+        mbar_expect_tx(fb, 2 * kKSlotBytes);  // one of four arrivals: this region of both CTAs
+        tma_load_3d(c.sbase + kSmK + s * kKSlotBytes, &m.k, fb, r * 64, row, un.g);
+      } else {
+        tma_load_3d_pair(c.sbase + kSmK + s * kKSlotBytes, &m.k, cluster_addr(fb, 0), r * 64, row, un.g);
+      }
+      ++uses;
     }
+    tc += ug.n_tiles;
   }
-  // every issued copy lands before the CTA may exit
-  if (kt > 0) (void)mbar_wait_drain(c.bar(B_KFULL + r), (kt - 1) & 1, kDrainNs);
+  // every issued copy lands before the CTA may exit: the MMAs that read the
+  // slot's last copy are done (bounded: on an error they may never run)
+  if (uses > 0) (void)mbar_wait_drain(c.bar(B_SFULL + par), (uses - 1) & 1, kDrainNs);
 }
 
-// V^T: the tiles' 64-key chunks go through a two-slot ring; lane s loads the
-// chunks that land in slot s.
+// V^T: lane s loads chunk ch = s % 2 (keys [64 ch, 64 ch + 64)) of the tiles of
+// parity s / 2 into slot s: this CTA's 128 of the 256 dims.  Lane (parity, 0)
+// of the even CTA expects the bytes of all the tile's chunks in both CTAs;
+// the slot is free again once PV of the tile two before is done.
 __device__ __forceinline__ void role_producer_v(const AttnParams& p, const AttnMaps& m, const Ctx& c, int s) {
-  uint32_t vc = 0;    // chunks of all tiles so far
-  uint32_t last = 0;  // 1 + index of the last chunk this lane loaded
+  const int ch = s & 1, par = s >> 1;
+  uint32_t uses = 0, tc = 0;  // tiles of this parity so far; tiles so far
   bool ok = true;
-  for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+  for (int u = c.pair; u < p.n_units && ok; u += c.n_pairs) {
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
-    const UnitGeom ug = unit_geom(un.t0, p.TQ, sg, p.S, p.W);
-    for (int j = 0; j < ug.n_tiles && ok; ++j) {
-      const TileGeom tg = tile_geom(ug, j, p.S, p.W);
-      const int crow = logical_block_row(sg, tg.kb0);
-      for (int ch = 0; ch < n_chunks(tg.nb); ++ch, ++vc) {
-        if ((int)(vc & 1) != s) continue;
-        if (!(ok = mbar_wait(c.bar(B_VEMPTY + s), ((vc >> 1) & 1) ^ 1, c.wc, 11))) break;
-        const uint32_t fb = c.bar(B_VFULL + s);
-        mbar_expect_tx(fb, kChunkBytes);
-        tma_load_3d(c.sbase + kSmV + s * kChunkBytes, &m.v, fb, crow + ch * kChunkKeys, 0, un.g);
-        last = vc + 1;
+    const UnitGeom ug = unit_geom(un.t0, 2 * p.TQ, sg, p.S, p.W);
+    for (int j = 0; j < ug.n_tiles; ++j) {
+      if ((int)((tc + j) & 1) != par) continue;
+      const int nch = n_chunks(tile_width(ug, j));
+      const uint32_t use = uses++;
+      // every lane waits for every tile of its parity, also one it has no
+      // chunk of: a parity wait cannot tell phase k from k - 2, so a lane that
+      // skipped a wait could pass the next one two phases early
+      if (!(ok = c.wait(B_VEMPTY + par, (use & 1) ^ 1, 11))) break;
+      if (ch >= nch) continue;  // a tile of one chunk
+      const int crow = logical_block_row(sg, tile_geom(ug, j, p.S, p.W).kb0);
+      const uint32_t fb = c.bar(B_VFULL + par);
+      const uint32_t dst = c.sbase + kSmV + s * kVSlotBytes;
+      if (c.rank == 0) {
+        if (ch == 0) mbar_expect_tx(fb, (uint32_t)nch * 2 * kVSlotBytes);
+        tma_load_3d(dst, &m.v, fb, crow + ch * kChunkKeys, 0, un.g);
+      } else {
+        tma_load_3d_pair(dst, &m.v, cluster_addr(fb, 0), crow + ch * kChunkKeys, kHeadDim / 2, un.g);
       }
     }
+    tc += ug.n_tiles;
   }
-  if (last > 0) (void)mbar_wait_drain(c.bar(B_VFULL + s), ((last - 1) >> 1) & 1, kDrainNs);
+  if (uses > 0) (void)mbar_wait_drain(c.bar(B_VEMPTY + par), (uses - 1) & 1, kDrainNs);
 }
 
-// Prefetch into L2 the rows of a unit in a [tokens][HQ][256] bf16 tensor (q or
-// the output gate): per token its G heads are contiguous.
-__device__ __forceinline__ void prefetch_unit_rows(const AttnParams& p, const __nv_bfloat16* base, const Unit& un,
-                                                   const SeqGeom& sg) {
-  const int tok0 = sg.q_off + (un.t0 - sg.q_start);
+// Prefetch into L2 the rows of TQ tokens from t0 in a [tokens][HQ][256] bf16
+// tensor (q or the output gate): per token its G heads are contiguous.
+__device__ __forceinline__ void prefetch_rows(const AttnParams& p, const __nv_bfloat16* base, int t0, int g,
+                                              const SeqGeom& sg) {
+  const int tok0 = sg.q_off + (t0 - sg.q_start);
   for (int i = 0; i < p.TQ; ++i) {
     const int tok = tok0 + i;
     if (tok >= sg.q_off && tok < sg.q_off + sg.n_q)
-      bulk_prefetch_l2(base + ((size_t)tok * p.HQ + (size_t)un.g * p.G) * kHeadDim, (uint32_t)p.G * kHeadDim * 2);
+      bulk_prefetch_l2(base + ((size_t)tok * p.HQ + (size_t)g * p.G) * kHeadDim, (uint32_t)p.G * kHeadDim * 2);
   }
 }
 
-// Q of each unit (after the previous unit's last QK^T): lane r loads region r.
-// Lane 0 also prefetches into L2 the unit's Q rows and the previous unit's
-// output-gate rows (both a few tiles before they are needed) and loads the
-// K/V scales of each tile (two-slot ring by tile parity).
+// Q of each unit (this CTA's 128 rows, after the pair's last QK^T of the
+// previous unit): lane r < 4 loads region r.  Lane 0 also prefetches into L2
+// the unit's Q rows and the previous unit's output-gate rows (both a few tiles
+// before they are needed) and, in the odd CTA, passes the arrival of its Q on
+// to the even CTA.  Lane 4 loads the K/V scales of each tile (two-slot ring
+// by tile parity).
 __device__ __forceinline__ void role_producer_q(const AttnParams& p, const AttnMaps& m, const Ctx& c, int r) {
   uint32_t ts = 0;  // tiles whose scales were loaded
   int k_unit = 0;   // units whose Q was loaded
   bool ok = true;
-  Unit prev_un{};
+  int prev_t0 = 0, prev_g = 0;
   SeqGeom prev_sg{};
-  for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+  for (int u = c.pair; u < p.n_units && ok; u += c.n_pairs) {
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
-    const UnitGeom ug = unit_geom(un.t0, p.TQ, sg, p.S, p.W);
-    // q row (token position in q) of the unit's first token; negative or past
-    // the sequence where the unit overhangs it: those rows are never output
-    const int tok0 = sg.q_off + (un.t0 - sg.q_start);
-    if (k_unit > 0) {
-      if (!(ok = mbar_wait(c.bar(B_QSOON), (k_unit - 1) & 1, c.wc, 12))) break;
-      if (r == 0) {
-        prefetch_unit_rows(p, p.q, un, sg);
-        if (p.gate) prefetch_unit_rows(p, p.gate, prev_un, prev_sg);
+    const int t0 = un.t0 + (int)c.rank * p.TQ;  // this CTA's first token
+    if (r == 4) {
+      const UnitGeom ug = unit_geom(un.t0, 2 * p.TQ, sg, p.S, p.W);
+      for (int j = 0; j < ug.n_tiles; ++j) {
+        const uint32_t s = ts & 1;
+        if (!(ok = c.wait(B_SCEMPTY + s, ((ts >> 1) & 1) ^ 1, 14))) break;
+        const TileGeom tg = tile_geom(ug, j, p.S, p.W);
+        const int crow = logical_block_row(sg, tg.kb0);
+        const uint32_t bytes = (uint32_t)(tg.nb * kPage * 4);
+        const uint32_t fb = c.bar(B_SCFULL + s);
+        mbar_expect_tx(fb, 2 * bytes);
+        bulk_load(c.sbase + kSmScale + s * 1024, p.ks + (size_t)un.g * p.n_tok_cap + crow, bytes, fb);
+        bulk_load(c.sbase + kSmScale + s * 1024 + 512, p.vs + (size_t)un.g * p.n_tok_cap + crow, bytes, fb);
+        ++ts;
       }
-      if (!(ok = mbar_wait(c.bar(B_QEMPTY), (k_unit - 1) & 1, c.wc, 13))) break;
+      continue;
     }
-    prev_un = un;
+    // q row (token position in q) of this CTA's first token; negative or past
+    // the sequence where the unit overhangs it: those rows are never output
+    const int tok0 = sg.q_off + (t0 - sg.q_start);
+    if (k_unit > 0) {
+      if (!(ok = c.wait(B_QSOON, (k_unit - 1) & 1, 12))) break;
+      if (r == 0) {
+        prefetch_rows(p, p.q, t0, un.g, sg);
+        if (p.gate) prefetch_rows(p, p.gate, prev_t0, prev_g, prev_sg);
+      }
+      if (!(ok = c.wait(B_QEMPTY, (k_unit - 1) & 1, 13))) break;
+    }
+    prev_t0 = t0;
+    prev_g = un.g;
     prev_sg = sg;
     mbar_expect_tx(c.bar(B_QFULL), kRegionBytes);
     tma_load_3d(c.sbase + kSmQ + r * kRegionBytes, &m.q, c.bar(B_QFULL), r * 64, un.g * p.G, tok0);
-    ++k_unit;
-    if (r != 0) continue;
-    for (int j = 0; j < ug.n_tiles; ++j) {
-      const uint32_t s = ts & 1;
-      if (!(ok = mbar_wait(c.bar(B_SCEMPTY + s), ((ts >> 1) & 1) ^ 1, c.wc, 14))) break;
-      const TileGeom tg = tile_geom(ug, j, p.S, p.W);
-      const int crow = logical_block_row(sg, tg.kb0);
-      const uint32_t bytes = (uint32_t)(tg.nb * kPage * 4);
-      const uint32_t fb = c.bar(B_SCFULL + s);
-      mbar_expect_tx(fb, 2 * bytes);
-      bulk_load(c.sbase + kSmScale + s * 1024, p.ks + (size_t)un.g * p.n_tok_cap + crow, bytes, fb);
-      bulk_load(c.sbase + kSmScale + s * 1024 + 512, p.vs + (size_t)un.g * p.n_tok_cap + crow, bytes, fb);
-      ++ts;
+    if (c.rank == 1 && r == 0) {
+      if (!(ok = c.wait(B_QFULL, k_unit & 1, 17))) break;
+      mbar_arrive_cluster(cluster_addr(c.bar(B_QFULL), 0));
     }
+    ++k_unit;
   }
-  if (k_unit > 0) (void)mbar_wait_drain(c.bar(B_QFULL), (k_unit - 1) & 1, kDrainNs);
+  if (r < 4 && k_unit > 0) (void)mbar_wait_drain(c.bar(B_QFULL), (k_unit - 1) & 1, kDrainNs);
   for (uint32_t i = 0; i < 2; ++i)
     if (ts > i) (void)mbar_wait_drain(c.bar(B_SCFULL + ((ts - 1 - i) & 1)), ((ts - 1 - i) >> 1) & 1, kDrainNs);
 }
 
 // ------------------------------------------------------------------ MMA issuer
+// One thread of the even CTA issues every MMA of the pair: 256 query rows
+// (128 in each CTA's TMEM lanes) against the tile's keys.
 __device__ __forceinline__ void role_mma(const AttnParams& p, const Ctx& c) {
-  uint32_t tc = 0;  // global tile counter: K phases and S buffer of every tile
-  uint32_t vc = 0;  // global V^T chunk counter
+  uint32_t tc = 0;  // global tile counter: K/V slots and S buffer by its parity
   int k_unit = 0;
   bool ok = true;
-  const uint32_t id_pv = idesc_f16(kRows, kHeadDim, false, false);
-  for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++k_unit) {
+  const uint32_t id_pv = idesc_f16(kUnitRows, kHeadDim, false, false);
+  const uint32_t qsoon_peer = cluster_addr(c.bar(B_QSOON), 1);
+  for (int u = c.pair; u < p.n_units && ok; u += c.n_pairs, ++k_unit) {
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
-    const UnitGeom ug = unit_geom(un.t0, p.TQ, sg, p.S, p.W);
+    const UnitGeom ug = unit_geom(un.t0, 2 * p.TQ, sg, p.S, p.W);
     const int n = ug.n_tiles;
-    const int qbar = p.debug_stall ? B_STALL : (p.q_mode == 1 ? B_QREADY : B_QFULL);
-    if (!(ok = mbar_wait(c.bar(qbar), k_unit & 1, c.wc, 20))) break;
+    const int qbar = p.debug_stall ? B_STALL : (p.q_mode == 1 ? B_QREADY2 : B_QFULL);
+    if (!(ok = (qbar == B_QREADY2 ? c.wait_cluster(qbar, k_unit & 1, 20) : c.wait(qbar, k_unit & 1, 20)))) break;
     for (int j = 0; j <= n; ++j) {
       if (j < n) {  // S(j) = Q K(j)^T, region by region
         const uint32_t t = tc + j;
         const uint32_t d = c.tb + kTmS + (t & 1) * kTileKeys;
-        const uint32_t id = idesc_f16(kRows, tile_width(ug, j) * kPage, true, true);  // bf16 Q, bf16 K codes
-        for (int r = 0; r < 4; ++r) {
-          if (!(ok = mbar_wait(c.bar(B_KFULL + r), t & 1, c.wc, 21))) break;
-          tc_fence_after();
-          // Q region r and K slot r: SW128 K-major, k-step s at +32 s bytes
-          const uint64_t qd = sdesc_k_sw128(c.sbase + kSmQ + r * kRegionBytes);
-          const uint64_t kd = sdesc_k_sw128(c.sbase + kSmK + r * kRegionBytes);
+        const uint32_t id = idesc_f16(kUnitRows, tile_width(ug, j) * kPage, true, true);  // bf16 Q, bf16 K codes
+        if (!(ok = c.wait(B_KFULL + (t & 1), (t >> 1) & 1, 21))) break;
+        tc_fence_after();
 #pragma unroll
-          for (int s = 0; s < 4; ++s) mma_ss(d, qd + 2 * s, kd + 2 * s, id, (r | s) != 0 ? 1u : 0u);
-          mma_commit(c.bar(B_KEMPTY + r));  // region slot r free once these four are done
+        for (int r = 0; r < 4; ++r) {
+          // Q region r and K slot (t & 1, r): SW128 K-major, k-step q at +32 q bytes
+          const uint64_t qd = sdesc_k_sw128(c.sbase + kSmQ + r * kRegionBytes);
+          const uint64_t kd = sdesc_k_sw128(c.sbase + kSmK + ((int)(t & 1) * 4 + r) * kKSlotBytes);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) mma_ss_pair(d, qd + 2 * q, kd + 2 * q, id, (r | q) != 0 ? 1u : 0u);
         }
-        if (!ok) break;
-        mma_commit(c.bar(B_SFULL + (t & 1)));
-        if (j == n - 1) mma_commit(c.bar(B_QEMPTY));
-        if (j == imax(0, n - kQSoon)) mbar_arrive(c.bar(B_QSOON));
+        mma_commit_pair(c.bar(B_SFULL + (t & 1)));  // S(t) ready; tile t's K slots free
+        if (j == n - 1) mma_commit_pair(c.bar(B_QEMPTY));
+        if (j == imax(0, n - kQSoon)) {
+          mbar_arrive(c.bar(B_QSOON));
+          mbar_arrive_cluster(qsoon_peer);
+        }
       }
       if (j >= 1) {  // O (+)= P(j-1) V(j-1), chunk by chunk
         const int jj = j - 1;
         const uint32_t t = tc + jj;
-        if (!(ok = mbar_wait(c.bar(B_PFULL + (t & 1)), (t >> 1) & 1, c.wc, 22))) break;
-        if (jj == 0 && k_unit > 0 && !(ok = mbar_wait(c.bar(B_OEMPTY), (k_unit - 1) & 1, c.wc, 24))) break;
+        if (!(ok = c.wait(B_PFULL + (t & 1), (t >> 1) & 1, 22))) break;
+        if (jj == 0 && k_unit > 0 && !(ok = c.wait(B_OEMPTY, (k_unit - 1) & 1, 24))) break;
         const uint32_t a = c.tb + kTmS + (t & 1) * kTileKeys;
         const int nb = tile_width(ug, jj);
-        for (int ch = 0; ch < n_chunks(nb); ++ch) {
-          const uint32_t s = vc & 1;
-          if (!(ok = mbar_wait(c.bar(B_VFULL + s), (vc >> 1) & 1, c.wc, 23))) break;
-          tc_fence_after();
-          const uint64_t vd = sdesc_k_sw128(c.sbase + kSmV + s * kChunkBytes);
-          // k-step ks covers keys [16 ks, 16 ks + 16) of the chunk; P of
-          // chunk ch sits at S columns [64 ch, 64 ch + 32)
-          const int nks = imin(4, nb - 4 * ch);
-          for (int ks = 0; ks < nks; ++ks)
-            mma_ts(c.tb + kTmO, a + 64 * ch + 8 * ks, vd + (uint64_t)(2 * ks), id_pv,
-                   (jj > 0 || ch > 0 || ks > 0) ? 1u : 0u);
-          mma_commit(c.bar(B_VEMPTY + s));  // V slot free; O holds PV up to this chunk
-          ++vc;
+        if (!(ok = c.wait(B_VFULL + (t & 1), (t >> 1) & 1, 23))) break;
+        tc_fence_after();
+        // k-step ks of chunk ch covers keys [64 ch + 16 ks, +16); P of chunk ch
+        // sits at S columns [64 ch, 64 ch + 32).  A full tile's eight MMAs are
+        // issued straight-line: a loop with a data-dependent trip count between
+        // MMAs leaves the tensor pipe idle for most of each instruction.
+        const uint64_t vd0 = sdesc_k_sw128(c.sbase + kSmV + (int)(t & 1) * 2 * kVSlotBytes);
+        const uint64_t vd1 = sdesc_k_sw128(c.sbase + kSmV + ((int)(t & 1) * 2 + 1) * kVSlotBytes);
+        const uint32_t acc0 = jj > 0 ? 1u : 0u;
+        if (nb == kTileBlocks) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ts_pair(c.tb + kTmO, a + 8 * ks, vd0 + (uint64_t)(2 * ks), id_pv, ks > 0 ? 1u : acc0);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) mma_ts_pair(c.tb + kTmO, a + 64 + 8 * ks, vd1 + (uint64_t)(2 * ks), id_pv, 1u);
+        } else {
+          for (int ch = 0; ch < n_chunks(nb); ++ch) {
+            const int nks = imin(4, nb - 4 * ch);
+            for (int ks = 0; ks < nks; ++ks)
+              mma_ts_pair(c.tb + kTmO, a + 64 * ch + 8 * ks, (ch ? vd1 : vd0) + (uint64_t)(2 * ks), id_pv,
+                          (ch > 0 || ks > 0) ? 1u : acc0);
+          }
         }
-        if (!ok) break;
-        if (jj == n - 1) mma_commit(c.bar(B_OFULL));
+        mma_commit_pair(c.bar(B_VEMPTY + (t & 1)));  // tile t's V^T slots free; O holds PV up to tile t
+        if (jj == n - 1) mma_commit_pair(c.bar(B_OFULL));
       }
     }
     if (!ok) break;
     tc += n;
   }
-  // every issued MMA completes before TMEM is freed
-  mma_commit(c.bar(B_DRAIN));
+  // every issued MMA completes before TMEM is freed (the odd CTA waits for
+  // its copy of this arrival too)
+  mma_commit_pair(c.bar(B_DRAIN));
   (void)mbar_wait_drain(c.bar(B_DRAIN), 0, kDrainNs);
 }
 
 // ------------------------------------------------------------------ softmax
 // Two warps per TMEM lane quadrant: warp half h owns key columns [64h, 64h+64)
-// of every 128-key tile for the same 32 rows.  The pair agrees on each row's
+// of every 128-key tile for the same 32 rows.  The two agree on each row's
 // running maximum through shared memory, so both halves use one reference and
-// their P', partial sums and halves of the O rescale add up exactly.
+// their P', partial sums and halves of the O rescale add up exactly.  Each CTA
+// of a pair runs its own softmax over its own 128 rows; only the arrival that
+// releases PV goes to the even CTA, whose MMA issuer multiplies both.
 __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, uint8_t* sm) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qd = warp & 3;              // lane quadrant
@@ -304,23 +418,24 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
   const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
   float* c_rows = reinterpret_cast<float*>(sm + kSmRows);
   float* l_rows = c_rows + 2 * kRows;           // [unit parity][half][row]
-  float* sp_rows = c_rows + 6 * kRows;          // [unit parity][row]
+  float* sp_rows = c_rows + (2 + 2 * kSlices) * kRows;  // [unit parity][row]
   float* xbuf = reinterpret_cast<float*>(sm + kSmXchg);  // [tile parity][half][row] row maxima
   float* pbuf = xbuf + 4 * kRows;                        // [tile parity][half][row] P' maxima (u8 grid)
   const bool u8 = p.p_mode == 1;
-  uint32_t tc = 0, vc = 0;
+  uint32_t tc = 0;
   int k_unit = 0;
   bool ok = true;
-  for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++k_unit) {
+  for (int u = c.pair; u < p.n_units && ok; u += c.n_pairs, ++k_unit) {
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
-    const UnitGeom ug = unit_geom(un.t0, p.TQ, sg, p.S, p.W);
+    const UnitGeom ug = unit_geom(un.t0, 2 * p.TQ, sg, p.S, p.W);
     const int n = ug.n_tiles;
-    const int t_row = un.t0 + r / p.G;
+    const int t_row = un.t0 + (int)c.rank * p.TQ + r / p.G;
     const float ev = (float)pow2_ceil_exp(__uint_as_float(p.vsmax[un.seq * p.HKV + un.g]));
-    // s_q * sm_scale * log2(e), kept positive so that -inf scores stay -inf;
-    // s_q = 1 for the bf16 query, per row on the int8 grid
-    float c_row = p.sm_scale_log2;
+    // the per-row query scale (s_q on the int8 grid, 1 for the bf16 query;
+    // sm_scale * log2(e) is in the K scales), kept positive so that -inf
+    // scores stay -inf
+    float c_row = 1.f;
     if (p.q_mode == 1) {
       // both warps of the pair agree before entering the unit's tiles
       ok = bar_red_and(1 + qd, 64, c.warp_wait(B_QREADY, k_unit & 1, 30));
@@ -452,7 +567,7 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
       // leaving the loop: the error word then fails the next tile's pair
       // barrier for both.
       if (j > 0 && __any_sync(0xffffffffu, corr != 1.f) &&
-          c.warp_wait(B_VEMPTY + ((vc - 1) & 1), ((vc - 1) >> 1) & 1, 33)) {
+          c.warp_wait(B_VEMPTY + ((t - 1) & 1), ((t - 1) >> 1) & 1, 33)) {
         tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
@@ -472,12 +587,11 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(B_PFULL + (t & 1)));
-      vc += n_chunks(tg.nb);
+      if (lane == 0) c.arrive_pair_tmem(B_PFULL + (t & 1));
     }
     if (!ok) break;
     tc += n;
-    l_rows[(k_unit & 1) * 2 * kRows + h * kRows + r] = l_run;
+    l_rows[(k_unit & 1) * kSlices * kRows + h * kRows + r] = l_run;
     if (h == 0) sp_rows[(k_unit & 1) * kRows + r] = sp_prev;
     __syncwarp();
     if (lane == 0) mbar_arrive(c.bar(B_STATS + (k_unit & 1)));
@@ -491,10 +605,11 @@ struct RowInfo {
   size_t off;  // element offset of the row in q / out
 };
 
-__device__ __forceinline__ RowInfo row_info(const AttnParams& p, const Unit& un, const SeqGeom& sg, int r) {
+// Row r of the CTA whose first token is t0, kv head g.
+__device__ __forceinline__ RowInfo row_info(const AttnParams& p, int t0, int g, const SeqGeom& sg, int r) {
   RowInfo ri;
-  const int t_row = un.t0 + r / p.G;
-  const int h_row = un.g * p.G + r % p.G;
+  const int t_row = t0 + r / p.G;
+  const int h_row = g * p.G + r % p.G;
   ri.valid = t_row >= sg.q_start && t_row < sg.q_start + sg.n_q;
   ri.off = ri.valid ? ((size_t)(sg.q_off + t_row - sg.q_start) * p.HQ + h_row) * kHeadDim : 0;
   return ri;
@@ -515,13 +630,13 @@ struct LaneRows {
   uint32_t row[8];  // row index in q / out (element offset row * 256)
   uint32_t valid;   // bit k: row k is a query row of the call
 };
-__device__ __forceinline__ LaneRows lane_rows(const AttnParams& p, const Unit& un, const SeqGeom& sg, int qd,
+__device__ __forceinline__ LaneRows lane_rows(const AttnParams& p, int t0, int g, const SeqGeom& sg, int qd,
                                               int lane) {
   LaneRows lr;
   lr.valid = 0;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const RowInfo ri = row_info(p, un, sg, 32 * qd + 4 * k + (lane >> 3));
+    const RowInfo ri = row_info(p, t0, g, sg, 32 * qd + 4 * k + (lane >> 3));
     lr.row[k] = (uint32_t)(ri.off / kHeadDim);
     lr.valid |= (ri.valid ? 1u : 0u) << k;
   }
@@ -530,7 +645,7 @@ __device__ __forceinline__ LaneRows lane_rows(const AttnParams& p, const Unit& u
 
 // Q on the pages' int8 grid (step a1), in place in shared memory: the row's
 // codes rint(q * 127/absmax) clamped to [-127, 127], held exactly as bf16;
-// returns s_q * sm_scale * log2(e) with s_q = absmax / 127.
+// returns s_q = absmax / 127 (sm_scale * log2(e) is in the K scales).
 __device__ __forceinline__ float q_codes_int8(const AttnParams& p, uint8_t* qs, int r) {
   float absmax = 0.f;
 #pragma unroll 1
@@ -562,7 +677,7 @@ __device__ __forceinline__ float q_codes_int8(const AttnParams& p, uint8_t* qs, 
       }
       *a = make_uint4(w[0], w[1], w[2], w[3]);
     }
-  return __fdiv_rn(absmax, 127.f) * p.sm_scale_log2;
+  return __fdiv_rn(absmax, 127.f);
 }
 
 // Eight bf16 outputs times sigmoid of their eight bf16 gate values, rounded
@@ -592,7 +707,8 @@ __device__ __forceinline__ bool epilogue(const AttnParams& p, const Ctx& c, cons
   if (!c.warp_wait(B_OFULL, k_unit & 1, 41)) return false;
   if (!c.warp_wait(B_STATS + (k_unit & 1), (k_unit >> 1) & 1, 42)) return false;
   tc_fence_after();
-  const float l = l_rows[(k_unit & 1) * 2 * kRows + r] + l_rows[(k_unit & 1) * 2 * kRows + kRows + r];
+  const float* lu = l_rows + (k_unit & 1) * kSlices * kRows;
+  const float l = lu[r] + lu[kRows + r];
   const float sp = sp_rows[(k_unit & 1) * kRows + r];
   const float fin = l > 0.f ? (p.p_mode == 1 ? sp : 1.f) / l : 0.f;
   const int pc = lane & 7;
@@ -606,7 +722,7 @@ __device__ __forceinline__ bool epilogue(const AttnParams& p, const Ctx& c, cons
     if (cb == 3) {
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(B_OEMPTY));
+      if (lane == 0) c.arrive_pair_tmem(B_OEMPTY);
     }
     uint32_t w[32];
 #pragma unroll
@@ -643,19 +759,19 @@ __device__ __forceinline__ bool epilogue(const AttnParams& p, const Ctx& c, cons
 }
 
 __device__ __forceinline__ void role_correction(const AttnParams& p, const Ctx& c, uint8_t* sm) {
-  const int r = threadIdx.x - 384;
+  const int r = threadIdx.x - 32 * (4 + kSoftmaxWarps);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qd = warp & 3;
   const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
   uint8_t* stage = sm + kSmStage + qd * 4096;
   float* c_rows = reinterpret_cast<float*>(sm + kSmRows);
   const float* l_rows = c_rows + 2 * kRows;
-  const float* sp_rows = c_rows + 6 * kRows;
+  const float* sp_rows = c_rows + (2 + 2 * kSlices) * kRows;
   int k_unit = 0;
   bool ok = true;
-  Unit prev_un{};
+  int prev_t0 = 0, prev_g = 0;
   SeqGeom prev_sg{};
-  for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++k_unit) {
+  for (int u = c.pair; u < p.n_units && ok; u += c.n_pairs, ++k_unit) {
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
     if (p.q_mode == 1) {  // the unit's Q codes, in place, before the MMA may read Q
@@ -663,20 +779,24 @@ __device__ __forceinline__ void role_correction(const AttnParams& p, const Ctx& 
       c_rows[(k_unit & 1) * kRows + r] = q_codes_int8(p, sm + kSmQ, r);
       fence_proxy_async_shared();  // generic-proxy writes, read next by the tensor core
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(B_QREADY));
+      if (lane == 0) {
+        mbar_arrive(c.bar(B_QREADY));
+        c.arrive_pair(B_QREADY2);
+      }
     }
     if (k_unit > 0)
-      ok = epilogue(p, c, lane_rows(p, prev_un, prev_sg, qd, lane), k_unit - 1, c.tb + lane_off + kTmO, l_rows,
-                    sp_rows, r, stage, lane);
-    prev_un = un;
+      ok = epilogue(p, c, lane_rows(p, prev_t0, prev_g, prev_sg, qd, lane), k_unit - 1, c.tb + lane_off + kTmO,
+                    l_rows, sp_rows, r, stage, lane);
+    prev_t0 = un.t0 + (int)c.rank * p.TQ;
+    prev_g = un.g;
     prev_sg = sg;
   }
   if (ok && k_unit > 0)
-    (void)epilogue(p, c, lane_rows(p, prev_un, prev_sg, qd, lane), k_unit - 1, c.tb + lane_off + kTmO, l_rows,
-                   sp_rows, r, stage, lane);
+    (void)epilogue(p, c, lane_rows(p, prev_t0, prev_g, prev_sg, qd, lane), k_unit - 1, c.tb + lane_off + kTmO,
+                   l_rows, sp_rows, r, stage, lane);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     attention_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ AttnMaps m) {
   extern __shared__ uint8_t smraw[];
   // 1024-byte aligned base by pointer arithmetic on the shared array, so the
@@ -685,27 +805,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   Ctx c;
   c.sbase = smem_u32(sm);
+  c.rank = cluster_rank();
+  c.pair = (int)(blockIdx.x >> 1);
+  c.n_pairs = (int)(gridDim.x >> 1);
   c.wc = WaitCtl{p.err, p.wait_ns};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kSmTmemSlot);
   if (threadIdx.x == 0) {
-    for (int r = 0; r < 4; ++r) {
-      mbar_init(c.bar(B_KFULL + r), 1);
-      mbar_init(c.bar(B_KEMPTY + r), 1);
-    }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(c.bar(B_VFULL + b), 1);
+      mbar_init(c.bar(B_KFULL + b), 4);  // the even CTA's four region lanes (expect_tx: bytes of both halves)
+      mbar_init(c.bar(B_VFULL + b), 1);  // the even CTA's chunk-0 lane (expect_tx: every chunk of both CTAs)
       mbar_init(c.bar(B_VEMPTY + b), 1);
       mbar_init(c.bar(B_SCFULL + b), 1);
-      mbar_init(c.bar(B_SCEMPTY + b), 8);  // every softmax warp, after reading the scales
+      mbar_init(c.bar(B_SCEMPTY + b), kSoftmaxWarps);  // every softmax warp, after reading the scales
       mbar_init(c.bar(B_SFULL + b), 1);
-      mbar_init(c.bar(B_PFULL + b), 8);
-      mbar_init(c.bar(B_STATS + b), 8);
+      mbar_init(c.bar(B_PFULL + b), 2 * kSoftmaxWarps);
+      mbar_init(c.bar(B_STATS + b), kSoftmaxWarps);
     }
-    mbar_init(c.bar(B_QFULL), 4);  // one arrival per Q region
+    mbar_init(c.bar(B_QFULL), c.rank == 0 ? 5 : 4);  // one arrival per Q region (+ the odd CTA's)
     mbar_init(c.bar(B_QREADY), 4);
+    mbar_init(c.bar(B_QREADY2), 8);
     mbar_init(c.bar(B_QEMPTY), 1);
     mbar_init(c.bar(B_OFULL), 1);
-    mbar_init(c.bar(B_OEMPTY), 4);
+    mbar_init(c.bar(B_OEMPTY), 8);
     mbar_init(c.bar(B_STALL), 1);
     mbar_init(c.bar(B_DRAIN), 1);
     mbar_init(c.bar(B_QSOON), 1);
@@ -715,8 +836,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&m.q);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(tmem_slot), 512);
+    tmem_relinquish_pair();
   }
   // scale slots start at zero: columns past a tile's width then hold finite
   // stale scales, which the softmax multiplies by p = 0
@@ -724,30 +845,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_proxy_async_shared();
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before either may arrive on the other's
   tc_fence_after();
   c.tb = *tmem_slot;
 
   const int lane = threadIdx.x & 31;
-  if (warp == 0) {
-    if (lane < 4) role_producer_k(p, m, c, lane);
-  } else if (warp == 1) {
-    if (lane == 0) role_mma(p, c);
-  } else if (warp == 2) {
-    if (lane < 2) role_producer_v(p, m, c, lane);
-  } else if (warp == 3) {
-    if (lane < 4) role_producer_q(p, m, c, lane);
-  } else if (warp < 12) {
+  if (warp < 4) {
+    if (warp == 0) {
+      if (lane < kKSlots) role_producer_k(p, m, c, lane);
+    } else if (warp == 1) {
+      if (lane == 0 && c.rank == 0) role_mma(p, c);
+    } else if (warp == 2) {
+      if (lane < kVSlots) role_producer_v(p, m, c, lane);
+    } else {
+      if (lane < 5) role_producer_q(p, m, c, lane);
+    }
+  } else if (warp < 4 + kSoftmaxWarps) {
     role_softmax(p, c, sm);
   } else {
     role_correction(p, c, sm);
   }
+  // the odd CTA's TMEM and shared memory are in use until the pair's last MMA is done
+  if (c.rank == 1 && warp == 1 && lane == 0) (void)mbar_wait_drain(c.bar(B_DRAIN), 0, kDrainNs);
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // no arrival from the other CTA is still on its way
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(c.tb, 512);
+    tmem_dealloc_pair(c.tb, 512);
   }
 }
 
@@ -756,8 +883,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_attention(const AttnParams& p, const AttnMaps& m, int n_sm, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
   if (e != cudaSuccess) return e;
-  const int grid = imax(1, imin(p.n_units, n_sm));
-  attention_kernel<<<grid, kThreads, kAttnSmem, st>>>(p, m);
+  // persistent grid: one CTA pair per co-resident cluster slot (or per unit)
+  static int max_pairs = -1;
+  if (max_pairs < 0) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * (unsigned)imax(1, n_sm / 2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kAttnSmem;
+    int mc = 0;
+    if (cudaOccupancyMaxActiveClusters(&mc, attention_kernel, &cfg) != cudaSuccess || mc <= 0) {
+      (void)cudaGetLastError();
+      mc = imax(1, n_sm / 2);
+    }
+    max_pairs = mc;
+  }
+  const int pairs = imax(1, imin(p.n_units, max_pairs));
+  attention_kernel<<<2 * pairs, kThreads, kAttnSmem, st>>>(p, m);
   return cudaGetLastError();
 }
 

@@ -11,11 +11,11 @@
 
 namespace pa {
 
-// One work unit: 128 query rows of one kv head (see pa_tiles.cuh).
+// One work unit: 256 query rows of one kv head (see pa_tiles.cuh).
 struct Unit {
   int seq;      // sequence index
   int g;        // kv head
-  int t0;       // absolute first token of the unit (multiple of TQ)
+  int t0;       // absolute first token of the unit (multiple of UT = 256 / G)
   int n_tiles;  // key tiles it visits (its cost)
 };
 
@@ -40,6 +40,7 @@ struct WidenParams {
   float* vs;                  // [HKV][n_tok_cap]        per-token V scale
   unsigned int* vsmax;        // [n_seq][HKV] float bits: max V scale (atomicMax)
   int* err;
+  float k_mult = 1.f;         // ks = k_scale * k_mult (the attention folds sm_scale * log2(e) in here)
 };
 
 struct AttnParams {
@@ -53,10 +54,10 @@ struct AttnParams {
   const unsigned int* vsmax;
   __nv_bfloat16* out;         // [total_q][HQ][256]
   const __nv_bfloat16* gate;  // [total_q][HQ][256] output gate (sigmoid), or nullptr
-  int HQ, HKV, G, TQ;
+  int HQ, HKV, G, TQ;         // TQ = 128 / G: tokens per CTA, half a unit
   int n_tok_cap;
   int S, W;
-  float sm_scale_log2;        // sm_scale * log2(e)
+  float sm_scale_log2;        // sm_scale * log2(e), already folded into ks
   int q_mode, p_mode;
   int* err;
   unsigned long long wait_ns;
@@ -65,9 +66,9 @@ struct AttnParams {
 };
 
 struct AttnMaps {
-  CUtensorMap k;   // Kw  [HKV][n_tok][256] bf16, box {64, 128, 1}: one 64-dim region of a key tile
-  CUtensorMap v;   // Vt  [HKV][256][n_tok] fp16, box {64, 256, 1}: one 64-key chunk
-  CUtensorMap q;   // q   [tokens][HQ][256] bf16, box {64, G, TQ}: one region of a unit's 128 rows
+  CUtensorMap k;   // Kw  [HKV][n_tok][256] bf16, box {64, 64, 1}: one CTA's keys of a 64-dim region of a key tile
+  CUtensorMap v;   // Vt  [HKV][256][n_tok] fp16, box {64, 128, 1}: one CTA's dims of a 64-key chunk
+  CUtensorMap q;   // q   [tokens][HQ][256] bf16, box {64, G, TQ}: one region of a CTA's 128 rows
 };
 
 // Launchers (return the launch's cudaError_t).
@@ -122,7 +123,7 @@ cudaError_t launch_attention(const AttnParams& p, const AttnMaps& m, int n_sm, c
 // Debug exports (tests only).
 cudaError_t launch_debug_gather(const WidenParams& p, int seq, int8_t* k_out, int8_t* v_out, float* ks_out,
                                 float* vs_out, int32_t* tok_out, cudaStream_t st);
-cudaError_t launch_debug_maskset(const SeqGeom* seqs, const Unit* units, int n_units, int TQ, int G, int S, int W,
+cudaError_t launch_debug_maskset(const SeqGeom* seqs, const Unit* units, int n_units, int UT, int G, int S, int W,
                                  int32_t* row_counts, int32_t* unit_blocks, int cap, cudaStream_t st);
 
 }  // namespace pa

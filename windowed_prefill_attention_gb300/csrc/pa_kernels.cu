@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kWidenThreads) widen_kernel(const WidenParams 
       ksv = p.k_scale[slot];
       vsv = p.v_scale[slot];
     }
-    p.ks[(size_t)g * p.n_tok_cap + row0 + tk] = ksv;
+    p.ks[(size_t)g * p.n_tok_cap + row0 + tk] = ksv * p.k_mult;
     p.vs[(size_t)g * p.n_tok_cap + row0 + tk] = vsv;
     if (vsv > 0.f) atomicMax(p.vsmax + s * HKV + g, __float_as_uint(vsv));
   }
@@ -225,11 +225,11 @@ cudaError_t launch_debug_gather(const WidenParams& p, int seq, int8_t* k_out, in
 
 // Per unit: the key blocks its tiles visit (in visiting order, -1 padded) and,
 // per row, how many keys the kernel's mask lets through.
-__global__ void debug_maskset_kernel(const SeqGeom* seqs, const Unit* units, int TQ, int G, int S, int W,
+__global__ void debug_maskset_kernel(const SeqGeom* seqs, const Unit* units, int UT, int G, int S, int W,
                                      int32_t* row_counts, int32_t* unit_blocks, int cap) {
   const Unit un = units[blockIdx.x];
   const SeqGeom sg = seqs[un.seq];
-  const UnitGeom ug = unit_geom(un.t0, TQ, sg, S, W);
+  const UnitGeom ug = unit_geom(un.t0, UT, sg, S, W);
   const int r = threadIdx.x;
   const int t_row = un.t0 + r / G;
   int count = 0, nblk = 0;
@@ -244,12 +244,12 @@ __global__ void debug_maskset_kernel(const SeqGeom* seqs, const Unit* units, int
   }
   if (r == 0)
     for (int k = nblk; k < cap; ++k) unit_blocks[(size_t)blockIdx.x * cap + k] = -1;
-  row_counts[(size_t)blockIdx.x * kRows + r] = count;
+  row_counts[(size_t)blockIdx.x * kUnitRows + r] = count;
 }
 
-cudaError_t launch_debug_maskset(const SeqGeom* seqs, const Unit* units, int n_units, int TQ, int G, int S, int W,
+cudaError_t launch_debug_maskset(const SeqGeom* seqs, const Unit* units, int n_units, int UT, int G, int S, int W,
                                  int32_t* row_counts, int32_t* unit_blocks, int cap, cudaStream_t st) {
-  debug_maskset_kernel<<<n_units, kRows, 0, st>>>(seqs, units, TQ, G, S, W, row_counts, unit_blocks, cap);
+  debug_maskset_kernel<<<n_units, kUnitRows, 0, st>>>(seqs, units, UT, G, S, W, row_counts, unit_blocks, cap);
   return cudaGetLastError();
 }
 

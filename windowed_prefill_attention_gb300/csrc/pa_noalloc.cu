@@ -58,12 +58,12 @@ void* scratch_address(int device, int* rc) {
 // decreasing first token: for one sequence the later query blocks see the
 // full window, so this is the longest-first order) and clears the words that
 // must start at zero.
-__global__ void noalloc_plan_kernel(SeqGeom sg, int S, int W, int HKV, int TQ, int n_t0, int t_first, SeqGeom* seq_out,
+__global__ void noalloc_plan_kernel(SeqGeom sg, int S, int W, int HKV, int UT, int n_t0, int t_first, SeqGeom* seq_out,
                                     Unit* units, unsigned int* vsmax, int* err) {
   const int n_units = n_t0 * HKV;
   for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < n_units; u += gridDim.x * blockDim.x) {
-    const int t0 = t_first + (n_t0 - 1 - u / HKV) * TQ;
-    units[u] = Unit{0, u % HKV, t0, unit_geom(t0, TQ, sg, S, W).n_tiles};
+    const int t0 = t_first + (n_t0 - 1 - u / HKV) * UT;
+    units[u] = Unit{0, u % HKV, t0, unit_geom(t0, UT, sg, S, W).n_tiles};
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     *seq_out = sg;
@@ -120,7 +120,8 @@ extern "C" int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_page
       !aligned_to(k_scale, 4) || !aligned_to(v_scale, 4) || !aligned_to(block_table, 4))
     return PA_EINVAL;
   if (!(sm_scale == sm_scale) || sm_scale < 0.f) return PA_EINVAL;
-  const int TQ = kRows / G;
+  const int TQ = kRows / G;      // tokens per CTA
+  const int UT = kUnitRows / G;  // tokens per unit (a CTA pair)
 
   SeqGeom sg{};
   sg.q_off = 0;
@@ -131,8 +132,8 @@ extern "C" int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_page
   sg.bt_row = 0;
   seq_geom_fill(sg, n_sink_blk, n_win_blk);
   const long long n_rows = (long long)sg.n_blocks * kPage;
-  const int t_first = (q_start / TQ) * TQ;
-  const int n_t0 = (q_start + n_q - 1 - t_first) / TQ + 1;
+  const int t_first = (q_start / UT) * UT;
+  const int n_t0 = (q_start + n_q - 1 - t_first) / UT + 1;
   // size limits of the static scratch: a clear error, never an overflow
   const long long row_bytes = (long long)n_kv_heads * (2 * kHeadDim * 2LL + 2 * sizeof(float));  // bf16 K + fp16 V^T, two scales
   const long long cap_rows = ((long long)PA_NOALLOC_SCRATCH_BYTES - (long long)kWidenedOffset) / row_bytes / 64 * 64;
@@ -164,17 +165,17 @@ extern "C" int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_page
 
   AttnMaps m;
   if ((rc = encode3(&m.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kw, kHeadDim, n_rows, n_kv_heads, kHeadDim * 2,
-                    (uint64_t)cap * kHeadDim * 2, 64, kTileKeys, 1)))
+                    (uint64_t)cap * kHeadDim * 2, 64, kTileKeys / 2, 1)))
     return rc;
   if ((rc = encode3(&m.v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, vt, n_rows, kHeadDim, n_kv_heads, (uint64_t)cap * 2,
-                    (uint64_t)cap * kHeadDim * 2, kChunkKeys, kHeadDim, 1)))
+                    (uint64_t)cap * kHeadDim * 2, kChunkKeys, kHeadDim / 2, 1)))
     return rc;
   if ((rc = encode3(&m.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, kHeadDim, n_q_heads, n_q, kHeadDim * 2,
                     (uint64_t)n_q_heads * kHeadDim * 2, 64, G, TQ)))
     return rc;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  noalloc_plan_kernel<<<(n_t0 * n_kv_heads + 255) / 256, 256, 0, st>>>(sg, n_sink_blk, n_win_blk, n_kv_heads, TQ, n_t0,
+  noalloc_plan_kernel<<<(n_t0 * n_kv_heads + 255) / 256, 256, 0, st>>>(sg, n_sink_blk, n_win_blk, n_kv_heads, UT, n_t0,
                                                                        t_first, seq_dev, units, vsmax, err);
   if (cudaGetLastError() != cudaSuccess) return PA_ECUDA;
 
@@ -197,6 +198,7 @@ extern "C" int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_page
   wp.vs = vs;
   wp.vsmax = vsmax;
   wp.err = err;
+  wp.k_mult = sm_scale * 1.4426950408889634f;  // the softmax's sm_scale * log2(e), folded into the K scales
   if (launch_widen(wp, st) != cudaSuccess) return PA_ECUDA;
 
   AttnParams a{};

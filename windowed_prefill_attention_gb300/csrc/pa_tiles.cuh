@@ -10,10 +10,13 @@
 // block(t) only, so it is constant over a 16-row query tile and only the
 // causal bound varies per row.
 //
-// A work unit is 128 query rows of one kv head g: TQ = 128 / G consecutive
-// tokens times the G q heads that share g (row r = token_in_unit * G + head_in_group).
-// Units start on absolute multiples of TQ, so for G = 8 a unit is exactly one
-// 16-token query block, the pages' 16-row tile.
+// A work unit is 256 query rows of one kv head g, one 256-row MMA over a pair
+// of CTAs: UT = 256 / G consecutive tokens times the G q heads that share g
+// (row r = token_in_unit * G + head_in_group); each CTA holds 128 rows, the
+// first or second TQ = UT / 2 tokens.  Units start on absolute multiples of UT,
+// so for G = 8 a unit is two 16-token query blocks (the pages' 16-row tiles).
+// Both halves of a unit visit the same key tiles: those of the union of the
+// unit's query blocks; the per-row mask hides what a row may not see.
 //
 // Key tiles: the unit's visible key blocks form at most two runs, the sink run
 // [0, S) and the window run [lo(first block), last block]; when they touch they
@@ -31,7 +34,8 @@ namespace pa {
 
 constexpr int kPage = 16;         // tokens per KV page (= mask block)
 constexpr int kHeadDim = 256;     // head dimension
-constexpr int kRows = 128;        // query rows per work unit (MMA M)
+constexpr int kRows = 128;        // query rows per CTA (TMEM lanes)
+constexpr int kUnitRows = 2 * kRows;  // query rows per work unit (MMA M over a CTA pair)
 constexpr int kTileBlocks = 8;    // 16-key blocks per key tile
 constexpr int kTileKeys = kTileBlocks * kPage;  // 128
 constexpr int kChunkKeys = 64;    // keys per V^T chunk (PV works through a tile in chunks)
