@@ -38,8 +38,8 @@
 //   warp 2        TMA producer of V^T (one lane per slot), as warp 0
 //   warp 3        producer of Q (TMA, one lane per region, after an L2
 //                 prefetch) and of the scales
-//   warps 4-11    softmax: one query row per thread (TMEM lane = row), two
-//                 warps per lane quadrant, each owning 64 of the 128 key columns
+//   warps 4-11    softmax: two warps per TMEM lane quadrant, each owning 16
+//                 whole rows (two rows per thread, 16-lane TMEM shapes)
 //   warps 12-15   epilogue of each unit (and Q codes on the int8 grid)
 #include <cstdint>
 #include <cuda.h>
@@ -53,7 +53,7 @@
 namespace pa {
 namespace {
 
-constexpr int kSlices = 2;                              // softmax warps per TMEM lane quadrant
+constexpr int kSlices = 2;                              // softmax warps per TMEM lane quadrant (16 rows each)
 constexpr int kSoftmaxWarps = 4 * kSlices;             // warps 4 .. 11
 constexpr int kThreads = 32 * (4 + kSoftmaxWarps + 4);  // + producers/MMA (0-3) and epilogue (12-15)
 constexpr int kRegionBytes = kRows * 128;                 // 16 KB: Q, 128 rows x 64 dims (bf16)
@@ -66,9 +66,8 @@ constexpr int kSmQ = 0;                                   // 4 regions of 128 ro
 constexpr int kSmK = kSmQ + 4 * kRegionBytes;             // K slots
 constexpr int kSmV = kSmK + kKSlots * kKSlotBytes;        // V^T slots
 constexpr int kSmScale = kSmV + kVSlots * kVSlotBytes;    // 2 slots: k'[128], vs[128]
-constexpr int kSmRows = kSmScale + 2 * 1024;              // c[2][128], l[2][kSlices][128], sp[2][128] floats
-constexpr int kSmXchg = kSmRows + (4 + 2 * kSlices) * kRows * 4;  // softmax slice exchange: 2 x [2][kSlices][128] floats
-constexpr int kSmStage = kSmXchg + 4 * kSlices * kRows * 4;  // epilogue: 4 x [32 rows][128 B]
+constexpr int kSmRows = kSmScale + 2 * 1024;              // c[2][128], l[2][128], sp[2][128] floats (by unit parity)
+constexpr int kSmStage = kSmRows + 6 * kRows * 4;         // epilogue: 4 x [32 rows][128 B]
 constexpr int kSmBars = kSmStage + 4 * 4096;
 // Barriers.  "Pair" barriers are waited on by the even CTA's MMA issuer and
 // count arrivals from both CTAs (the odd CTA arrives through the cluster);
@@ -404,23 +403,25 @@ __device__ __forceinline__ void role_mma(const AttnParams& p, const Ctx& c) {
 }
 
 // ------------------------------------------------------------------ softmax
-// Two warps per TMEM lane quadrant: warp half h owns key columns [64h, 64h+64)
-// of every 128-key tile for the same 32 rows.  The two agree on each row's
-// running maximum through shared memory, so both halves use one reference and
-// their P', partial sums and halves of the O rescale add up exactly.  Each CTA
-// of a pair runs its own softmax over its own 128 rows; only the arrival that
-// releases PV goes to the even CTA, whose MMA issuer multiplies both.
+// Two warps per TMEM lane quadrant, each owning 16 whole rows of the
+// quadrant's 32 (lanes 32 qd + 16 hh + [0, 16)) across all 128 key columns of
+// a tile, read and written in the 16-lane TMEM shapes: thread t holds rows
+// t/4 and t/4 + 8 of the 16 and, of every 8 key columns, columns 2 (t % 4)
+// and 2 (t % 4) + 1.  Each K/V scale a thread loads so serves two rows (the
+// scale loads, broadcast from shared memory, bound the softmax otherwise), and
+// a row's maximum and sum take two shuffles among the four threads that share
+// it, with no exchange between warps.  Each CTA of a pair runs its own
+// softmax over its own 128 rows; only the arrival that releases PV goes to the
+// even CTA, whose MMA issuer multiplies both.
 __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, uint8_t* sm) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qd = warp & 3;              // lane quadrant
-  const int h = (warp - 4) >> 2;        // column half
-  const int r = qd * 32 + lane;         // query row = TMEM lane
-  const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+  const int lb = 32 * (warp & 3) + 16 * ((warp - 4) >> 2);  // first of this warp's 16 rows (TMEM lanes)
+  const int tcol = 2 * (lane & 3);                          // this thread's first column of every 8
+  const int rr[2] = {lb + (lane >> 2), lb + (lane >> 2) + 8};  // its two rows
+  const uint32_t lane_off = (uint32_t)lb << 16;
   float* c_rows = reinterpret_cast<float*>(sm + kSmRows);
-  float* l_rows = c_rows + 2 * kRows;           // [unit parity][half][row]
-  float* sp_rows = c_rows + (2 + 2 * kSlices) * kRows;  // [unit parity][row]
-  float* xbuf = reinterpret_cast<float*>(sm + kSmXchg);  // [tile parity][half][row] row maxima
-  float* pbuf = xbuf + 4 * kRows;                        // [tile parity][half][row] P' maxima (u8 grid)
+  float* l_rows = c_rows + 2 * kRows;   // [unit parity][row]
+  float* sp_rows = c_rows + 4 * kRows;  // [unit parity][row]
   const bool u8 = p.p_mode == 1;
   uint32_t tc = 0;
   int k_unit = 0;
@@ -430,158 +431,164 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
     const SeqGeom sg = p.seqs[un.seq];
     const UnitGeom ug = unit_geom(un.t0, 2 * p.TQ, sg, p.S, p.W);
     const int n = ug.n_tiles;
-    const int t_row = un.t0 + (int)c.rank * p.TQ + r / p.G;
+    const int t0 = un.t0 + (int)c.rank * p.TQ;  // this CTA's first token
+    const int t_row[2] = {t0 + rr[0] / p.G, t0 + rr[1] / p.G};
     const float ev = (float)pow2_ceil_exp(__uint_as_float(p.vsmax[un.seq * p.HKV + un.g]));
     // the per-row query scale (s_q on the int8 grid, 1 for the bf16 query;
     // sm_scale * log2(e) is in the K scales), kept positive so that -inf
     // scores stay -inf
-    float c_row = 1.f;
+    float c_row[2] = {1.f, 1.f};
     if (p.q_mode == 1) {
-      // both warps of the pair agree before entering the unit's tiles
-      ok = bar_red_and(1 + qd, 64, c.warp_wait(B_QREADY, k_unit & 1, 30));
-      if (!ok) break;
-      c_row = c_rows[(k_unit & 1) * kRows + r];
+      if (!(ok = c.warp_wait(B_QREADY, k_unit & 1, 30))) break;
+      c_row[0] = c_rows[(k_unit & 1) * kRows + rr[0]];
+      c_row[1] = c_rows[(k_unit & 1) * kRows + rr[1]];
     }
-    c_row = fmaxf(c_row, 1e-30f);
-    float m_run = -INFINITY, l_run = 0.f, sp_prev = 1.f;
+    c_row[0] = fmaxf(c_row[0], 1e-30f);
+    c_row[1] = fmaxf(c_row[1], 1e-30f);
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f}, sp_prev[2] = {1.f, 1.f};
     for (int j = 0; j < n; ++j) {
       const uint32_t t = tc + j;
       const TileGeom tg = tile_geom(ug, j, p.S, p.W);
-      // Every path through a tile passes the pair barrier the same number of
-      // times, so a wait that runs out in one warp cannot strand its partner.
-      bool okl = c.warp_wait(B_SFULL + (t & 1), (t >> 1) & 1, 31);
-      const uint32_t sd = c.tb + lane_off + kTmS + (t & 1) * kTileKeys + 64 * h;
-      // this half's K scales (64 floats); its V scales follow 512 bytes later
-      const float4* ks4 = reinterpret_cast<const float4*>(sm + kSmScale + (t & 1) * 1024 + 256 * h);
-      const float4* vs4 = ks4 + 32;
-      float y[64];
-      float my = -INFINITY;
-      if (okl) {
-        tc_fence_after();
-        uint32_t sa[32], sb[32];
-        tmem_ld32(sd, sa);
-        tmem_ld32(sd + 32, sb);
-        // the tile's scales (normally there long since), checked while the
-        // score loads are in flight
-        okl = c.warp_wait(B_SCFULL + (t & 1), (t >> 1) & 1, 32);
-        tmem_wait_ld(sa);
-        reg_fence(sb);
-        // y = S * k_scale (masked: -inf), and this half's row maximum; the
-        // products in fp32 pairs, the maximum three operands at a time
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        const bool full = !tg.needs_mask && tg.nb == kTileBlocks;  // every row sees every key
-        const unsigned long long vis = full ? ~0ull : visible_columns(tg, t_row, p.S, p.W, h);
+      if (!(ok = c.warp_wait(B_SFULL + (t & 1), (t >> 1) & 1, 31))) break;
+      const uint32_t sd = c.tb + lane_off + kTmS + (t & 1) * kTileKeys;
+      // this thread's K scales at +8k (two floats each); its V scales 128 floats on
+      const float* ksp = reinterpret_cast<const float*>(sm + kSmScale + (t & 1) * 1024) + tcol;
+      const float* vsp = ksp + 128;
+      tc_fence_after();
+      uint32_t sv[64];
+      tmem_ld_16x256b_x16(sd, sv);
+      // the tile's scales (normally there long since), checked while the
+      // score load is in flight
+      const bool oks = c.warp_wait(B_SCFULL + (t & 1), (t >> 1) & 1, 32);
+      tmem_wait_ld(sv);
+      if (!(ok = oks)) break;
+      // y = S * k_scale (masked: -inf), in place, and each row's maximum; the
+      // products in fp32 pairs, the maximum three operands at a time
+      const bool full = !tg.needs_mask && tg.nb == kTileBlocks;  // every row sees every key
+      unsigned long long vis[2][2] = {{~0ull, ~0ull}, {~0ull, ~0ull}};  // [row][key half] >> tcol
+      if (!full) {
 #pragma unroll
-        for (int q4 = 0; q4 < 16; ++q4) {
-          const float4 k4 = ks4[q4];
-          const int q = 4 * q4;
-          const uint32_t* src = q < 32 ? sa + q : sb + (q - 32);
-          float2 y01 = mul2(make_float2(__uint_as_float(src[0]), __uint_as_float(src[1])), make_float2(k4.x, k4.y));
-          float2 y23 = mul2(make_float2(__uint_as_float(src[2]), __uint_as_float(src[3])), make_float2(k4.z, k4.w));
-          if (!full) {
-            y01.x = ((vis >> q) & 1ull) ? y01.x : -INFINITY;
-            y01.y = ((vis >> (q + 1)) & 1ull) ? y01.y : -INFINITY;
-            y23.x = ((vis >> (q + 2)) & 1ull) ? y23.x : -INFINITY;
-            y23.y = ((vis >> (q + 3)) & 1ull) ? y23.y : -INFINITY;
-          }
-          y[q] = y01.x;
-          y[q + 1] = y01.y;
-          y[q + 2] = y23.x;
-          y[q + 3] = y23.y;
-          m4[2 * (q4 & 1)] = max3(m4[2 * (q4 & 1)], y01.x, y01.y);
-          m4[2 * (q4 & 1) + 1] = max3(m4[2 * (q4 & 1) + 1], y23.x, y23.y);
-        }
-        my = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c_row;  // log2 units
-      } else {
+        for (int i = 0; i < 2; ++i)
 #pragma unroll
-        for (int q = 0; q < 64; ++q) y[q] = -INFINITY;
+          for (int hf = 0; hf < 2; ++hf) vis[i][hf] = visible_columns(tg, t_row[i], p.S, p.W, hf) >> tcol;
       }
-      // the reference moves only when some row's max grew by more than 2^kLazy
-      const bool grow = okl && (m_run == -INFINITY || my > m_run + kLazy);
-      float alpha = 1.f;
-      if (bar_red_popc(1 + qd, 64, grow || !okl) != 0) {
-        float* xb = xbuf + (t & 1) * 2 * kRows;
-        xb[h * kRows + r] = my;
-        if (!bar_red_and(1 + qd, 64, okl)) {
-          ok = false;
-          break;
-        }
-        const float mx = fmaxf(xb[r], xb[kRows + r]);
-        if (m_run == -INFINITY) {
-          m_run = mx == -INFINITY ? mx : mx + kLift;  // alpha irrelevant: nothing accumulated yet
-          alpha = 0.f;
-        } else if (mx > m_run + kLazy) {
-          alpha = ex2_approx(m_run - mx);
-          m_run = mx;
-        }
-      }
-      const float mref = m_run == -INFINITY ? 0.f : m_run + ev;
-      // p = 2^(y c - mref); P' = p * v_scale (V scale folded into P).  Column
-      // q adds into partial sum q mod 4; (s01, s23) hold the four partials.
-      float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
-      const float2 c2 = make_float2(c_row, c_row), nm2 = make_float2(-mref, -mref);
+      float mx[2][2] = {{-INFINITY, -INFINITY}, {-INFINITY, -INFINITY}};
 #pragma unroll
-      for (int q4 = 0; q4 < 16; ++q4) {
-        const float4 v4 = vs4[q4];
-        const int q = 4 * q4;
-        const float2 a01 = fma2(make_float2(y[q], y[q + 1]), c2, nm2);
-        const float2 a23 = fma2(make_float2(y[q + 2], y[q + 3]), c2, nm2);
-        const float2 p01 = make_float2(ex2_approx(a01.x), ex2_approx(a01.y));
-        const float2 p23 = make_float2(ex2_approx(a23.x), ex2_approx(a23.y));
-        s01 = add2(s01, p01);
-        s23 = add2(s23, p23);
-        const float2 w01 = mul2(p01, make_float2(v4.x, v4.y));
-        const float2 w23 = mul2(p23, make_float2(v4.z, v4.w));
-        y[q] = w01.x;
-        y[q + 1] = w01.y;
-        y[q + 2] = w23.x;
-        y[q + 3] = w23.y;
+      for (int k = 0; k < 16; ++k) {
+        const float2 k2 = *reinterpret_cast<const float2*>(ksp + 8 * k);
+        float2 a = mul2(make_float2(__uint_as_float(sv[4 * k]), __uint_as_float(sv[4 * k + 1])), k2);
+        float2 b = mul2(make_float2(__uint_as_float(sv[4 * k + 2]), __uint_as_float(sv[4 * k + 3])), k2);
+        if (!full) {
+          const int hf = k >> 3, sh = 8 * (k & 7);
+          a.x = ((vis[0][hf] >> sh) & 1ull) ? a.x : -INFINITY;
+          a.y = ((vis[0][hf] >> (sh + 1)) & 1ull) ? a.y : -INFINITY;
+          b.x = ((vis[1][hf] >> sh) & 1ull) ? b.x : -INFINITY;
+          b.y = ((vis[1][hf] >> (sh + 1)) & 1ull) ? b.y : -INFINITY;
+        }
+        sv[4 * k] = __float_as_uint(a.x);
+        sv[4 * k + 1] = __float_as_uint(a.y);
+        sv[4 * k + 2] = __float_as_uint(b.x);
+        sv[4 * k + 3] = __float_as_uint(b.y);
+        mx[0][k & 1] = max3(mx[0][k & 1], a.x, a.y);
+        mx[1][k & 1] = max3(mx[1][k & 1], b.x, b.y);
       }
-      const float s4[4] = {s01.x, s01.y, s23.x, s23.y};
+      // the reference of a row moves only when its max grew by more than 2^kLazy
+      float alpha[2] = {1.f, 1.f}, mref[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        float m = fmaxf(mx[i][0], mx[i][1]);
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        const float my = m * c_row[i];  // log2 units
+        if (m_run[i] == -INFINITY) {
+          m_run[i] = my == -INFINITY ? my : my + kLift;  // alpha irrelevant: nothing accumulated yet
+          alpha[i] = 0.f;
+        } else if (my > m_run[i] + kLazy) {
+          alpha[i] = ex2_approx(m_run[i] - my);
+          m_run[i] = my;
+        }
+        mref[i] = m_run[i] == -INFINITY ? 0.f : m_run[i] + ev;
+      }
+      // p = 2^(y c - mref); P' = p * v_scale (V scale folded into P)
+      float2 s2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      const float2 c2[2] = {make_float2(c_row[0], c_row[0]), make_float2(c_row[1], c_row[1])};
+      const float2 nm2[2] = {make_float2(-mref[0], -mref[0]), make_float2(-mref[1], -mref[1])};
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float2 v2 = *reinterpret_cast<const float2*>(vsp + 8 * k);
+        const float2 a = fma2(make_float2(__uint_as_float(sv[4 * k]), __uint_as_float(sv[4 * k + 1])), c2[0], nm2[0]);
+        const float2 b = fma2(make_float2(__uint_as_float(sv[4 * k + 2]), __uint_as_float(sv[4 * k + 3])), c2[1], nm2[1]);
+        const float2 pa = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+        const float2 pb = make_float2(ex2_approx(b.x), ex2_approx(b.y));
+        s2[0] = add2(s2[0], pa);
+        s2[1] = add2(s2[1], pb);
+        const float2 wa = mul2(pa, v2), wb = mul2(pb, v2);
+        sv[4 * k] = __float_as_uint(wa.x);
+        sv[4 * k + 1] = __float_as_uint(wa.y);
+        sv[4 * k + 2] = __float_as_uint(wb.x);
+        sv[4 * k + 3] = __float_as_uint(wb.y);
+      }
       // this warp is done with the tile's scales
       __syncwarp();
-      if (okl && lane == 0) mbar_arrive(c.bar(B_SCEMPTY + (t & 1)));
-      l_run = l_run * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
-      float corr = alpha;
+      if (lane == 0) mbar_arrive(c.bar(B_SCEMPTY + (t & 1)));
+      float corr[2] = {alpha[0], alpha[1]};
+#pragma unroll
+      for (int i = 0; i < 2; ++i) l_run[i] = l_run[i] * alpha[i] + (s2[i].x + s2[i].y);
       if (u8) {  // P' per row on the u8 grid over the whole tile, scale max/255
-        float pm = 0.f;
 #pragma unroll
-        for (int q = 0; q < 64; ++q) pm = fmaxf(pm, y[q]);
-        float* pb = pbuf + (t & 1) * 2 * kRows;
-        pb[h * kRows + r] = pm;
-        bar_red_and(1 + qd, 64, true);
-        const float pmax = fmaxf(pb[r], pb[kRows + r]);
-        const float sp = pmax > 0.f ? __fdiv_rn(pmax, 255.f) : sp_prev;
-        const float inv = pmax > 0.f ? __fdiv_rn(255.f, pmax) : 0.f;
+        for (int i = 0; i < 2; ++i) {
+          float pm = 0.f;
 #pragma unroll
-        for (int q = 0; q < 64; ++q) y[q] = rintf(y[q] * inv);
-        corr = alpha * __fdiv_rn(sp_prev, sp);
-        sp_prev = sp;
+          for (int k = 0; k < 16; ++k) pm = max3(pm, __uint_as_float(sv[4 * k + 2 * i]), __uint_as_float(sv[4 * k + 2 * i + 1]));
+          pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
+          pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
+          const float sp = pm > 0.f ? __fdiv_rn(pm, 255.f) : sp_prev[i];
+          const float inv = pm > 0.f ? __fdiv_rn(255.f, pm) : 0.f;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            sv[4 * k + 2 * i] = __float_as_uint(rintf(__uint_as_float(sv[4 * k + 2 * i]) * inv));
+            sv[4 * k + 2 * i + 1] = __float_as_uint(rintf(__uint_as_float(sv[4 * k + 2 * i + 1]) * inv));
+          }
+          corr[i] = alpha[i] * __fdiv_rn(sp_prev[i], sp);
+          sp_prev[i] = sp;
+        }
       }
-      uint32_t pk[32];
+      // P' as fp16 pairs over S columns [0, 32) (keys 0-63) and [64, 96) (keys
+      // 64-127), where the PV issuer reads them
+      uint32_t pk0[16], pk1[16];
 #pragma unroll
-      for (int q = 0; q < 32; ++q) pk[q] = pack_half2(y[2 * q], y[2 * q + 1]);
-      tmem_st32(sd, pk);
-      // O holds PV up to tile j-1 once that MMA's last chunk is done; rescale
-      // this half in place.  A wait that runs out skips the rescale without
-      // leaving the loop: the error word then fails the next tile's pair
-      // barrier for both.
-      if (j > 0 && __any_sync(0xffffffffu, corr != 1.f) &&
+      for (int k = 0; k < 8; ++k) {
+        pk0[2 * k] = pack_half2(__uint_as_float(sv[4 * k]), __uint_as_float(sv[4 * k + 1]));
+        pk0[2 * k + 1] = pack_half2(__uint_as_float(sv[4 * k + 2]), __uint_as_float(sv[4 * k + 3]));
+        pk1[2 * k] = pack_half2(__uint_as_float(sv[32 + 4 * k]), __uint_as_float(sv[32 + 4 * k + 1]));
+        pk1[2 * k + 1] = pack_half2(__uint_as_float(sv[32 + 4 * k + 2]), __uint_as_float(sv[32 + 4 * k + 3]));
+      }
+      tmem_st_16x128b_x8(sd, pk0);
+      tmem_st_16x128b_x8(sd + 64, pk1);
+      // O holds PV up to tile j-1 once that MMA is done; rescale this warp's
+      // rows in place.  A wait that runs out skips the rescale (the error word
+      // is set; the results of the call are void).
+      if (j > 0 && __any_sync(0xffffffffu, corr[0] != 1.f || corr[1] != 1.f) &&
           c.warp_wait(B_VEMPTY + ((t - 1) & 1), ((t - 1) >> 1) & 1, 33)) {
         tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t o[32];
-          const uint32_t oa = c.tb + lane_off + kTmO + 128 * h + cc * 32;
-          tmem_ld32(oa, o);
+          const uint32_t oa = c.tb + lane_off + kTmO + 64 * cc;
+          tmem_ld_16x256b_x8(oa, o);
           tmem_wait_ld(o);
 #pragma unroll
-          for (int q = 0; q < 32; q += 2) {
-            const float2 v = mul2(make_float2(__uint_as_float(o[q]), __uint_as_float(o[q + 1])), make_float2(corr, corr));
-            o[q] = __float_as_uint(v.x);
-            o[q + 1] = __float_as_uint(v.y);
+          for (int k = 0; k < 8; ++k) {
+            const float2 x = mul2(make_float2(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1])),
+                                  make_float2(corr[0], corr[0]));
+            const float2 y = mul2(make_float2(__uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3])),
+                                  make_float2(corr[1], corr[1]));
+            o[4 * k] = __float_as_uint(x.x);
+            o[4 * k + 1] = __float_as_uint(x.y);
+            o[4 * k + 2] = __float_as_uint(y.x);
+            o[4 * k + 3] = __float_as_uint(y.y);
           }
-          tmem_st32(oa, o);
+          tmem_st_16x256b_x8(oa, o);
         }
       }
       tmem_wait_st();
@@ -591,8 +598,17 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
     }
     if (!ok) break;
     tc += n;
-    l_rows[(k_unit & 1) * kSlices * kRows + h * kRows + r] = l_run;
-    if (h == 0) sp_rows[(k_unit & 1) * kRows + r] = sp_prev;
+    // each row's sum over the four threads that share it
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      float l = l_run[i];
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      if ((lane & 3) == 0) {
+        l_rows[(k_unit & 1) * kRows + rr[i]] = l;
+        sp_rows[(k_unit & 1) * kRows + rr[i]] = sp_prev[i];
+      }
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(c.bar(B_STATS + (k_unit & 1)));
   }
@@ -707,8 +723,7 @@ __device__ __forceinline__ bool epilogue(const AttnParams& p, const Ctx& c, cons
   if (!c.warp_wait(B_OFULL, k_unit & 1, 41)) return false;
   if (!c.warp_wait(B_STATS + (k_unit & 1), (k_unit >> 1) & 1, 42)) return false;
   tc_fence_after();
-  const float* lu = l_rows + (k_unit & 1) * kSlices * kRows;
-  const float l = lu[r] + lu[kRows + r];
+  const float l = l_rows[(k_unit & 1) * kRows + r];
   const float sp = sp_rows[(k_unit & 1) * kRows + r];
   const float fin = l > 0.f ? (p.p_mode == 1 ? sp : 1.f) / l : 0.f;
   const int pc = lane & 7;
@@ -766,7 +781,7 @@ __device__ __forceinline__ void role_correction(const AttnParams& p, const Ctx& 
   uint8_t* stage = sm + kSmStage + qd * 4096;
   float* c_rows = reinterpret_cast<float*>(sm + kSmRows);
   const float* l_rows = c_rows + 2 * kRows;
-  const float* sp_rows = c_rows + (2 + 2 * kSlices) * kRows;
+  const float* sp_rows = c_rows + 4 * kRows;
   int k_unit = 0;
   bool ok = true;
   int prev_t0 = 0, prev_g = 0;

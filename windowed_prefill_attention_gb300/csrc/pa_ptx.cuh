@@ -448,12 +448,44 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       PA_W8(0), PA_W8(8)
       : "memory");
 }
+// 16-lane shapes.  A warp addresses 16 TMEM lanes from the lane in taddr;
+// thread t holds lanes base + t/4 and base + t/4 + 8.  16x256b: per
+// repetition k (8 columns), registers 4k..4k+3 are (lane t/4, column
+// 8k + 2(t%4)), (lane t/4, that + 1), (lane t/4 + 8, column 8k + 2(t%4)),
+// (lane t/4 + 8, that + 1).  16x128b: per repetition k (4 columns), registers
+// 2k, 2k+1 are column 4k + t%4 of lanes t/4 and t/4 + 8.
+__device__ __forceinline__ void tmem_ld_16x256b_x16(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+               : PA_R8(0), PA_R8(8), PA_R8(16), PA_R8(24), PA_R8(32), PA_R8(40), PA_R8(48), PA_R8(56)
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+               : PA_R8(0), PA_R8(8), PA_R8(16), PA_R8(24)
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st_16x256b_x8(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+               PA_W8(0), PA_W8(8), PA_W8(16), PA_W8(24)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_16x128b_x8(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile("tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+               PA_W8(0), PA_W8(8)
+               : "memory");
+}
 #define PA_RW8(i) "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]), \
                   "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])
 // Wait for this thread's tcgen05.ld's.  The registers of `r` are named as
 // in/out operands so the compiler cannot move their uses above the wait.
 __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" : PA_RW8(0), PA_RW8(8), PA_RW8(16), PA_RW8(24)
+               :
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[64]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : PA_RW8(0), PA_RW8(8), PA_RW8(16), PA_RW8(24), PA_RW8(32), PA_RW8(40), PA_RW8(48), PA_RW8(56)
                :
                : "memory");
 }
