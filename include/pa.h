@@ -123,8 +123,13 @@ int pa_prefill_batch_gated(pa_handle h, int n_seq, const pa_seq* seqs, const voi
                            void* stream);
 
 /* pa_prefill_batch on HOST buffers: copies the inputs to handle-owned device
- * memory on `stream`, runs, copies out back and synchronises the stream; the
- * return value includes device-side errors.  Pinned host memory is fastest. */
+ * memory, runs, copies out back and synchronises `stream`; the return value
+ * includes device-side errors.  The copies overlap the computation: the query
+ * rows are split into chunks (whole 256-token blocks of work), and while one
+ * chunk is computed on `stream` the next one's q rows are copied in and the
+ * previous one's output rows copied out on two copy streams the handle owns.
+ * Output rows that belong to no sequence are left as they were.  Pinned host
+ * memory is fastest (pageable memory makes the copies synchronous). */
 int pa_prefill_host(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* k_pool,
                     const int8_t* v_pool, const float* k_scale, const float* v_scale, const int32_t* block_table,
                     int n_sink_blk, int n_win_blk, float sm_scale, void* out, void* stream);

@@ -138,6 +138,16 @@ struct pa_ctx {
   // host-buffer path staging
   void* hb[7] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
   size_t hb_cap[7] = {0, 0, 0, 0, 0, 0, 0};
+  cudaStream_t s_h2d = nullptr, s_d2h = nullptr;  // the host path's copy streams
+  std::vector<cudaEvent_t> pipe_ev;                // and its events (no timing)
+  SeqGeom* d_pseqs = nullptr;                      // its chunks' plans, uploaded together
+  int pseqs_cap = 0;
+  Unit* d_punits = nullptr;
+  int punits_cap = 0;
+  void* h_pstage = nullptr;
+  size_t h_pstage_cap = 0;
+  cudaEvent_t pstage_done = nullptr;
+  bool pstage_recorded = false;
 
   // timing
   std::vector<cudaEvent_t> ev_free;
@@ -202,6 +212,31 @@ int encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, c
 }
 
 // Plan (cached by its inputs), workspace sizing and the upload of the plan.
+// Widened-row workspace for at least `rows` rows (reallocating frees the old
+// buffers, which waits for the device).
+int reserve_rows(pa_handle h, size_t rows) {
+  const size_t need_tok = (rows + 63) / 64 * 64;
+  if ((size_t)h->n_tok_cap >= need_tok) return PA_OK;
+  size_t cap = std::max(need_tok, (size_t)h->n_tok_cap + (size_t)h->n_tok_cap / 2);
+  cap = (cap + 63) / 64 * 64;
+  if (h->kw) cudaFree(h->kw);
+  if (h->vt) cudaFree(h->vt);
+  if (h->ks) cudaFree(h->ks);
+  if (h->vs) cudaFree(h->vs);
+  h->kw = nullptr;
+  h->vt = nullptr;
+  h->ks = nullptr;
+  h->vs = nullptr;
+  h->n_tok_cap = 0;
+  h->kv_ptr = nullptr;
+  PA_CUDA(cudaMalloc(&h->kw, cap * h->HKV * kHeadDim * sizeof(__nv_bfloat16)));
+  PA_CUDA(cudaMalloc(&h->vt, cap * h->HKV * kHeadDim * sizeof(__half)));
+  PA_CUDA(cudaMalloc(&h->ks, cap * h->HKV * sizeof(float)));
+  PA_CUDA(cudaMalloc(&h->vs, cap * h->HKV * sizeof(float)));
+  h->n_tok_cap = (int)cap;
+  return PA_OK;
+}
+
 int prepare(pa_handle h, int n_seq, const pa_seq* seqs, int S, int W, cudaStream_t st) {
   std::vector<int> key;
   key.reserve(4 + 4 * n_seq);
@@ -219,26 +254,7 @@ int prepare(pa_handle h, int n_seq, const pa_seq* seqs, int S, int W, cudaStream
   int rc = build_plan(h->HQ, h->HKV, n_seq, seqs, S, W, h->max_pages, P);
   if (rc) return rc;
   // workspace
-  const size_t need_tok = ((size_t)P.n_tok_total + 63) / 64 * 64;
-  if ((size_t)h->n_tok_cap < need_tok) {
-    size_t cap = std::max(need_tok, (size_t)h->n_tok_cap + (size_t)h->n_tok_cap / 2);
-    cap = (cap + 63) / 64 * 64;
-    if (h->kw) cudaFree(h->kw);
-    if (h->vt) cudaFree(h->vt);
-    if (h->ks) cudaFree(h->ks);
-    if (h->vs) cudaFree(h->vs);
-    h->kw = nullptr;
-    h->vt = nullptr;
-    h->ks = nullptr;
-    h->vs = nullptr;
-    h->n_tok_cap = 0;
-    h->kv_ptr = nullptr;
-    PA_CUDA(cudaMalloc(&h->kw, cap * h->HKV * kHeadDim * sizeof(__nv_bfloat16)));
-    PA_CUDA(cudaMalloc(&h->vt, cap * h->HKV * kHeadDim * sizeof(__half)));
-    PA_CUDA(cudaMalloc(&h->ks, cap * h->HKV * sizeof(float)));
-    PA_CUDA(cudaMalloc(&h->vs, cap * h->HKV * sizeof(float)));
-    h->n_tok_cap = (int)cap;
-  }
+  if ((rc = reserve_rows(h, (size_t)P.n_tok_total))) return rc;
   if ((rc = grow(h->vsmax, h->vsmax_cap, (size_t)n_seq * h->HKV))) return rc;
   if ((rc = grow(h->d_seqs, h->seqs_cap, P.seqs.size()))) return rc;
   if ((rc = grow(h->d_units, h->units_cap, P.units.size()))) return rc;
@@ -273,7 +289,7 @@ int check_inputs(pa_handle h, const void* q, const int8_t* kp, const int8_t* vp,
 }
 
 WidenParams widen_params(pa_handle h, const int8_t* kp, const int8_t* vp, const float* ksc, const float* vsc,
-                         const int32_t* bt, int n_seq) {
+                         const int32_t* bt, int n_seq, const SeqGeom* d_seqs = nullptr, int n_stored_blocks = -1) {
   WidenParams w{};
   w.k_pool = kp;
   w.v_pool = vp;
@@ -283,9 +299,9 @@ WidenParams widen_params(pa_handle h, const int8_t* kp, const int8_t* vp, const 
   w.bt_stride = h->max_pages;
   w.n_pool = h->n_pool;
   w.HKV = h->HKV;
-  w.seqs = h->d_seqs;
+  w.seqs = d_seqs ? d_seqs : h->d_seqs;
   w.n_seq = n_seq;
-  w.n_stored_blocks = h->plan.n_stored_blocks;
+  w.n_stored_blocks = n_stored_blocks >= 0 ? n_stored_blocks : h->plan.n_stored_blocks;
   w.n_tok_cap = h->n_tok_cap;
   w.kw = h->kw;
   w.vt = h->vt;
@@ -307,15 +323,13 @@ cudaEvent_t take_event(pa_handle h) {
   return e;
 }
 
-int run(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* kp, const int8_t* vp,
-        const float* ksc, const float* vsc, const int32_t* bt, int S, int W, float sm_scale, void* out,
-        cudaStream_t st, const void* gate = nullptr) {
-  int rc = check_inputs(h, q, kp, vp, ksc, vsc, bt, out);
-  if (rc) return rc;
-  if (gate && !aligned(gate, 16)) return PA_EINVAL;
-  if (!(sm_scale == sm_scale) || sm_scale < 0.f) return PA_EINVAL;
-  if ((rc = prepare(h, n_seq, seqs, S, W, st))) return rc;
-  const Plan& P = h->plan;
+// The widening pass and the attention kernel of plan P, whose sequence table
+// and unit list are already on the device at d_seqs / d_units (the caller
+// has sized the widened workspace for P).
+int launch_plan(pa_handle h, const Plan& P, const SeqGeom* d_seqs, const Unit* d_units, int n_seq, const void* q,
+                const int8_t* kp, const int8_t* vp, const float* ksc, const float* vsc, const int32_t* bt, int S,
+                int W, float sm_scale, void* out, cudaStream_t st, const void* gate) {
+  int rc = PA_OK;
   // tensor maps
   if (h->kw != h->kv_ptr || P.n_tok_total != h->kv_rows || h->n_tok_cap != h->kv_cap) {
     const uint64_t kd[3] = {(uint64_t)kHeadDim, (uint64_t)P.n_tok_total, (uint64_t)h->HKV};
@@ -352,15 +366,15 @@ int run(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t*
     PA_CUDA(cudaEventRecord(e0, st));
   }
   PA_CUDA(cudaMemsetAsync(h->vsmax, 0, sizeof(unsigned int) * n_seq * h->HKV, st));
-  WidenParams wp = widen_params(h, kp, vp, ksc, vsc, bt, n_seq);
+  WidenParams wp = widen_params(h, kp, vp, ksc, vsc, bt, n_seq, d_seqs, P.n_stored_blocks);
   wp.k_mult = sm_scale * 1.4426950408889634f;  // the softmax's sm_scale * log2(e), folded into the K scales
   PA_CUDA(launch_widen(wp, st));
   if (e1) PA_CUDA(cudaEventRecord(e1, st));
   AttnParams a{};
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.total_q = P.total_q;
-  a.seqs = h->d_seqs;
-  a.units = h->d_units;
+  a.seqs = d_seqs;
+  a.units = d_units;
   a.n_units = (int)P.units.size();
   a.ks = h->ks;
   a.vs = h->vs;
@@ -389,6 +403,18 @@ int run(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t*
     h->ev_pending.push_back(e2);
   }
   return PA_OK;
+}
+
+int run(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* kp, const int8_t* vp,
+        const float* ksc, const float* vsc, const int32_t* bt, int S, int W, float sm_scale, void* out,
+        cudaStream_t st, const void* gate = nullptr) {
+  int rc = check_inputs(h, q, kp, vp, ksc, vsc, bt, out);
+  if (rc) return rc;
+  if (gate && !aligned(gate, 16)) return PA_EINVAL;
+  if (!(sm_scale == sm_scale) || sm_scale < 0.f) return PA_EINVAL;
+  if ((rc = prepare(h, n_seq, seqs, S, W, st))) return rc;
+  return launch_plan(h, h->plan, h->d_seqs, h->d_units, n_seq, q, kp, vp, ksc, vsc, bt, S, W, sm_scale, out, st,
+                     gate);
 }
 
 }  // namespace
@@ -474,6 +500,13 @@ void pa_destroy(pa_handle h) {
   if (h->dec_done) cudaEventDestroy(h->dec_done);
   for (cudaEvent_t e : h->ev_free) cudaEventDestroy(e);
   for (cudaEvent_t e : h->ev_pending) cudaEventDestroy(e);
+  for (cudaEvent_t e : h->pipe_ev) cudaEventDestroy(e);
+  if (h->d_pseqs) cudaFree(h->d_pseqs);
+  if (h->d_punits) cudaFree(h->d_punits);
+  if (h->h_pstage) cudaFreeHost(h->h_pstage);
+  if (h->pstage_done) cudaEventDestroy(h->pstage_done);
+  if (h->s_h2d) cudaStreamDestroy(h->s_h2d);
+  if (h->s_d2h) cudaStreamDestroy(h->s_d2h);
   delete h;
 }
 
@@ -501,36 +534,181 @@ int pa_prefill_batch_gated(pa_handle h, int n_seq, const pa_seq* seqs, const voi
              static_cast<cudaStream_t>(stream), q_gate);
 }
 
+// A piece of a sequence's query rows, computed as one call of its own.
+struct Piece {
+  int seq;     // sequence index (its block-table row)
+  pa_seq s;    // the piece as a sequence: its rows, same context
+};
+
+// The host-buffer path is a pipeline over chunks of the query rows: the pool,
+// scales and block table go in first, then each chunk's q rows on one copy
+// stream, while the previous chunk is computed on the caller's stream and
+// the chunk before that is copied out on another copy stream.  A chunk is a
+// contiguous run of the sequences' rows laid end to end, so it holds at most
+// one piece of each sequence, sequences in order, and its block-table rows
+// are consecutive; a piece boundary inside a sequence falls on a multiple of
+// 256 tokens (a whole number of work units for every GQA ratio), so no unit
+// is split between chunks.
 int pa_prefill_host(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* k_pool,
                     const int8_t* v_pool, const float* k_scale, const float* v_scale, const int32_t* block_table,
                     int n_sink_blk, int n_win_blk, float sm_scale, void* out, void* stream) {
   if (!h || n_seq <= 0 || !seqs) return PA_EINVAL;
-  int total_q = 0;
-  for (int s = 0; s < n_seq; ++s) total_q = std::max(total_q, seqs[s].q_off + seqs[s].n_q);
+  // the whole call's plan validates it and sizes the widened workspace once
+  Plan whole;
+  int rc = build_plan(h->HQ, h->HKV, n_seq, seqs, n_sink_blk, n_win_blk, h->max_pages, whole);
+  if (rc) return rc;
+  const int total_q = whole.total_q;
+  const size_t row_bytes = (size_t)h->HQ * kHeadDim * 2;  // one token's q (or out) row
   const size_t bytes[7] = {
-      (size_t)total_q * h->HQ * kHeadDim * 2,                  // q
+      (size_t)total_q * row_bytes,                           // q
       (size_t)h->n_pool * kPage * h->HKV * kHeadDim,          // k_pool
       (size_t)h->n_pool * kPage * h->HKV * kHeadDim,          // v_pool
       (size_t)h->n_pool * kPage * h->HKV * sizeof(float),     // k_scale
       (size_t)h->n_pool * kPage * h->HKV * sizeof(float),     // v_scale
       (size_t)n_seq * h->max_pages * sizeof(int32_t),         // block table
-      (size_t)total_q * h->HQ * kHeadDim * 2};                // out
+      (size_t)total_q * row_bytes};                           // out
   const void* src[6] = {q, k_pool, v_pool, k_scale, v_scale, block_table};
   for (int i = 0; i < 6; ++i)
     if (!src[i]) return PA_EINVAL;
   if (!out) return PA_EINVAL;
+  if (!(sm_scale == sm_scale) || sm_scale < 0.f) return PA_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  for (int i = 0; i < 7; ++i) {
-    int rc = grow_bytes(h->hb[i], h->hb_cap[i], bytes[i]);
-    if (rc) return rc;
+  for (int i = 0; i < 7; ++i)
+    if ((rc = grow_bytes(h->hb[i], h->hb_cap[i], bytes[i]))) return rc;
+
+  // chunk boundaries on the sequences' rows laid end to end: a short first
+  // chunk (its copy-in is the pipeline's start-up) and a short last one (its
+  // copy-out is the drain), the rest in chunks of at most 12288 tokens; a
+  // boundary inside a sequence moves to a multiple of 256 tokens
+  std::vector<long long> base(n_seq + 1, 0);  // first row of each sequence, end to end
+  for (int s = 0; s < n_seq; ++s) base[s + 1] = base[s] + seqs[s].n_q;
+  const long long T = base[n_seq];
+  std::vector<long long> cuts;  // chunk ends, end to end
+  if (T <= 4096) {
+    cuts.push_back(T);
+  } else {
+    const long long edge = 2048, mid = T - 2 * edge;
+    const long long k = std::max(1LL, (mid + 12287) / 12288);
+    for (long long i = 0; i <= k; ++i) cuts.push_back(edge + mid * i / k);
+    cuts.push_back(T);
   }
-  for (int i = 0; i < 6; ++i) PA_CUDA(cudaMemcpyAsync(h->hb[i], src[i], bytes[i], cudaMemcpyHostToDevice, st));
-  int rc = run(h, n_seq, seqs, h->hb[0], static_cast<const int8_t*>(h->hb[1]), static_cast<const int8_t*>(h->hb[2]),
-               static_cast<const float*>(h->hb[3]), static_cast<const float*>(h->hb[4]),
-               static_cast<const int32_t*>(h->hb[5]), n_sink_blk, n_win_blk, sm_scale, h->hb[6], st);
-  if (rc) return rc;
-  PA_CUDA(cudaMemcpyAsync(out, h->hb[6], bytes[6], cudaMemcpyDeviceToHost, st));
-  return pa_last_error(h, stream);
+  for (long long& cut : cuts) {  // inside a sequence: down (or up) to a multiple of 256 tokens
+    const int s = (int)(std::upper_bound(base.begin(), base.end(), cut) - base.begin()) - 1;
+    if (s < 0 || s >= n_seq || cut == base[s]) continue;
+    const long long abs_pos = seqs[s].q_start + (cut - base[s]);
+    long long r = abs_pos / 256 * 256;
+    if (r <= seqs[s].q_start) r = std::min((long long)seqs[s].q_start + seqs[s].n_q, (abs_pos / 256 + 1) * 256);
+    cut = base[s] + (r - seqs[s].q_start);
+  }
+  std::vector<std::vector<Piece>> chunks;
+  long long lo = 0;
+  for (const long long hi : cuts) {
+    if (hi <= lo) continue;
+    chunks.emplace_back();
+    for (int s = 0; s < n_seq; ++s) {
+      const long long a = std::max(lo, base[s]), b = std::min(hi, base[s + 1]);
+      if (a >= b) continue;
+      const int qa = seqs[s].q_start + (int)(a - base[s]);
+      chunks.back().push_back(Piece{s, pa_seq{seqs[s].q_off + (qa - seqs[s].q_start), qa, (int)(b - a), seqs[s].n_ctx}});
+    }
+    lo = hi;
+  }
+  const int n_ch = (int)chunks.size();
+
+  // every chunk's plan, uploaded in one go ahead of the large copies (a small
+  // copy queued behind them on the copy engine would hold up the first chunk)
+  std::vector<Plan> plans(n_ch);
+  std::vector<size_t> off_s(n_ch), off_u(n_ch);
+  std::vector<std::vector<pa_seq>> cseqs(n_ch);
+  size_t n_s = 0, n_u = 0, max_rows = 0, max_seq = 0;
+  for (int c = 0; c < n_ch; ++c) {
+    for (const Piece& pc : chunks[c]) cseqs[c].push_back(pc.s);
+    if ((rc = build_plan(h->HQ, h->HKV, (int)cseqs[c].size(), cseqs[c].data(), n_sink_blk, n_win_blk, h->max_pages,
+                         plans[c])))
+      return rc;
+    off_s[c] = n_s;
+    off_u[c] = n_u;
+    n_s += plans[c].seqs.size();
+    n_u += plans[c].units.size();
+    max_rows = std::max(max_rows, (size_t)plans[c].n_tok_total);
+    max_seq = std::max(max_seq, cseqs[c].size());
+  }
+  if ((rc = reserve_rows(h, max_rows))) return rc;
+  if ((rc = grow(h->vsmax, h->vsmax_cap, max_seq * h->HKV))) return rc;
+  if ((rc = grow(h->d_pseqs, h->pseqs_cap, n_s))) return rc;
+  if ((rc = grow(h->d_punits, h->punits_cap, n_u))) return rc;
+  if (!h->pstage_done) PA_CUDA(cudaEventCreateWithFlags(&h->pstage_done, cudaEventDisableTiming));
+  if (h->pstage_recorded) PA_CUDA(cudaEventSynchronize(h->pstage_done));  // staging free again
+  const size_t bytes_s = n_s * sizeof(SeqGeom), bytes_u = n_u * sizeof(Unit);
+  if (h->h_pstage_cap < bytes_s + bytes_u) {
+    if (h->h_pstage) cudaFreeHost(h->h_pstage);
+    h->h_pstage = nullptr;
+    h->h_pstage_cap = 0;
+    PA_CUDA(cudaMallocHost(&h->h_pstage, bytes_s + bytes_u));
+    h->h_pstage_cap = bytes_s + bytes_u;
+  }
+  for (int c = 0; c < n_ch; ++c) {
+    std::memcpy(static_cast<SeqGeom*>(h->h_pstage) + off_s[c], plans[c].seqs.data(),
+                plans[c].seqs.size() * sizeof(SeqGeom));
+    std::memcpy(reinterpret_cast<Unit*>(static_cast<char*>(h->h_pstage) + bytes_s) + off_u[c], plans[c].units.data(),
+                plans[c].units.size() * sizeof(Unit));
+  }
+  PA_CUDA(cudaMemcpyAsync(h->d_pseqs, h->h_pstage, bytes_s, cudaMemcpyHostToDevice, st));
+  PA_CUDA(cudaMemcpyAsync(h->d_punits, static_cast<char*>(h->h_pstage) + bytes_s, bytes_u, cudaMemcpyHostToDevice, st));
+  PA_CUDA(cudaEventRecord(h->pstage_done, st));
+  h->pstage_recorded = true;
+
+  // streams and events
+  if (!h->s_h2d) PA_CUDA(cudaStreamCreateWithFlags(&h->s_h2d, cudaStreamNonBlocking));
+  if (!h->s_d2h) PA_CUDA(cudaStreamCreateWithFlags(&h->s_d2h, cudaStreamNonBlocking));
+  const size_t n_ev = 2 + 2 * (size_t)n_ch;
+  while (h->pipe_ev.size() < n_ev) {
+    cudaEvent_t e;
+    PA_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    h->pipe_ev.push_back(e);
+  }
+  cudaEvent_t ev_start = h->pipe_ev[0], ev_end = h->pipe_ev[1];
+  cudaEvent_t* ev_in = h->pipe_ev.data() + 2;           // chunk c's q rows are in
+  cudaEvent_t* ev_done = h->pipe_ev.data() + 2 + n_ch;  // chunk c is computed
+
+  // inputs: after whatever the caller's stream did before
+  PA_CUDA(cudaEventRecord(ev_start, st));
+  PA_CUDA(cudaStreamWaitEvent(h->s_h2d, ev_start, 0));
+  for (int i = 1; i < 6; ++i) PA_CUDA(cudaMemcpyAsync(h->hb[i], src[i], bytes[i], cudaMemcpyHostToDevice, h->s_h2d));
+  for (int c = 0; c < n_ch; ++c) {
+    for (const Piece& pc : chunks[c]) {
+      const size_t off = (size_t)pc.s.q_off * row_bytes;
+      PA_CUDA(cudaMemcpyAsync(static_cast<char*>(h->hb[0]) + off, static_cast<const char*>(q) + off,
+                              (size_t)pc.s.n_q * row_bytes, cudaMemcpyHostToDevice, h->s_h2d));
+    }
+    PA_CUDA(cudaEventRecord(ev_in[c], h->s_h2d));
+  }
+  // compute each chunk once its rows are in; copy its output out behind it
+  PA_CUDA(cudaStreamWaitEvent(h->s_d2h, ev_start, 0));
+  for (int c = 0; c < n_ch; ++c) {
+    const int s0 = chunks[c].front().seq;
+    PA_CUDA(cudaStreamWaitEvent(st, ev_in[c], 0));
+    rc = launch_plan(h, plans[c], h->d_pseqs + off_s[c], h->d_punits + off_u[c], (int)cseqs[c].size(), h->hb[0],
+                     static_cast<const int8_t*>(h->hb[1]), static_cast<const int8_t*>(h->hb[2]),
+                     static_cast<const float*>(h->hb[3]), static_cast<const float*>(h->hb[4]),
+                     static_cast<const int32_t*>(h->hb[5]) + (size_t)s0 * h->max_pages, n_sink_blk, n_win_blk,
+                     sm_scale, h->hb[6], st, nullptr);
+    if (rc) break;
+    PA_CUDA(cudaEventRecord(ev_done[c], st));
+    PA_CUDA(cudaStreamWaitEvent(h->s_d2h, ev_done[c], 0));
+    for (const Piece& pc : chunks[c]) {
+      const size_t off = (size_t)pc.s.q_off * row_bytes;
+      PA_CUDA(cudaMemcpyAsync(static_cast<char*>(out) + off, static_cast<const char*>(h->hb[6]) + off,
+                              (size_t)pc.s.n_q * row_bytes, cudaMemcpyDeviceToHost, h->s_d2h));
+    }
+  }
+  // the caller's stream waits for both copy streams
+  PA_CUDA(cudaEventRecord(ev_end, h->s_d2h));
+  PA_CUDA(cudaStreamWaitEvent(st, ev_end, 0));
+  PA_CUDA(cudaEventRecord(ev_start, h->s_h2d));
+  PA_CUDA(cudaStreamWaitEvent(st, ev_start, 0));
+  const int le = pa_last_error(h, stream);
+  return rc ? rc : le;
 }
 
 int pa_last_error(pa_handle h, void* stream) {
