@@ -108,7 +108,17 @@ cudaError_t launch_widen(const WidenParams& p, cudaStream_t st) {
 // values per lane per row, all rows' loads in flight before any reduction.
 constexpr int kAppendWarps = 8;
 
-__device__ __forceinline__ uint2 quantise_row8(const uint4 raw, float& scale_out) {
+// |x| of a lane's eight bf16 values, as the bit pattern of their largest
+// magnitude (non-negative bf16 patterns order like their values).
+__device__ __forceinline__ uint32_t absmax_bits8(const uint4 raw) {
+  const uint32_t m = __vmaxu2(__vmaxu2(raw.x & 0x7fff7fffu, raw.y & 0x7fff7fffu),
+                              __vmaxu2(raw.z & 0x7fff7fffu, raw.w & 0x7fff7fffu));
+  return max(m & 0xffffu, m >> 16);
+}
+
+// Quantise a lane's eight bf16 values of a row whose absolute maximum over
+// the warp is `am`: codes rint(x / scale) half to even, scale = absmax / 127.
+__device__ __forceinline__ uint2 quantise_row8(const uint4 raw, float am, float& scale_out) {
   const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
   float x[8];
 #pragma unroll
@@ -116,27 +126,31 @@ __device__ __forceinline__ uint2 quantise_row8(const uint4 raw, float& scale_out
     x[2 * e] = __uint_as_float(w[e] << 16);
     x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
   }
-  float am = 0.f;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(x[e]));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
   const float scale = __fdiv_rn(am, 127.f);
-  // code = rint(x / scale) on the IEEE-rounded quotient.  x * (1/scale) is
-  // within 2.3e-5 of that quotient (|quotient| <= 127.5; two roundings of
-  // 2^-24 relative each), so away from the half-integers (farther than 1e-4)
-  // both round the same way; near them the division itself decides.
-  const float rcp = scale > 0.f ? __frcp_rn(scale) : 0.f;
-  uint32_t packed[2] = {0u, 0u};
+  // code = rint(x / scale) on the IEEE-rounded quotient.  x * rcp, with rcp
+  // the hardware reciprocal (within 1 ulp), is within 3.1e-5 of that quotient
+  // (|quotient| <= 127.5), so where it is farther than 1e-4 from a
+  // half-integer both round the same way; near one the division itself
+  // decides.  |code| <= 127 without a clamp: |x| <= absmax and scale =
+  // RN(absmax / 127), so |x / scale| <= 127 (1 + 2^-23).
+  float rcp = 0.f;
+  if (scale > 0.f) asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rcp) : "f"(scale));
+  int c[8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    float qv = x[e] * rcp;
-    if (fabsf(qv - floorf(qv) - 0.5f) < 1e-4f && scale > 0.f) qv = __fdiv_rn(x[e], scale);
-    const int code = scale > 0.f ? (int)fminf(127.f, fmaxf(-127.f, rintf(qv))) : 0;
-    packed[e >> 2] |= ((uint32_t)code & 0xffu) << (8 * (e & 3));
+  for (int e = 0; e < 4; ++e) {
+    const float2 q = mul2(make_float2(x[2 * e], x[2 * e + 1]), make_float2(rcp, rcp));
+    float r0 = rintf(q.x), r1 = rintf(q.y);
+    const float2 d = add2(q, make_float2(-r0, -r1));
+    if (fabsf(d.x) > 0.4999f) r0 = rintf(__fdiv_rn(x[2 * e], scale));
+    if (fabsf(d.y) > 0.4999f) r1 = rintf(__fdiv_rn(x[2 * e + 1], scale));
+    c[2 * e] = (int)r0;
+    c[2 * e + 1] = (int)r1;
   }
+  // low bytes of the codes, four to a word
+  const uint32_t lo = __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
+  const uint32_t hi = __byte_perm(__byte_perm(c[4], c[5], 0x0040), __byte_perm(c[6], c[7], 0x0040), 0x5410);
   scale_out = scale;
-  return make_uint2(packed[0], packed[1]);
+  return make_uint2(lo, hi);
 }
 
 template <int HKV>
@@ -161,9 +175,14 @@ __global__ void __launch_bounds__(kAppendWarps * 32) kv_append_kernel(const KvAp
   const size_t slot0 = ((size_t)phys * kPage + tok % kPage) * HKV;
 #pragma unroll
   for (int g = 0; g < HKV; ++g) {
+      // the K and V rows' absolute maxima reduced over the warp together, as
+      // the two 16-bit halves of one word (each is a bf16 magnitude)
+      uint32_t m2 = absmax_bits8(rk[g]) | (absmax_bits8(rv[g]) << 16);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m2 = __vmaxu2(m2, __shfl_xor_sync(0xffffffffu, m2, o));
       float sk, sv;
-      const uint2 ck = quantise_row8(rk[g], sk);
-      const uint2 cv = quantise_row8(rv[g], sv);
+      const uint2 ck = quantise_row8(rk[g], __uint_as_float(m2 << 16), sk);
+      const uint2 cv = quantise_row8(rv[g], __uint_as_float(m2 & 0xffff0000u), sv);
       reinterpret_cast<uint2*>(p.k_pool + (slot0 + g) * kHeadDim)[lane] = ck;
       reinterpret_cast<uint2*>(p.v_pool + (slot0 + g) * kHeadDim)[lane] = cv;
       if (lane == 0) {
