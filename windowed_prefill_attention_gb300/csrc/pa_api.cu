@@ -833,8 +833,25 @@ int pa_decode(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const i
     d.lo = n_win_blk > 0 ? std::max(0, last + 1 - n_win_blk) : 0;
     d.n_sink = n_win_blk > 0 ? std::min(std::max(n_sink_blk, 0), d.lo) : 0;
     d.n_vis = d.n_sink + (last - d.lo + 1);
-    d.n_splits = (d.n_vis + kDecSplitBlocks - 1) / kDecSplitBlocks;
-    d.per_split = kDecSplitBlocks;
+  }
+  // blocks per split (one CTA): the size whose grid best fills whole waves of
+  // the SMs, each CTA costing its blocks plus a fixed ~8 blocks' worth
+  // (query load, combining its warps, writing its partial)
+  const long long slots = (long long)h->n_sm * decode_ctas_per_sm();
+  int per_split = kDecMaxSplitBlocks;
+  long long best = -1;
+  for (int ps = 16; ps <= kDecMaxSplitBlocks; ++ps) {
+    long long ctas = 0;
+    for (const DecSeq& d : tab) ctas += (long long)h->HKV * ((d.n_vis + ps - 1) / ps);
+    const long long cost = (ctas + slots - 1) / slots * (ps + 8);
+    if (best < 0 || cost < best) {
+      best = cost;
+      per_split = ps;
+    }
+  }
+  for (DecSeq& d : tab) {
+    d.per_split = per_split;
+    d.n_splits = (d.n_vis + per_split - 1) / per_split;
     max_splits = std::max(max_splits, d.n_splits);
   }
   if ((rc = grow(h->d_dec, h->dec_cap, (size_t)n_seq))) return rc;

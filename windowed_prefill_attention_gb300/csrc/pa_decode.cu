@@ -354,6 +354,20 @@ __global__ void __launch_bounds__(kHeadDim) decode_combine_kernel(const DecodePa
 
 }  // namespace
 
+int decode_ctas_per_sm() {
+  static int n = 0;
+  if (n <= 0) {
+    if (cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel, kDecWarps * 32, kDecSmem) != cudaSuccess)
+      n = 0;
+    if (n <= 0) {
+      (void)cudaGetLastError();
+      n = 1;
+    }
+  }
+  return n;
+}
+
 cudaError_t launch_decode(const DecodeParams& p, int n_seq, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
   if (e != cudaSuccess) return e;

@@ -89,7 +89,7 @@ struct KvAppendParams {
 cudaError_t launch_kv_append(const KvAppendParams& p, cudaStream_t st);
 
 // Decode: one query token per sequence, split over its visible blocks.
-constexpr int kDecSplitBlocks = 64;  // 16-token blocks per split (one CTA)
+constexpr int kDecMaxSplitBlocks = 128;  // 16-token blocks per split (one CTA) at most: 32 per warp
 constexpr int kDecPartStride = 260;  // floats per partial: row max (log2), row sum, 2 pad, O[256]
 struct DecSeq {
   int q_row;     // row of the query token in q / out
@@ -98,7 +98,7 @@ struct DecSeq {
   int n_sink;    // sink blocks listed ahead of the window run
   int lo;        // first block of the window run (0 with the window off)
   int n_vis;     // visible blocks
-  int n_splits;  // ceil(n_vis / kDecSplitBlocks)
+  int n_splits;  // ceil(n_vis / per_split)
   int per_split; // blocks per split (the last split may have fewer)
 };
 struct DecodeParams {
@@ -118,6 +118,8 @@ struct DecodeParams {
   int* err;
 };
 cudaError_t launch_decode(const DecodeParams& p, int n_seq, cudaStream_t st);
+// Split-kernel CTAs that fit on one SM at a time (occupancy, cached).
+int decode_ctas_per_sm();
 cudaError_t launch_attention(const AttnParams& p, const AttnMaps& m, int n_sm, cudaStream_t st);
 
 // Debug exports (tests only).
