@@ -98,10 +98,10 @@ def kernel_source_hash():
     return h.hexdigest()
 
 
-def profiled_traffic(config_name):
-    """DRAM bytes per attention launch from the committed ncu summary, if it was
-    taken on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", "attention_kernel_%s.md" % config_name)
+def profiled_traffic(config_name, kernel="attention_kernel"):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel, config_name))
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -413,7 +413,7 @@ def run_kv_append(args, wl):
         "gpu_launches": args.steps, "clocks": clocks,
         "roofline": {"bound": "hbm", "kernel": "kv_append_kernel", "achieved": gbs, "peak": peak, "unit": "GB/s",
                      "frac": gbs / peak, "peak_source": "measured copy bandwidth (MEASURED_PEAKS.json)",
-                     "traffic": None, "bytes_per_launch": nbytes}}), flush=True)
+                     "traffic": profiled_traffic(wl.name, "kv_append_kernel"), "bytes_per_launch": nbytes}}), flush=True)
 
 
 def run_decode(args, wl):
@@ -481,8 +481,8 @@ def run_decode(args, wl):
         "tokens_per_s": n_seq / (ms / 1e3), "gpu_launches": 2 * args.steps, "clocks": clocks,
         "roofline": {"bound": "hbm", "kernel": "decode_split_kernel + decode_combine_kernel", "achieved": gbs,
                      "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                     "peak_source": "measured copy bandwidth (MEASURED_PEAKS.json)", "traffic": None,
-                     "bytes_per_step": nbytes}}), flush=True)
+                     "peak_source": "measured copy bandwidth (MEASURED_PEAKS.json)",
+                     "traffic": profiled_traffic(wl.name, "decode_split_kernel"), "bytes_per_step": nbytes}}), flush=True)
 
 
 def _row_count_decode(ctx, S, W):
