@@ -578,7 +578,8 @@ int pa_prefill_host(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, c
 
   // chunk boundaries on the sequences' rows laid end to end: a short first
   // chunk (its copy-in is the pipeline's start-up) and a short last one (its
-  // copy-out is the drain), the rest in chunks of at most 12288 tokens; a
+  // copy-out is the drain), the rest in chunks of at most 6144 tokens (the
+  // best of 3072..12288 measured at 32k); a
   // boundary inside a sequence moves to a multiple of 256 tokens
   std::vector<long long> base(n_seq + 1, 0);  // first row of each sequence, end to end
   for (int s = 0; s < n_seq; ++s) base[s + 1] = base[s] + seqs[s].n_q;
@@ -588,7 +589,7 @@ int pa_prefill_host(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, c
     cuts.push_back(T);
   } else {
     const long long edge = 2048, mid = T - 2 * edge;
-    const long long k = std::max(1LL, (mid + 12287) / 12288);
+    const long long k = std::max(1LL, (mid + 6143) / 6144);
     for (long long i = 0; i <= k; ++i) cuts.push_back(edge + mid * i / k);
     cuts.push_back(T);
   }
