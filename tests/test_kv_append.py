@@ -65,6 +65,49 @@ def test_kv_append_is_bit_exact(seq, tok_start, n_new):
                               ref.view(np.uint8) if ref.dtype == np.int8 else ref.view(np.uint32))
 
 
+def _tie_rows(n_new, hkv, seed):
+    """Rows whose quotients x / scale sit on or next to half-integers, where
+    the kernel's reciprocal shortcut hands over to the division: the golden
+    row (scale 2, odd integers: exact ties), exact ties at the power-of-two
+    scales 1/2 and 4, and bf16 rows at non-power-of-two scales whose
+    quotients crowd around k + 0.5."""
+    import json
+    import os
+    gold = json.load(open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "kv_codes.json")))
+    rng = np.random.default_rng(seed)
+    rows = np.zeros((n_new, hkv, 256), dtype=np.float32)
+    for i in range(n_new):
+        for g in range(hkv):
+            kind = (i * hkv + g) % 4
+            if kind == 0:
+                r = np.asarray(gold["values"], dtype=np.float32)
+            elif kind in (1, 2):
+                sc = 0.5 if kind == 1 else 4.0
+                k = rng.integers(-126, 126, size=256)
+                r = ((k + 0.5) * sc).astype(np.float32)  # exact ties
+                r[0] = 127.0 * sc                           # the row's absmax: scale = sc exactly
+            else:
+                am = np.float32(rng.uniform(1.0, 100.0))
+                sc = np.float32(am / np.float32(127.0))
+                k = rng.integers(-126, 126, size=256)
+                r = ((k + 0.5 + rng.uniform(-3e-4, 3e-4, size=256)) * sc).astype(np.float32)
+                r[0] = am
+            rows[i, g] = r
+    return _bf16_bits(rows)
+
+
+def test_kv_append_half_way_codes_are_bit_exact():
+    inp = make_inputs(CONFIGS["chunked_ragged"])
+    hkv = inp.wl.n_kv_heads
+    kn, vn = _tie_rows(64, hkv, 7), _tie_rows(64, hkv, 8)
+    (kp, vp, ks, vs), rc = _append_gpu(inp, 0, 1024, kn, vn)
+    assert rc == 0
+    want = oracle.kv_append(inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale, inp.block_table[0], 1024, kn, vn)
+    for got, ref in zip((kp, vp, ks, vs), want):
+        assert np.array_equal(got.view(np.uint8) if got.dtype == np.int8 else got.view(np.uint32),
+                              ref.view(np.uint8) if ref.dtype == np.int8 else ref.view(np.uint32))
+
+
 def test_append_then_prefill_matches_oracle():
     """A fresh chunk appended on the GPU, then prefilled over the pool it wrote:
     against the fp64 definition on the oracle's own appended pool."""
