@@ -124,10 +124,12 @@ int pa_prefill_batch_gated(pa_handle h, int n_seq, const pa_seq* seqs, const voi
 
 /* pa_prefill_batch on HOST buffers: copies the inputs to handle-owned device
  * memory, runs, copies out back and synchronises `stream`; the return value
- * includes device-side errors.  The copies overlap the computation: the query
- * rows are split into chunks (whole 256-token blocks of work), and while one
- * chunk is computed on `stream` the next one's q rows are copied in and the
- * previous one's output rows copied out on two copy streams the handle owns.
+ * includes device-side errors.  The copies overlap the computation: the pool
+ * goes in first and is widened once, the query rows are split into chunks
+ * (whole work units of 256 / G tokens), and while one chunk is computed on
+ * `stream` the next one's q rows are copied in and the previous one's output
+ * rows copied out on two copy streams the handle owns.  The result is the one
+ * pa_prefill_batch gives on device copies of the same buffers.
  * Output rows that belong to no sequence are left as they were.  Pinned host
  * memory is fastest (pageable memory makes the copies synchronous). */
 int pa_prefill_host(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* k_pool,
@@ -140,7 +142,9 @@ int pa_last_error(pa_handle h, void* stream);
 
 /* Launch times recorded since the last reset (needs record_timing): sums of
  * the widening pass and the attention kernel in milliseconds, and the number
- * of calls.  Waits for the recorded events. */
+ * of calls.  A pa_prefill_host call counts once; its attention time runs from
+ * the end of its widening pass to the end of its last chunk, waits for the
+ * chunks' rows included.  Waits for the recorded events. */
 int pa_timing(pa_handle h, int reset, double* widen_ms, double* attention_ms, int* n_calls);
 
 const char* pa_strerror(int code);

@@ -36,6 +36,23 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+typedef CUresult (*WriteValue32Fn)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+
+// cuStreamWriteValue32: a 32-bit store that a stream performs in order with
+// its copies (after a memory barrier), without a kernel
+WriteValue32Fn write_value_fn() {
+  static WriteValue32Fn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<WriteValue32Fn>(p);
+  });
+  return fn;
+}
+
 struct Plan {
   std::vector<SeqGeom> seqs;
   std::vector<Unit> units;
@@ -109,7 +126,9 @@ struct pa_ctx {
   Unit* d_units = nullptr;
   int units_cap = 0;
   int* d_err = nullptr;
-  int* d_counter = nullptr;
+  unsigned int* d_qflags = nullptr;  // host path: chunk c's q rows are in when d_qflags[c] == q_epoch
+  int qflags_cap = 0;
+  unsigned int q_epoch = 0;
 
   // plan upload through pinned staging
   void* h_stage = nullptr;
@@ -323,12 +342,25 @@ cudaEvent_t take_event(pa_handle h) {
   return e;
 }
 
-// The widening pass and the attention kernel of plan P, whose sequence table
-// and unit list are already on the device at d_seqs / d_units (the caller
-// has sized the widened workspace for P).
-int launch_plan(pa_handle h, const Plan& P, const SeqGeom* d_seqs, const Unit* d_units, int n_seq, const void* q,
-                const int8_t* kp, const int8_t* vp, const float* ksc, const float* vsc, const int32_t* bt, int S,
-                int W, float sm_scale, void* out, cudaStream_t st, const void* gate) {
+// The widening pass of plan P, whose sequence table is already on the device
+// at d_seqs (the caller has sized the widened workspace for P).
+int launch_widen_plan(pa_handle h, const Plan& P, const SeqGeom* d_seqs, int n_seq, const int8_t* kp,
+                      const int8_t* vp, const float* ksc, const float* vsc, const int32_t* bt, float sm_scale,
+                      cudaStream_t st) {
+  PA_CUDA(cudaMemsetAsync(h->vsmax, 0, sizeof(unsigned int) * n_seq * h->HKV, st));
+  WidenParams wp = widen_params(h, kp, vp, ksc, vsc, bt, n_seq, d_seqs, P.n_stored_blocks);
+  wp.k_mult = sm_scale * 1.4426950408889634f;  // the softmax's sm_scale * log2(e), folded into the K scales
+  PA_CUDA(launch_widen(wp, st));
+  return PA_OK;
+}
+
+// The attention kernel over n_units work units at d_units, all of plan P
+// (whose sequence table is on the device at d_seqs and whose pages the
+// widening pass has already written).
+int launch_attention_plan(pa_handle h, const Plan& P, const SeqGeom* d_seqs, const Unit* d_units, int n_units,
+                          const void* q, int S, int W, float sm_scale, void* out, cudaStream_t st,
+                          const void* gate, bool overlap_prev = false, const unsigned int* q_ready = nullptr,
+                          unsigned int q_epoch = 0) {
   int rc = PA_OK;
   // tensor maps
   if (h->kw != h->kv_ptr || P.n_tok_total != h->kv_rows || h->n_tok_cap != h->kv_cap) {
@@ -357,25 +389,12 @@ int launch_plan(pa_handle h, const Plan& P, const SeqGeom* d_seqs, const Unit* d
     if ((rc = encode(&maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, qd, qst, qbox, CU_TENSOR_MAP_SWIZZLE_128B)))
       return rc;
   }
-  cudaEvent_t e0 = nullptr, e1 = nullptr, e2 = nullptr;
-  if (h->opt.record_timing) {
-    e0 = take_event(h);
-    e1 = take_event(h);
-    e2 = take_event(h);
-    if (!e0 || !e1 || !e2) return PA_ECUDA;
-    PA_CUDA(cudaEventRecord(e0, st));
-  }
-  PA_CUDA(cudaMemsetAsync(h->vsmax, 0, sizeof(unsigned int) * n_seq * h->HKV, st));
-  WidenParams wp = widen_params(h, kp, vp, ksc, vsc, bt, n_seq, d_seqs, P.n_stored_blocks);
-  wp.k_mult = sm_scale * 1.4426950408889634f;  // the softmax's sm_scale * log2(e), folded into the K scales
-  PA_CUDA(launch_widen(wp, st));
-  if (e1) PA_CUDA(cudaEventRecord(e1, st));
   AttnParams a{};
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.total_q = P.total_q;
   a.seqs = d_seqs;
   a.units = d_units;
-  a.n_units = (int)P.units.size();
+  a.n_units = n_units;
   a.ks = h->ks;
   a.vs = h->vs;
   a.vsmax = h->vsmax;
@@ -393,16 +412,46 @@ int launch_plan(pa_handle h, const Plan& P, const SeqGeom* d_seqs, const Unit* d
   a.p_mode = h->opt.p_mode;
   a.err = h->d_err;
   a.wait_ns = (unsigned long long)h->opt.wait_timeout_ms * 1000000ull;
-  a.unit_counter = h->d_counter;
+  a.q_ready = q_ready;
+  a.q_epoch = q_epoch;
   a.debug_stall = h->opt.debug_stall;
-  PA_CUDA(launch_attention(a, maps, h->n_sm, st));
-  if (e2) {
-    PA_CUDA(cudaEventRecord(e2, st));
-    h->ev_pending.push_back(e0);
-    h->ev_pending.push_back(e1);
-    h->ev_pending.push_back(e2);
-  }
+  PA_CUDA(launch_attention(a, maps, h->n_sm, st, overlap_prev));
   return PA_OK;
+}
+
+// Events for pa_timing around a widening pass and the attention work after
+// it: mark(0) before the pass, mark(1) after it, mark(2) after the attention.
+struct TimingMarks {
+  cudaEvent_t e[3] = {nullptr, nullptr, nullptr};
+  int init(pa_handle h) {
+    if (!h->opt.record_timing) return PA_OK;
+    for (auto& x : e)
+      if (!(x = take_event(h))) return PA_ECUDA;
+    return PA_OK;
+  }
+  int mark(pa_handle h, int i, cudaStream_t st) {
+    if (!e[i]) return PA_OK;
+    PA_CUDA(cudaEventRecord(e[i], st));
+    if (i == 2)
+      for (auto& x : e) h->ev_pending.push_back(x);
+    return PA_OK;
+  }
+};
+
+// The widening pass and the attention kernel of plan P, whose sequence table
+// and unit list are already on the device at d_seqs / d_units (the caller
+// has sized the widened workspace for P).
+int launch_plan(pa_handle h, const Plan& P, const SeqGeom* d_seqs, const Unit* d_units, int n_seq, const void* q,
+                const int8_t* kp, const int8_t* vp, const float* ksc, const float* vsc, const int32_t* bt, int S,
+                int W, float sm_scale, void* out, cudaStream_t st, const void* gate) {
+  TimingMarks tm;
+  int rc;
+  if ((rc = tm.init(h)) || (rc = tm.mark(h, 0, st))) return rc;
+  if ((rc = launch_widen_plan(h, P, d_seqs, n_seq, kp, vp, ksc, vsc, bt, sm_scale, st))) return rc;
+  if ((rc = tm.mark(h, 1, st))) return rc;
+  if ((rc = launch_attention_plan(h, P, d_seqs, d_units, (int)P.units.size(), q, S, W, sm_scale, out, st, gate)))
+    return rc;
+  return tm.mark(h, 2, st);
 }
 
 int run(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* kp, const int8_t* vp,
@@ -475,7 +524,7 @@ int pa_create(pa_handle* out, int n_q_heads, int n_kv_heads, int head_dim, int p
   h->opt = o;
   h->device = dev;
   h->n_sm = prop.multiProcessorCount;
-  if (cudaMalloc(&h->d_err, sizeof(int)) != cudaSuccess || cudaMalloc(&h->d_counter, sizeof(int)) != cudaSuccess ||
+  if (cudaMalloc(&h->d_err, sizeof(int)) != cudaSuccess ||
       cudaMemset(h->d_err, 0, sizeof(int)) != cudaSuccess ||
       cudaEventCreateWithFlags(&h->upload_done, cudaEventDisableTiming) != cudaSuccess) {
     pa_destroy(h);
@@ -488,7 +537,7 @@ int pa_create(pa_handle* out, int n_q_heads, int n_kv_heads, int head_dim, int p
 void pa_destroy(pa_handle h) {
   if (!h) return;
   cudaDeviceSynchronize();
-  void* ptrs[] = {h->kw, h->vt, h->ks, h->vs, h->vsmax, h->d_seqs, h->d_units, h->d_err, h->d_counter, h->d_dec,
+  void* ptrs[] = {h->kw, h->vt, h->ks, h->vs, h->vsmax, h->d_seqs, h->d_units, h->d_err, h->d_qflags, h->d_dec,
                   h->d_part};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -535,20 +584,15 @@ int pa_prefill_batch_gated(pa_handle h, int n_seq, const pa_seq* seqs, const voi
 }
 
 // A piece of a sequence's query rows, computed as one call of its own.
-struct Piece {
-  int seq;     // sequence index (its block-table row)
-  pa_seq s;    // the piece as a sequence: its rows, same context
-};
-
 // The host-buffer path is a pipeline over chunks of the query rows: the pool,
-// scales and block table go in first, then each chunk's q rows on one copy
-// stream, while the previous chunk is computed on the caller's stream and
-// the chunk before that is copied out on another copy stream.  A chunk is a
-// contiguous run of the sequences' rows laid end to end, so it holds at most
-// one piece of each sequence, sequences in order, and its block-table rows
-// are consecutive; a piece boundary inside a sequence falls on a multiple of
-// 256 tokens (a whole number of work units for every GQA ratio), so no unit
-// is split between chunks.
+// scales and block table go in first and are widened once, then each chunk's
+// q rows go in on one copy stream while the previous chunk is computed on the
+// caller's stream and the one before that is copied out on another copy
+// stream.  A chunk is a contiguous run of the sequences' rows laid end to
+// end; a chunk boundary inside a sequence falls on a multiple of a work
+// unit's tokens (256 / G, units start on those multiples), so every unit of
+// the call's one plan belongs to exactly one chunk, and a chunk's attention
+// launch runs just its units.
 int pa_prefill_host(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* k_pool,
                     const int8_t* v_pool, const float* k_scale, const float* v_scale, const int32_t* block_table,
                     int n_sink_blk, int n_win_blk, float sm_scale, void* out, void* stream) {
@@ -576,66 +620,70 @@ int pa_prefill_host(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, c
   for (int i = 0; i < 7; ++i)
     if ((rc = grow_bytes(h->hb[i], h->hb_cap[i], bytes[i]))) return rc;
 
-  // chunk boundaries on the sequences' rows laid end to end: a short first
-  // chunk (its copy-in is the pipeline's start-up) and a short last one (its
-  // copy-out is the drain), the rest in chunks of at most 6144 tokens (the
-  // best of 3072..12288 measured at 32k); a
-  // boundary inside a sequence moves to a multiple of 256 tokens
+  // chunk boundaries on the sequences' rows laid end to end: chunks of two
+  // waves of work units (a wave: one unit for every SM pair the kernel runs
+  // at once; a part-filled wave leaves pairs idle), the remainder last.  Short
+  // chunks shorten the copy-in before the first one and the copy-out after
+  // the last; one or two waves measured best at 32k tokens.  A boundary
+  // inside a sequence moves to a multiple of a unit's tokens.
   std::vector<long long> base(n_seq + 1, 0);  // first row of each sequence, end to end
   for (int s = 0; s < n_seq; ++s) base[s + 1] = base[s] + seqs[s].n_q;
   const long long T = base[n_seq];
+  const long long UT = kUnitRows / h->G;  // tokens per unit
+  const long long wave = std::max(UT, (long long)pa::attention_pairs(h->n_sm) * UT / h->HKV);
   std::vector<long long> cuts;  // chunk ends, end to end
-  if (T <= 4096) {
-    cuts.push_back(T);
-  } else {
-    const long long edge = 2048, mid = T - 2 * edge;
-    const long long k = std::max(1LL, (mid + 6143) / 6144);
-    for (long long i = 0; i <= k; ++i) cuts.push_back(edge + mid * i / k);
-    cuts.push_back(T);
+  for (long long at = 0; at < T;) {
+    at = std::min(T, at + 2 * wave);
+    cuts.push_back(at);
   }
-  for (long long& cut : cuts) {  // inside a sequence: down (or up) to a multiple of 256 tokens
+  for (long long& cut : cuts) {  // inside a sequence: down (or up) to a multiple of UT tokens
     const int s = (int)(std::upper_bound(base.begin(), base.end(), cut) - base.begin()) - 1;
     if (s < 0 || s >= n_seq || cut == base[s]) continue;
     const long long abs_pos = seqs[s].q_start + (cut - base[s]);
-    long long r = abs_pos / 256 * 256;
-    if (r <= seqs[s].q_start) r = std::min((long long)seqs[s].q_start + seqs[s].n_q, (abs_pos / 256 + 1) * 256);
+    long long r = abs_pos / UT * UT;
+    if (r <= seqs[s].q_start) r = std::min((long long)seqs[s].q_start + seqs[s].n_q, (abs_pos / UT + 1) * UT);
     cut = base[s] + (r - seqs[s].q_start);
   }
-  std::vector<std::vector<Piece>> chunks;
+  std::vector<std::vector<pa_seq>> chunks;  // per chunk, its pieces of the sequences (rows, same context)
+  std::vector<long long> ends;  // chunk ends, end to end
   long long lo = 0;
   for (const long long hi : cuts) {
     if (hi <= lo) continue;
     chunks.emplace_back();
+    ends.push_back(hi);
     for (int s = 0; s < n_seq; ++s) {
       const long long a = std::max(lo, base[s]), b = std::min(hi, base[s + 1]);
       if (a >= b) continue;
       const int qa = seqs[s].q_start + (int)(a - base[s]);
-      chunks.back().push_back(Piece{s, pa_seq{seqs[s].q_off + (qa - seqs[s].q_start), qa, (int)(b - a), seqs[s].n_ctx}});
+      chunks.back().push_back(pa_seq{seqs[s].q_off + (qa - seqs[s].q_start), qa, (int)(b - a), seqs[s].n_ctx});
     }
     lo = hi;
   }
   const int n_ch = (int)chunks.size();
 
-  // every chunk's plan, uploaded in one go ahead of the large copies (a small
-  // copy queued behind them on the copy engine would hold up the first chunk)
-  std::vector<Plan> plans(n_ch);
-  std::vector<size_t> off_s(n_ch), off_u(n_ch);
-  std::vector<std::vector<pa_seq>> cseqs(n_ch);
-  size_t n_s = 0, n_u = 0, max_rows = 0, max_seq = 0;
-  for (int c = 0; c < n_ch; ++c) {
-    for (const Piece& pc : chunks[c]) cseqs[c].push_back(pc.s);
-    if ((rc = build_plan(h->HQ, h->HKV, (int)cseqs[c].size(), cseqs[c].data(), n_sink_blk, n_win_blk, h->max_pages,
-                         plans[c])))
-      return rc;
-    off_s[c] = n_s;
-    off_u[c] = n_u;
-    n_s += plans[c].seqs.size();
-    n_u += plans[c].units.size();
-    max_rows = std::max(max_rows, (size_t)plans[c].n_tok_total);
-    max_seq = std::max(max_seq, cseqs[c].size());
+  // one plan for the whole call (so one widening pass and the same per-sequence
+  // V-scale maximum as pa_prefill_batch); its units split by chunk, each
+  // chunk's list still in decreasing cost; all uploaded in one go ahead of the
+  // large copies (a small copy queued behind them would hold up the first chunk)
+  Plan P;
+  if ((rc = build_plan(h->HQ, h->HKV, n_seq, seqs, n_sink_blk, n_win_blk, h->max_pages, P))) return rc;
+  std::vector<std::vector<Unit>> cunits(n_ch);
+  for (const Unit& u : P.units) {
+    const pa_seq& q0 = seqs[u.seq];
+    const long long row = base[u.seq] + (std::max(u.t0, q0.q_start) - q0.q_start);  // its first row, end to end
+    const int c = (int)(std::upper_bound(ends.begin(), ends.end(), row) - ends.begin());
+    if (c >= n_ch) return PA_EINVAL;  // cannot happen: every row lies in a chunk
+    cunits[c].push_back(u);
   }
-  if ((rc = reserve_rows(h, max_rows))) return rc;
-  if ((rc = grow(h->vsmax, h->vsmax_cap, max_seq * h->HKV))) return rc;
+  std::vector<size_t> off_u(n_ch);
+  size_t n_u = 0;
+  for (int c = 0; c < n_ch; ++c) {
+    off_u[c] = n_u;
+    n_u += cunits[c].size();
+  }
+  const size_t n_s = P.seqs.size();
+  if ((rc = reserve_rows(h, (size_t)P.n_tok_total))) return rc;
+  if ((rc = grow(h->vsmax, h->vsmax_cap, (size_t)n_seq * h->HKV))) return rc;
   if ((rc = grow(h->d_pseqs, h->pseqs_cap, n_s))) return rc;
   if ((rc = grow(h->d_punits, h->punits_cap, n_u))) return rc;
   if (!h->pstage_done) PA_CUDA(cudaEventCreateWithFlags(&h->pstage_done, cudaEventDisableTiming));
@@ -648,61 +696,89 @@ int pa_prefill_host(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, c
     PA_CUDA(cudaMallocHost(&h->h_pstage, bytes_s + bytes_u));
     h->h_pstage_cap = bytes_s + bytes_u;
   }
-  for (int c = 0; c < n_ch; ++c) {
-    std::memcpy(static_cast<SeqGeom*>(h->h_pstage) + off_s[c], plans[c].seqs.data(),
-                plans[c].seqs.size() * sizeof(SeqGeom));
-    std::memcpy(reinterpret_cast<Unit*>(static_cast<char*>(h->h_pstage) + bytes_s) + off_u[c], plans[c].units.data(),
-                plans[c].units.size() * sizeof(Unit));
-  }
+  std::memcpy(h->h_pstage, P.seqs.data(), bytes_s);
+  for (int c = 0; c < n_ch; ++c)
+    std::memcpy(reinterpret_cast<Unit*>(static_cast<char*>(h->h_pstage) + bytes_s) + off_u[c], cunits[c].data(),
+                cunits[c].size() * sizeof(Unit));
   PA_CUDA(cudaMemcpyAsync(h->d_pseqs, h->h_pstage, bytes_s, cudaMemcpyHostToDevice, st));
   PA_CUDA(cudaMemcpyAsync(h->d_punits, static_cast<char*>(h->h_pstage) + bytes_s, bytes_u, cudaMemcpyHostToDevice, st));
   PA_CUDA(cudaEventRecord(h->pstage_done, st));
   h->pstage_recorded = true;
 
+  // chunk c > 0 waits for its rows on the device (a flag the copy stream
+  // writes after them), not with an event wait on the stream, so that its
+  // launch can overlap the previous chunk's (programmatic dependent launch)
+  const WriteValue32Fn write_value = write_value_fn();
+  if (write_value && h->qflags_cap < n_ch) {
+    if (h->d_qflags) cudaFree(h->d_qflags);
+    h->d_qflags = nullptr;
+    h->qflags_cap = 0;
+    PA_CUDA(cudaMalloc(&h->d_qflags, (size_t)n_ch * sizeof(unsigned int)));
+    PA_CUDA(cudaMemset(h->d_qflags, 0, (size_t)n_ch * sizeof(unsigned int)));
+    h->qflags_cap = n_ch;
+  }
+  if (++h->q_epoch == 0) h->q_epoch = 1;  // flags start at 0: never a live epoch
+  const unsigned int epoch = h->q_epoch;
+
   // streams and events
   if (!h->s_h2d) PA_CUDA(cudaStreamCreateWithFlags(&h->s_h2d, cudaStreamNonBlocking));
   if (!h->s_d2h) PA_CUDA(cudaStreamCreateWithFlags(&h->s_d2h, cudaStreamNonBlocking));
-  const size_t n_ev = 2 + 2 * (size_t)n_ch;
+  const size_t n_ev = 3 + 2 * (size_t)n_ch;
   while (h->pipe_ev.size() < n_ev) {
     cudaEvent_t e;
     PA_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
     h->pipe_ev.push_back(e);
   }
-  cudaEvent_t ev_start = h->pipe_ev[0], ev_end = h->pipe_ev[1];
-  cudaEvent_t* ev_in = h->pipe_ev.data() + 2;           // chunk c's q rows are in
-  cudaEvent_t* ev_done = h->pipe_ev.data() + 2 + n_ch;  // chunk c is computed
+  cudaEvent_t ev_start = h->pipe_ev[0], ev_end = h->pipe_ev[1], ev_pool = h->pipe_ev[2];
+  cudaEvent_t* ev_in = h->pipe_ev.data() + 3;           // chunk c's q rows are in
+  cudaEvent_t* ev_done = h->pipe_ev.data() + 3 + n_ch;  // chunk c is computed
 
   // inputs: after whatever the caller's stream did before
   PA_CUDA(cudaEventRecord(ev_start, st));
   PA_CUDA(cudaStreamWaitEvent(h->s_h2d, ev_start, 0));
   for (int i = 1; i < 6; ++i) PA_CUDA(cudaMemcpyAsync(h->hb[i], src[i], bytes[i], cudaMemcpyHostToDevice, h->s_h2d));
+  PA_CUDA(cudaEventRecord(ev_pool, h->s_h2d));
   for (int c = 0; c < n_ch; ++c) {
-    for (const Piece& pc : chunks[c]) {
-      const size_t off = (size_t)pc.s.q_off * row_bytes;
+    for (const pa_seq& pc : chunks[c]) {
+      const size_t off = (size_t)pc.q_off * row_bytes;
       PA_CUDA(cudaMemcpyAsync(static_cast<char*>(h->hb[0]) + off, static_cast<const char*>(q) + off,
-                              (size_t)pc.s.n_q * row_bytes, cudaMemcpyHostToDevice, h->s_h2d));
+                              (size_t)pc.n_q * row_bytes, cudaMemcpyHostToDevice, h->s_h2d));
     }
     PA_CUDA(cudaEventRecord(ev_in[c], h->s_h2d));
+    if (write_value && c > 0 &&
+        write_value(h->s_h2d, (CUdeviceptr)(h->d_qflags + c), epoch, CU_STREAM_WRITE_VALUE_DEFAULT) != CUDA_SUCCESS)
+      return PA_ECUDA;
   }
-  // compute each chunk once its rows are in; copy its output out behind it
+  // widen the whole pool once it is in, then compute each chunk once its rows
+  // are in; copy its output out behind it
   PA_CUDA(cudaStreamWaitEvent(h->s_d2h, ev_start, 0));
-  for (int c = 0; c < n_ch; ++c) {
-    const int s0 = chunks[c].front().seq;
-    PA_CUDA(cudaStreamWaitEvent(st, ev_in[c], 0));
-    rc = launch_plan(h, plans[c], h->d_pseqs + off_s[c], h->d_punits + off_u[c], (int)cseqs[c].size(), h->hb[0],
-                     static_cast<const int8_t*>(h->hb[1]), static_cast<const int8_t*>(h->hb[2]),
-                     static_cast<const float*>(h->hb[3]), static_cast<const float*>(h->hb[4]),
-                     static_cast<const int32_t*>(h->hb[5]) + (size_t)s0 * h->max_pages, n_sink_blk, n_win_blk,
-                     sm_scale, h->hb[6], st, nullptr);
-    if (rc) break;
+  PA_CUDA(cudaStreamWaitEvent(st, ev_pool, 0));
+  TimingMarks tm;
+  if (!(rc = tm.init(h)) && !(rc = tm.mark(h, 0, st)))
+    rc = launch_widen_plan(h, P, h->d_pseqs, n_seq, static_cast<const int8_t*>(h->hb[1]),
+                           static_cast<const int8_t*>(h->hb[2]), static_cast<const float*>(h->hb[3]),
+                           static_cast<const float*>(h->hb[4]), static_cast<const int32_t*>(h->hb[5]), sm_scale, st);
+  if (!rc) rc = tm.mark(h, 1, st);
+  bool after_attn = false;  // the last launch on st is an attention launch of this call
+  for (int c = 0; c < n_ch && !rc; ++c) {
+    const bool on_device = write_value && c > 0 && after_attn;
+    if (!on_device) PA_CUDA(cudaStreamWaitEvent(st, ev_in[c], 0));
+    if (!cunits[c].empty()) {
+      if ((rc = launch_attention_plan(h, P, h->d_pseqs, h->d_punits + off_u[c], (int)cunits[c].size(), h->hb[0],
+                                      n_sink_blk, n_win_blk, sm_scale, h->hb[6], st, nullptr, on_device,
+                                      on_device ? h->d_qflags + c : nullptr, epoch)))
+        break;
+      after_attn = true;
+    }
     PA_CUDA(cudaEventRecord(ev_done[c], st));
     PA_CUDA(cudaStreamWaitEvent(h->s_d2h, ev_done[c], 0));
-    for (const Piece& pc : chunks[c]) {
-      const size_t off = (size_t)pc.s.q_off * row_bytes;
+    for (const pa_seq& pc : chunks[c]) {
+      const size_t off = (size_t)pc.q_off * row_bytes;
       PA_CUDA(cudaMemcpyAsync(static_cast<char*>(out) + off, static_cast<const char*>(h->hb[6]) + off,
-                              (size_t)pc.s.n_q * row_bytes, cudaMemcpyDeviceToHost, h->s_d2h));
+                              (size_t)pc.n_q * row_bytes, cudaMemcpyDeviceToHost, h->s_d2h));
     }
   }
+  if (!rc) rc = tm.mark(h, 2, st);
   // the caller's stream waits for both copy streams
   PA_CUDA(cudaEventRecord(ev_end, h->s_d2h));
   PA_CUDA(cudaStreamWaitEvent(st, ev_end, 0));

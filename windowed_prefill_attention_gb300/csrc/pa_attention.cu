@@ -274,6 +274,8 @@ __device__ __forceinline__ void role_producer_q(const AttnParams& p, const AttnM
   bool ok = true;
   int prev_t0 = 0, prev_g = 0;
   SeqGeom prev_sg{};
+  // rows still on their way in from another stream: wait for their flag
+  if (r < 4 && p.q_ready && c.pair < p.n_units) ok = flag_wait(p.q_ready, p.q_epoch, c.wc, 18);
   for (int u = c.pair; u < p.n_units && ok; u += c.n_pairs) {
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
@@ -824,6 +826,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   c.pair = (int)(blockIdx.x >> 1);
   c.n_pairs = (int)(gridDim.x >> 1);
   c.wc = WaitCtl{p.err, p.wait_ns};
+  // a launch queued behind this one that reads nothing this one writes may
+  // start on each pair this one leaves
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kSmTmemSlot);
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
@@ -895,12 +900,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_attention(const AttnParams& p, const AttnMaps& m, int n_sm, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
-  if (e != cudaSuccess) return e;
-  // persistent grid: one CTA pair per co-resident cluster slot (or per unit)
+int attention_pairs(int n_sm) {
   static int max_pairs = -1;
   if (max_pairs < 0) {
+    if (cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem) !=
+        cudaSuccess) {
+      (void)cudaGetLastError();
+      return imax(1, n_sm / 2);
+    }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2 * (unsigned)imax(1, n_sm / 2));
     cfg.blockDim = dim3(kThreads);
@@ -912,9 +919,31 @@ cudaError_t launch_attention(const AttnParams& p, const AttnMaps& m, int n_sm, c
     }
     max_pairs = mc;
   }
-  const int pairs = imax(1, imin(p.n_units, max_pairs));
-  attention_kernel<<<2 * pairs, kThreads, kAttnSmem, st>>>(p, m);
-  return cudaGetLastError();
+  return max_pairs;
+}
+
+cudaError_t launch_attention(const AttnParams& p, const AttnMaps& m, int n_sm, cudaStream_t st, bool overlap_prev) {
+  cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+  if (e != cudaSuccess) return e;
+  // persistent grid: one CTA pair per co-resident cluster slot (or per unit)
+  const int pairs = imax(1, imin(p.n_units, attention_pairs(n_sm)));
+  if (!overlap_prev) {
+    attention_kernel<<<2 * pairs, kThreads, kAttnSmem, st>>>(p, m);
+    return cudaGetLastError();
+  }
+  // programmatic dependent launch: its pairs start as the previous attention
+  // launch's pairs leave (the two share no data)
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(2 * (unsigned)pairs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kAttnSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attention_kernel, p, m);
 }
 
 }  // namespace pa

@@ -61,7 +61,8 @@ struct AttnParams {
   int q_mode, p_mode;
   int* err;
   unsigned long long wait_ns;
-  int* unit_counter;          // persistent-grid work counter (zeroed per launch)
+  const unsigned int* q_ready;  // nullptr, or a word that equals q_epoch once q holds the units' rows
+  unsigned int q_epoch;
   int debug_stall;            // test hook: first wait targets a barrier nothing arrives at
 };
 
@@ -120,7 +121,12 @@ struct DecodeParams {
 cudaError_t launch_decode(const DecodeParams& p, int n_seq, cudaStream_t st);
 // Split-kernel CTAs that fit on one SM at a time (occupancy, cached).
 int decode_ctas_per_sm();
-cudaError_t launch_attention(const AttnParams& p, const AttnMaps& m, int n_sm, cudaStream_t st);
+// overlap_prev: the launch may start while the previous attention launch on
+// `st` is still running (it must read nothing that launch writes).
+cudaError_t launch_attention(const AttnParams& p, const AttnMaps& m, int n_sm, cudaStream_t st,
+                             bool overlap_prev = false);
+// CTA pairs of the attention kernel that run at once (its persistent grid).
+int attention_pairs(int n_sm);
 
 // Debug exports (tests only).
 cudaError_t launch_debug_gather(const WidenParams& p, int seq, int8_t* k_out, int8_t* v_out, float* ks_out,

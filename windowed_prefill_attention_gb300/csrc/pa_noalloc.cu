@@ -224,7 +224,7 @@ extern "C" int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_page
   a.p_mode = PA_P_F16;
   a.err = err;
   a.wait_ns = 2000ull * 1000000ull;
-  a.unit_counter = nullptr;
+  a.q_ready = nullptr;
   a.debug_stall = 0;
   if (launch_attention(a, m, prop.multiProcessorCount, st) != cudaSuccess) return PA_ECUDA;
 

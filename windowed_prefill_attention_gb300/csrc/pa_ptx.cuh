@@ -164,6 +164,34 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   }
 }
 
+// Wait until the word at `flag` (written from another stream by a stream
+// memory operation, after a copy) equals `value`: acquire at GPU scope, then
+// a proxy fence so that TMA loads issued afterwards see what the copy wrote.
+// Bounded like mbar_wait.
+__device__ __forceinline__ bool flag_wait(const unsigned int* flag, unsigned int value, const WaitCtl& w, int site) {
+  auto load = [flag]() {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    return v;
+  };
+  if (load() != value) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+      __nanosleep(200);
+      if (load() == value) break;
+      if ((i & 31u) == 0u) {
+        if (*reinterpret_cast<volatile int*>(w.err) != 0) return false;
+        if (globaltimer_ns() - t0 > w.limit_ns) {
+          atomicCAS(w.err, 0, DEV_ERR_TIMEOUT | (site & 0xff));
+          return false;
+        }
+      }
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
 // Teardown wait: ignores the error word (the copies or MMAs it waits for were
 // issued and will land) and gives up only when `limit_ns` runs out.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
