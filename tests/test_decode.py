@@ -85,3 +85,33 @@ def test_decode_bad_page_is_reported():
     bt[0, (inp.seq_desc[0, 3] - 1) // 16] = inp.k_pool.shape[0] + 9  # the query's own block: always visible
     _, rc = run_decode(inp, bt=bt)
     assert rc == pa.PA_EBADPAGE
+
+
+def test_decode_repeated_calls_on_one_handle_are_identical():
+    """Calls on one handle, with batches of other sizes and split counts in
+    between (its partials buffer grows and is reused), give the bits of a call
+    on a fresh handle."""
+    import torch
+
+    import windowed_prefill_attention_gb300 as pa
+    big, small = make_inputs(CASES["many"]), make_inputs(CASES["mixed"])
+    ref_big, rc0 = run_decode(big)
+    ref_small, rc1 = run_decode(small)
+    assert rc0 == 0 and rc1 == 0
+    wl = big.wl
+    pool = max(big.k_pool.shape[0], small.k_pool.shape[0])
+    width = max(big.block_table.shape[1], small.block_table.shape[1])
+    h = pa.pa_create(wl.n_q_heads, wl.n_kv_heads, pool, width)
+    try:
+        for inp, ref in ((big, ref_big), (small, ref_small), (big, ref_big), (small, ref_small), (small, ref_small)):
+            d = to_device(inp)
+            bt = np.zeros((inp.block_table.shape[0], width), np.int32)  # the handle's row stride
+            bt[:, :inp.block_table.shape[1]] = inp.block_table
+            d["block_table"] = torch.from_numpy(bt).cuda()
+            out = torch.full_like(d["q"], float("nan"))
+            pa.pa_decode(h, inp.seq_desc, d["q"], d["k_pool"], d["v_pool"], d["k_scale"], d["v_scale"],
+                         d["block_table"], inp.wl.n_sink_blk, inp.wl.n_win_blk, inp.wl.sm_scale, out)
+            assert pa.pa_last_error(h) == 0
+            assert np.array_equal(out.float().cpu().numpy(), ref, equal_nan=True)
+    finally:
+        pa.pa_destroy(h)
