@@ -27,10 +27,18 @@ namespace pa {
 // ======================================================================
 constexpr int kWidenThreads = 256;
 
+// One CTA per stored 16-token block.  Every load of the block (its K and V
+// codes, HKV x 16-byte chunks each per thread, and its scales) is issued
+// before the first store: the stores go to other arrays, but the compiler
+// cannot tell, and a load behind each store would leave one load in flight
+// per thread (the kernel is bound by load latency, not by bandwidth).
+template <int HKV>
 __global__ void __launch_bounds__(kWidenThreads) widen_kernel(const WidenParams p) {
-  __shared__ __align__(16) int8_t vpage[kPage * 8 * kHeadDim];  // up to 8 kv heads staged
+  __shared__ __align__(16) int8_t vpage[kPage * HKV * kHeadDim];
+  __shared__ unsigned int vmax_sh[HKV];  // the block's largest V scale per head (bit pattern)
   const int blk = blockIdx.x;
   const int tid = threadIdx.x;
+  if (tid < HKV) vmax_sh[tid] = 0u;
   int s = 0;
   while (s + 1 < p.n_seq && p.seqs[s + 1].tok_off <= blk * kPage) ++s;
   const SeqGeom sg = p.seqs[s];
@@ -41,18 +49,33 @@ __global__ void __launch_bounds__(kWidenThreads) widen_kernel(const WidenParams 
   const bool bad = phys < 0 || phys >= p.n_pool;
   if (bad && tid == 0) atomicCAS(p.err, 0, DEV_ERR_BAD_PAGE);
   const int n_valid = bad ? 0 : imax(0, imin(kPage, sg.n_ctx - kb * kPage));
-  const int HKV = p.HKV;
   const size_t page_base = (size_t)(bad ? 0 : phys) * kPage * HKV * kHeadDim;
 
-  // K: 16-byte chunks of 16 codes, (token, head, chunk) over the block.
-  for (int idx = tid; idx < kPage * HKV * 16; idx += kWidenThreads) {
-    const int c = idx & 15;
-    const int g = (idx >> 4) % HKV;
-    const int tk = (idx >> 4) / HKV;
-    int4 raw = make_int4(0, 0, 0, 0);
-    if (tk < n_valid)
-      raw = *reinterpret_cast<const int4*>(p.k_pool + page_base + ((size_t)tk * HKV + g) * kHeadDim + c * 16);
-    const int8_t* cb = reinterpret_cast<const int8_t*>(&raw);
+  // loads: chunk idx = tid + 256 i is bytes [16 idx, 16 idx + 16) of the
+  // page, i.e. token idx / (16 HKV), head (idx / 16) % HKV, dims 16 (idx % 16) on
+  int4 kr[HKV], vr[HKV];
+#pragma unroll
+  for (int i = 0; i < HKV; ++i) {
+    const int idx = tid + kWidenThreads * i;
+    kr[i] = vr[i] = make_int4(0, 0, 0, 0);
+    if (idx / (HKV * 16) < n_valid) {
+      kr[i] = __ldg(reinterpret_cast<const int4*>(p.k_pool + page_base) + idx);
+      vr[i] = __ldg(reinterpret_cast<const int4*>(p.v_pool + page_base) + idx);
+    }
+  }
+  float ksv = 0.f, vsv = 0.f;  // thread tid < 16 HKV: token tid / HKV, head tid % HKV
+  if (tid < kPage * HKV && tid / HKV < n_valid) {
+    const size_t slot = ((size_t)phys * kPage + tid / HKV) * HKV + tid % HKV;
+    ksv = __ldg(p.k_scale + slot);
+    vsv = __ldg(p.v_scale + slot);
+  }
+
+  // K: each chunk's 16 codes as bf16, at its row of the head's widened K
+#pragma unroll
+  for (int i = 0; i < HKV; ++i) {
+    const int idx = tid + kWidenThreads * i;
+    const int c = idx & 15, g = (idx >> 4) % HKV, tk = (idx >> 4) / HKV;
+    const int8_t* cb = reinterpret_cast<const int8_t*>(&kr[i]);
     __align__(16) __nv_bfloat16 h[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) h[e] = __int2bfloat16_rn((int)cb[e]);
@@ -60,13 +83,9 @@ __global__ void __launch_bounds__(kWidenThreads) widen_kernel(const WidenParams 
     dst[0] = reinterpret_cast<const int4*>(h)[0];
     dst[1] = reinterpret_cast<const int4*>(h)[1];
   }
-  // V: stage the page, then write each (head, dim) column of 16 tokens.
-  for (int idx = tid; idx < kPage * HKV * 16; idx += kWidenThreads) {
-    const int tk = idx / (HKV * 16);
-    int4 raw = make_int4(0, 0, 0, 0);
-    if (tk < n_valid) raw = *reinterpret_cast<const int4*>(p.v_pool + page_base + (size_t)idx * 16);
-    reinterpret_cast<int4*>(vpage)[idx] = raw;
-  }
+  // V: stage the page, then write each (head, dim) column of 16 tokens
+#pragma unroll
+  for (int i = 0; i < HKV; ++i) reinterpret_cast<int4*>(vpage)[tid + kWidenThreads * i] = vr[i];
   __syncthreads();
   for (int col = tid; col < HKV * kHeadDim; col += kWidenThreads) {
     const int g = col / kHeadDim, d = col % kHeadDim;
@@ -77,24 +96,35 @@ __global__ void __launch_bounds__(kWidenThreads) widen_kernel(const WidenParams 
     dst[0] = reinterpret_cast<const int4*>(h)[0];
     dst[1] = reinterpret_cast<const int4*>(h)[1];
   }
-  // Scales (0 past the end of the context) and the running max of V scales.
+  // scales (0 past the end of the context) and the running max of V scales:
+  // reduced in the block first, then one global atomic per head, and only
+  // when it raises the maximum (thousands of blocks update the same words)
   if (tid < kPage * HKV) {
     const int tk = tid / HKV, g = tid % HKV;
-    float ksv = 0.f, vsv = 0.f;
-    if (tk < n_valid) {
-      const size_t slot = ((size_t)phys * kPage + tk) * HKV + g;
-      ksv = p.k_scale[slot];
-      vsv = p.v_scale[slot];
-    }
     p.ks[(size_t)g * p.n_tok_cap + row0 + tk] = ksv * p.k_mult;
     p.vs[(size_t)g * p.n_tok_cap + row0 + tk] = vsv;
-    if (vsv > 0.f) atomicMax(p.vsmax + s * HKV + g, __float_as_uint(vsv));
+    if (vsv > 0.f) atomicMax(&vmax_sh[g], __float_as_uint(vsv));
+  }
+  __syncthreads();
+  if (tid < HKV) {
+    const unsigned int m = vmax_sh[tid];
+    unsigned int* gm = p.vsmax + s * HKV + tid;
+    if (m > *reinterpret_cast<volatile unsigned int*>(gm)) atomicMax(gm, m);
   }
 }
 
 cudaError_t launch_widen(const WidenParams& p, cudaStream_t st) {
-  if (p.HKV > 8) return cudaErrorInvalidValue;
-  widen_kernel<<<p.n_stored_blocks, kWidenThreads, 0, st>>>(p);
+  switch (p.HKV) {
+    case 1: widen_kernel<1><<<p.n_stored_blocks, kWidenThreads, 0, st>>>(p); break;
+    case 2: widen_kernel<2><<<p.n_stored_blocks, kWidenThreads, 0, st>>>(p); break;
+    case 3: widen_kernel<3><<<p.n_stored_blocks, kWidenThreads, 0, st>>>(p); break;
+    case 4: widen_kernel<4><<<p.n_stored_blocks, kWidenThreads, 0, st>>>(p); break;
+    case 5: widen_kernel<5><<<p.n_stored_blocks, kWidenThreads, 0, st>>>(p); break;
+    case 6: widen_kernel<6><<<p.n_stored_blocks, kWidenThreads, 0, st>>>(p); break;
+    case 7: widen_kernel<7><<<p.n_stored_blocks, kWidenThreads, 0, st>>>(p); break;
+    case 8: widen_kernel<8><<<p.n_stored_blocks, kWidenThreads, 0, st>>>(p); break;
+    default: return cudaErrorInvalidValue;  // the handle accepts 1..8 kv heads
+  }
   return cudaGetLastError();
 }
 
