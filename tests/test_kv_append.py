@@ -146,3 +146,34 @@ def test_kv_append_bad_page_is_reported_and_skipped():
         good[inp.block_table[0][(1024 + 20) // 16]] = False  # the slots the bad entry stood for keep old values
         assert np.array_equal(bits(got)[good], bits(ref)[good])
         assert np.array_equal(bits(got)[~good], bits(orig)[~good])
+
+
+def test_kv_append_scale_is_the_rounded_quotient_for_every_bf16_magnitude():
+    """The kernel's scale absmax / 127 (a reciprocal product and one FMA
+    correction, no division) against the IEEE quotient, for every positive
+    finite bf16 absmax: one row per value, K and V, every kv head."""
+    import dataclasses as dc
+    inp = make_inputs(CONFIGS["chunked_ragged"])
+    hkv = inp.wl.n_kv_heads
+    mags = np.arange(0x0001, 0x7F80, dtype=np.uint32)  # bf16 bit patterns of the positive finite values
+    n_new = len(mags)
+    pages = (n_new + 15) // 16
+    a = (mags << 16).view(np.float32)
+    rows = np.zeros((n_new, hkv, 256), dtype=np.float32)
+    rows[:, :, 0] = a[:, None]                      # the row's absmax
+    rows[:, :, 1] = -a[:, None] * np.float32(0.37)  # and a code that is not +-127
+    bits = _bf16_bits(rows)
+    pool = dc.replace(inp, k_pool=np.zeros((pages, 16, hkv, 256), np.int8),
+                      v_pool=np.zeros((pages, 16, hkv, 256), np.int8),
+                      k_scale=np.zeros((pages, 16, hkv), np.float32), v_scale=np.zeros((pages, 16, hkv), np.float32),
+                      block_table=np.arange(pages, dtype=np.int32)[None, :])
+    (kp, vp, ks, vs), rc = _append_gpu(pool, 0, 0, bits, bits, bt_row=np.arange(pages, dtype=np.int32))
+    assert rc == 0
+    want_scale = (a / np.float32(127.0)).astype(np.float32)
+    for sc in (ks, vs):
+        got = sc.reshape(-1, hkv)[:n_new]
+        assert np.array_equal(got.view(np.uint32), np.repeat(want_scale[:, None], hkv, 1).view(np.uint32))
+    want = oracle.kv_append(pool.k_pool, pool.v_pool, pool.k_scale, pool.v_scale, np.arange(pages, dtype=np.int32),
+                            0, bits, bits)
+    for got, ref in zip((kp, vp), want[:2]):
+        assert np.array_equal(got.view(np.uint8), ref.view(np.uint8))

@@ -156,29 +156,47 @@ __device__ __forceinline__ uint2 quantise_row8(const uint4 raw, float am, float&
     x[2 * e] = __uint_as_float(w[e] << 16);
     x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
   }
-  const float scale = __fdiv_rn(am, 127.f);
+  // scale = RN(am / 127) without a division: Markstein's division by a
+  // constant (q0 = RN(am r), r = RN(1/127); the remainder am - 127 q0 is exact
+  // in one FMA; q1 = RN(q0 + rem r)).  Checked exhaustively: for every
+  // positive finite bf16 magnitude the remainder is representable and q1 is
+  // the correctly rounded quotient.
+  constexpr float kInv127 = 1.0f / 127.0f;
+  const float q0 = __fmul_rn(am, kInv127);
+  const float scale = __fmaf_rn(__fmaf_rn(-q0, 127.f, am), kInv127, q0);
   // code = rint(x / scale) on the IEEE-rounded quotient.  x * rcp, with rcp
   // the hardware reciprocal (within 1 ulp), is within 3.1e-5 of that quotient
   // (|quotient| <= 127.5), so where it is farther than 1e-4 from a
   // half-integer both round the same way; near one the division itself
   // decides.  |code| <= 127 without a clamp: |x| <= absmax and scale =
-  // RN(absmax / 127), so |x / scale| <= 127 (1 + 2^-23).
+  // RN(absmax / 127), so |x / scale| <= 127 (1 + 2^-23).  Adding 1.5 * 2^23
+  // rounds a value of magnitude < 2^22 to an integer, ties to even, and the
+  // sum's low byte is that integer's two's complement byte: the code.
   float rcp = 0.f;
   if (scale > 0.f) asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rcp) : "f"(scale));
-  int c[8];
+  constexpr float kRound = 12582912.f;  // 1.5 * 2^23
+  uint32_t f[8];
+  float dmax = 0.f;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const float2 q = mul2(make_float2(x[2 * e], x[2 * e + 1]), make_float2(rcp, rcp));
-    float r0 = rintf(q.x), r1 = rintf(q.y);
-    const float2 d = add2(q, make_float2(-r0, -r1));
-    if (fabsf(d.x) > 0.4999f) r0 = rintf(__fdiv_rn(x[2 * e], scale));
-    if (fabsf(d.y) > 0.4999f) r1 = rintf(__fdiv_rn(x[2 * e + 1], scale));
-    c[2 * e] = (int)r0;
-    c[2 * e + 1] = (int)r1;
+    const float2 fr = add2(q, make_float2(kRound, kRound));
+    const float2 r = add2(fr, make_float2(-kRound, -kRound));
+    const float2 d = add2(q, make_float2(-r.x, -r.y));
+    dmax = max3(dmax, fabsf(d.x), fabsf(d.y));
+    f[2 * e] = __float_as_uint(fr.x);
+    f[2 * e + 1] = __float_as_uint(fr.y);
   }
-  // low bytes of the codes, four to a word
-  const uint32_t lo = __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
-  const uint32_t hi = __byte_perm(__byte_perm(c[4], c[5], 0x0040), __byte_perm(c[6], c[7], 0x0040), 0x5410);
+  // A quotient near a half-integer is rounded from the division (rare), and so
+  // is every quotient of a row with a subnormal scale (absmax < 127 * 2^-126),
+  // whose reciprocal the approximate instruction cannot give.
+  if (dmax > 0.4999f || (scale > 0.f && scale < 1.17549435e-38f)) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = __float_as_uint(rintf(__fdiv_rn(x[e], scale)) + kRound);
+  }
+  // low bytes of the sums, four to a word
+  const uint32_t lo = __byte_perm(__byte_perm(f[0], f[1], 0x0040), __byte_perm(f[2], f[3], 0x0040), 0x5410);
+  const uint32_t hi = __byte_perm(__byte_perm(f[4], f[5], 0x0040), __byte_perm(f[6], f[7], 0x0040), 0x5410);
   scale_out = scale;
   return make_uint2(lo, hi);
 }
