@@ -202,6 +202,18 @@ int pa_decode(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const i
 int pa_plan(int n_q_heads, int n_kv_heads, int n_seq, const pa_seq* seqs, int n_sink_blk, int n_win_blk,
             int32_t* units_out, int cap, int* n_units, long long* n_tiles, int* n_widened_rows);
 
+/* Host-only, no GPU needed: the chunks pa_prefill_host cuts the query rows of
+ * a call into, when the attention kernel runs n_pairs CTA pairs at once (76 on
+ * a 152-SM GB300).  The rows of the sequences laid end to end (seqs order) go
+ * in chunks of two waves of work units (a wave: one unit per pair), the
+ * remainder last; a boundary inside a sequence falls on a multiple of
+ * PA_UNIT_ROWS / G tokens (absolute position), so every work unit lies in one
+ * chunk.  chunk_end (may be NULL) receives up to cap increasing row counts,
+ * the last = the total rows; *n_chunks the count.  PA_EINVAL for bad shapes
+ * or cap < the count. */
+int pa_host_chunks(int n_q_heads, int n_kv_heads, int n_seq, const pa_seq* seqs, int n_pairs, long long* chunk_end,
+                   int cap, int* n_chunks);
+
 /* Debug (tests): run the widening pass, then export sequence `seq`'s widened
  * rows: k_out/v_out int8 [n_kv_heads][n_rows][256], ks_out/vs_out fp32
  * [n_kv_heads][n_rows], tok_out int32 [n_rows] (logical token of each row, -1

@@ -190,3 +190,57 @@ def test_no_product_module_uses_the_oracle():
         for f in files:
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 assert not pat.search(open(os.path.join(dirpath, f)).read()), f
+
+
+def _chunk_cases():
+    rng = np.random.default_rng(5)
+    cases = []
+    for name in ("32k", "chunked", "chunked_ragged", "4k"):
+        wl = CONFIGS[name]
+        offs = np.concatenate([[0], np.cumsum([nq for _, nq in wl.seqs])])
+        desc = np.array([(o, qs, nq, qs + nq) for o, (qs, nq) in zip(offs, wl.seqs)], np.int32)
+        cases.append((name, wl.n_q_heads, wl.n_kv_heads, desc, 76))
+    # unaligned starts, short pieces, several GQA ratios and pair counts
+    for i, (hq, hkv, pairs) in enumerate(((16, 2, 76), (8, 4, 76), (4, 4, 7), (32, 2, 1), (16, 2, 200))):
+        rows, descs = 0, []
+        for _ in range(int(rng.integers(1, 6))):
+            q_start = int(rng.integers(0, 20000))
+            n_q = int(rng.integers(1, 9000))
+            descs.append((rows, q_start, n_q, q_start + n_q + int(rng.integers(0, 50))))
+            rows += n_q
+        cases.append(("random%d" % i, hq, hkv, np.array(descs, np.int32), pairs))
+    return cases
+
+
+@pytest.mark.parametrize("case", _chunk_cases(), ids=lambda c: c[0])
+def test_host_chunks_cut_on_unit_boundaries_and_keep_every_unit_whole(pa, case):
+    """The host-buffer path's chunks (pa_host_chunks, the schedule pa_prefill_host
+    uses): increasing, ending at the total rows, at most two waves of units
+    (+ one unit's rounding) each, a boundary inside a sequence on a multiple of
+    a unit's tokens, and no work unit of the call's plan split between chunks."""
+    _, hq, hkv, seqs, pairs = case
+    ends = pa.pa_host_chunks(hq, hkv, seqs, pairs)
+    n_q = seqs[:, 2].astype(np.int64)
+    base = np.concatenate([[0], np.cumsum(n_q)])
+    total = int(base[-1])
+    ut = pa.UNIT_ROWS // (hq // hkv)
+    wave = max(ut, pairs * ut // hkv)
+    assert ends[-1] == total and np.all(np.diff(ends) > 0)
+    assert np.all(np.diff(np.concatenate([[0], ends])) <= 2 * wave + ut)
+    for e in ends[:-1]:
+        s = int(np.searchsorted(base, e, side="right")) - 1
+        if base[s] < e < base[s + 1]:
+            assert (int(seqs[s, 1]) + int(e - base[s])) % ut == 0
+    units, _, _ = pa.pa_plan(hq, hkv, seqs, 1, 256)
+    for s, _, t0, _ in units:
+        q_start, n = int(seqs[s, 1]), int(seqs[s, 2])
+        lo = base[s] + max(int(t0), q_start) - q_start
+        hi = base[s] + min(int(t0) + ut, q_start + n) - q_start
+        assert lo < hi and not np.any((ends > lo) & (ends < hi)), (s, t0)
+
+
+def test_host_chunks_rejects_bad_shapes(pa):
+    seqs = np.array([[0, 0, 100, 100]], np.int32)
+    for args in ((16, 3, seqs, 76), (16, 2, seqs, 0)):
+        with pytest.raises(pa.PAError):
+            pa.pa_host_chunks(*args)

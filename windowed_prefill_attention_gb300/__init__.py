@@ -31,8 +31,8 @@ PA_P_F16, PA_P_U8 = 0, 1
 
 EXPORTED = ("pa_default_options", "pa_create", "pa_destroy", "pa_prefill", "pa_prefill_batch",
             "pa_prefill_batch_gated", "pa_prefill_host", "pa_kv_append", "pa_decode",
-            "pa_last_error", "pa_timing", "pa_strerror", "pa_plan", "pa_debug_gather", "pa_debug_maskset",
-            "pa_prefill_noalloc")
+            "pa_last_error", "pa_timing", "pa_strerror", "pa_plan", "pa_host_chunks", "pa_debug_gather",
+            "pa_debug_maskset", "pa_prefill_noalloc")
 
 
 class pa_options(C.Structure):
@@ -62,6 +62,7 @@ _lib.pa_strerror.argtypes = [_i]
 _lib.pa_strerror.restype = C.c_char_p
 _lib.pa_plan.argtypes = [_i, _i, _i, C.POINTER(pa_seq), _i, _i, _vp, _i, C.POINTER(_i), C.POINTER(C.c_longlong),
                          C.POINTER(_i)]
+_lib.pa_host_chunks.argtypes = [_i, _i, _i, C.POINTER(pa_seq), _i, _vp, _i, C.POINTER(_i)]
 _lib.pa_debug_gather.argtypes = ([_vp, _i, C.POINTER(pa_seq)] + [_vp] * 5 + [_i, _i, _i] + [_vp] * 5
                                  + [_i, C.POINTER(_i), _vp])
 _lib.pa_debug_maskset.argtypes = [_vp, _i, C.POINTER(pa_seq), _i, _i, _vp, _vp, _i, _vp, _i, C.POINTER(_i), _vp]
@@ -235,6 +236,17 @@ def pa_plan(n_q_heads, n_kv_heads, seqs, n_sink_blk, n_win_blk):
     _check(_lib.pa_plan(n_q_heads, n_kv_heads, len(s), s, n_sink_blk, n_win_blk, units.ctypes.data_as(C.c_void_p),
                         n_units.value, C.byref(n_units), C.byref(n_tiles), C.byref(n_rows)), "pa_plan")
     return units, n_tiles.value, n_rows.value
+
+
+def pa_host_chunks(n_q_heads, n_kv_heads, seqs, n_pairs):
+    """Host-only: the chunk ends (rows of the sequences laid end to end) of pa_prefill_host."""
+    s = _seqs(seqs)
+    n = C.c_int()
+    _check(_lib.pa_host_chunks(n_q_heads, n_kv_heads, len(s), s, n_pairs, None, 0, C.byref(n)), "pa_host_chunks")
+    ends = np.zeros(n.value, dtype=np.int64)
+    _check(_lib.pa_host_chunks(n_q_heads, n_kv_heads, len(s), s, n_pairs, ends.ctypes.data_as(C.c_void_p), n.value,
+                               C.byref(n)), "pa_host_chunks")
+    return ends
 
 
 def pa_debug_gather(h, seqs, k_pool, v_pool, k_scale, v_scale, block_table, n_sink_blk, n_win_blk, seq, cap,

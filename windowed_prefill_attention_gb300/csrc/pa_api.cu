@@ -106,6 +106,44 @@ int build_plan(int HQ, int HKV, int n_seq, const pa_seq* seqs, int S, int W, int
 
 bool same_plan_key(const std::vector<int>& a, const std::vector<int>& b) { return a == b; }
 
+// The host-buffer path's chunks: ends (rows of the sequences laid end to end)
+// of chunks of two waves of work units (a wave: one unit for every one of the
+// n_pairs SM pairs the kernel runs at once; a part-filled wave leaves pairs
+// idle), the remainder last.  Short chunks shorten the copy-in before the
+// first one and the copy-out after the last; one or two waves measured best
+// at 32k tokens.  A boundary inside a sequence moves to a multiple of a
+// unit's tokens (down, or up to the sequence's end when that would empty the
+// piece), so every unit lies in one chunk.  ends is increasing, last = total rows.
+int host_chunk_ends(int HQ, int HKV, int n_seq, const pa_seq* seqs, int n_pairs, std::vector<long long>& ends) {
+  if (HQ <= 0 || HKV <= 0 || HQ % HKV != 0 || kUnitRows % (HQ / HKV) != 0) return PA_EINVAL;
+  if (n_seq <= 0 || seqs == nullptr || n_pairs <= 0) return PA_EINVAL;
+  std::vector<long long> base(n_seq + 1, 0);  // first row of each sequence, end to end
+  for (int s = 0; s < n_seq; ++s) {
+    if (seqs[s].n_q < 1 || seqs[s].q_start < 0) return PA_EINVAL;
+    base[s + 1] = base[s] + seqs[s].n_q;
+  }
+  const long long T = base[n_seq];
+  const long long UT = kUnitRows / (HQ / HKV);  // tokens per unit
+  const long long wave = std::max(UT, (long long)n_pairs * UT / HKV);
+  std::vector<long long> cuts;
+  for (long long at = 0; at < T;) {
+    at = std::min(T, at + 2 * wave);
+    cuts.push_back(at);
+  }
+  ends.clear();
+  for (long long cut : cuts) {
+    const int s = (int)(std::upper_bound(base.begin(), base.end(), cut) - base.begin()) - 1;
+    if (s >= 0 && s < n_seq && cut != base[s]) {  // inside sequence s
+      const long long abs_pos = seqs[s].q_start + (cut - base[s]);
+      long long r = abs_pos / UT * UT;
+      if (r <= seqs[s].q_start) r = std::min((long long)seqs[s].q_start + seqs[s].n_q, (abs_pos / UT + 1) * UT);
+      cut = base[s] + (r - seqs[s].q_start);
+    }
+    if (ends.empty() || cut > ends.back()) ends.push_back(cut);
+  }
+  return PA_OK;
+}
+
 }  // namespace
 
 struct pa_ctx {
@@ -620,30 +658,11 @@ int pa_prefill_host(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, c
   for (int i = 0; i < 7; ++i)
     if ((rc = grow_bytes(h->hb[i], h->hb_cap[i], bytes[i]))) return rc;
 
-  // chunk boundaries on the sequences' rows laid end to end: chunks of two
-  // waves of work units (a wave: one unit for every SM pair the kernel runs
-  // at once; a part-filled wave leaves pairs idle), the remainder last.  Short
-  // chunks shorten the copy-in before the first one and the copy-out after
-  // the last; one or two waves measured best at 32k tokens.  A boundary
-  // inside a sequence moves to a multiple of a unit's tokens.
+  // chunk boundaries on the sequences' rows laid end to end
   std::vector<long long> base(n_seq + 1, 0);  // first row of each sequence, end to end
   for (int s = 0; s < n_seq; ++s) base[s + 1] = base[s] + seqs[s].n_q;
-  const long long T = base[n_seq];
-  const long long UT = kUnitRows / h->G;  // tokens per unit
-  const long long wave = std::max(UT, (long long)pa::attention_pairs(h->n_sm) * UT / h->HKV);
-  std::vector<long long> cuts;  // chunk ends, end to end
-  for (long long at = 0; at < T;) {
-    at = std::min(T, at + 2 * wave);
-    cuts.push_back(at);
-  }
-  for (long long& cut : cuts) {  // inside a sequence: down (or up) to a multiple of UT tokens
-    const int s = (int)(std::upper_bound(base.begin(), base.end(), cut) - base.begin()) - 1;
-    if (s < 0 || s >= n_seq || cut == base[s]) continue;
-    const long long abs_pos = seqs[s].q_start + (cut - base[s]);
-    long long r = abs_pos / UT * UT;
-    if (r <= seqs[s].q_start) r = std::min((long long)seqs[s].q_start + seqs[s].n_q, (abs_pos / UT + 1) * UT);
-    cut = base[s] + (r - seqs[s].q_start);
-  }
+  std::vector<long long> cuts;
+  if ((rc = host_chunk_ends(h->HQ, h->HKV, n_seq, seqs, pa::attention_pairs(h->n_sm), cuts))) return rc;
   std::vector<std::vector<pa_seq>> chunks;  // per chunk, its pieces of the sequences (rows, same context)
   std::vector<long long> ends;  // chunk ends, end to end
   long long lo = 0;
@@ -840,6 +859,19 @@ int pa_plan(int n_q_heads, int n_kv_heads, int n_seq, const pa_seq* seqs, int n_
       units_out[4 * i + 2] = P.units[i].t0;
       units_out[4 * i + 3] = P.units[i].n_tiles;
     }
+  }
+  return PA_OK;
+}
+
+int pa_host_chunks(int n_q_heads, int n_kv_heads, int n_seq, const pa_seq* seqs, int n_pairs, long long* chunk_end,
+                   int cap, int* n_chunks) {
+  std::vector<long long> ends;
+  const int rc = host_chunk_ends(n_q_heads, n_kv_heads, n_seq, seqs, n_pairs, ends);
+  if (rc) return rc;
+  if (n_chunks) *n_chunks = (int)ends.size();
+  if (chunk_end) {
+    if ((int)ends.size() > cap) return PA_EINVAL;
+    std::copy(ends.begin(), ends.end(), chunk_end);
   }
   return PA_OK;
 }
