@@ -201,8 +201,9 @@ __device__ __forceinline__ uint2 quantise_row8(const uint4 raw, float am, float&
   return make_uint2(lo, hi);
 }
 
+// Six blocks per SM (40 registers): more warps to cover the loads; measured
+// ~5 % faster than the five that 43 registers allow.
 template <int HKV>
-// six blocks per SM (40 registers): more warps to cover the loads; measured ~5 % faster than five
 __global__ void __launch_bounds__(kAppendWarps * 32, 6) kv_append_kernel(const KvAppendParams p) {
   const int i = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);  // new token
   const int lane = threadIdx.x & 31;
