@@ -14,10 +14,12 @@
  *     K_j = k_pool code * k_scale,  V_j = v_pool code * v_scale   (per token, per kv head)
  *     out[t][h] = softmax_j(sm_scale * <q[t][h], K_j>) . V_j     over visible j
  *
- * computed with the pages' method: the query quantised per row in a fused
- * prologue, per-row Q / per-token K / softmax scales applied to the integer-
- * valued scores, an online softmax over key tiles that skips masked blocks,
- * and the per-token V scale folded into P before P is quantised per row.
+ * computed along the pages' method: per-row Q / per-token K / softmax scales
+ * applied to the scores of integer-valued K codes, an online softmax over key
+ * tiles that skips masked blocks, and the per-token V scale folded into P.  By
+ * default the query enters the tensor core as given (bf16) and P' = p * v_scale
+ * is held in fp16; the pages' per-row int8 query and u8 P grids are options
+ * (PA_Q_INT8, PA_P_U8 below).
  *
  * Layouts (all row-major, C order):
  *   q, out        bf16  [total_q][n_q_heads][256]          16-byte aligned
