@@ -269,6 +269,58 @@ def test_f16_p_rounding_is_exact_on_dyadic_values():
     assert norm_err(b, a).max() < 1e-12
 
 
+def _fp16_grid_values(rng):
+    """fp32 values over the binary16 normal range [2^-14, 65504]: grid points,
+    exact half-way points between neighbours (even and odd lower neighbour),
+    the fp32 values either side of each half-way point, and random fp32
+    values of every binade."""
+    vals = []
+    for e in range(-14, 16):
+        ulp = 2.0 ** (e - 10)
+        m = rng.integers(1024, 2048, size=24)
+        m[:2] = (1024, 2046)  # an even and (with +1 below) odd lower neighbour at the binade's ends
+        grid = m * ulp
+        half = grid + ulp / 2
+        vals += [grid, half, (m + 1) * ulp + ulp / 2]
+        h32 = half.astype(np.float32)
+        vals += [np.nextafter(h32, np.float32(np.inf)), np.nextafter(h32, np.float32(0))]
+        vals.append(rng.uniform(2.0 ** e, 2.0 ** (e + 1), size=24))
+    v = np.concatenate(vals).astype(np.float32)
+    return v[(v >= np.float32(2.0 ** -14)) & (v <= np.float32(65504.0))]
+
+
+def test_f16_p_rounding_is_ieee_binary16_nearest_even():
+    """The method's fp16 container for P' (P_F16) against IEEE binary16
+    round-to-nearest-even (numpy's float32 -> float16 cast) over the fp16
+    normal range, through the whole P_F16 path: one-token sequences see one
+    key, so p = 1 and P' = v_scale, and a V code of 1 (-1) in dim 0 (1) puts
+    the rounded P' in the output.  Ties must go to the even neighbour: 10
+    significant bits, truncation or ties-away each fail."""
+    rng = np.random.default_rng(16)
+    vs = _fp16_grid_values(rng)
+    n = vs.shape[0]
+    D = 256
+    q = np.full((n, 1, D), 0x3F80, dtype=np.uint16)  # bf16 1.0
+    kp = np.ones((n, 16, 1, D), dtype=np.int8)
+    vp = np.zeros((n, 16, 1, D), dtype=np.int8)
+    vp[:, :, 0, 0] = 1
+    vp[:, :, 0, 1] = -1
+    ks = np.full((n, 16, 1), 0.01, dtype=np.float32)
+    v_scale = np.zeros((n, 16, 1), dtype=np.float32)
+    v_scale[:, 0, 0] = vs
+    bt = np.arange(n, dtype=np.int32)[:, None]
+    seqs = np.stack([np.arange(n), np.zeros(n), np.ones(n), np.ones(n)], 1).astype(np.int32)
+    prob = oracle.Problem(q, kp, vp, ks, v_scale, bt, seqs, 0, 0, 1.0 / 16)
+    rows = np.stack([np.arange(n), np.zeros(n)], 1).astype(np.int32)
+    out = oracle.method(prob, rows, oracle.Q_LOSSLESS, oracle.P_F16, tile=64)
+    want = vs.astype(np.float16).astype(np.float64)
+    assert np.isfinite(want).all()
+    assert np.array_equal(out[:, 0], want)
+    assert np.array_equal(out[:, 1], -want)
+    # the grid really holds cases that tell the roundings apart
+    assert (want != vs.astype(np.float64)).sum() > n // 3
+
+
 def test_gate_against_library_sigmoid_and_special_values():
     """The output gate (out * sigmoid(g)) against scipy's logistic function on
     random values and on the special points: sigmoid(0) = 1/2 exactly, the
