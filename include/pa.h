@@ -76,6 +76,10 @@ typedef struct {
   int debug_stall;      /* test hook: nonzero makes the attention kernel's first wait target a
                            barrier nothing arrives at, so the bounded wait runs out, the kernel
                            exits cleanly and pa_last_error reports PA_ETIMEOUT; 0 in normal use */
+  int debug_fail_host;  /* test hook: nonzero makes pa_prefill_host fail as if a CUDA call had
+                           failed while it was still enqueuing (after the pool's and the first
+                           chunks' copies were issued), to test that it drains its copies before
+                           returning PA_ECUDA; 0 in normal use */
 } pa_options;
 
 typedef struct {
@@ -85,7 +89,7 @@ typedef struct {
   int n_ctx;    /* context tokens in the pool; q_start + n_q <= n_ctx */
 } pa_seq;
 
-/* Fill *opt with the defaults (bf16 query as given, fp16 P', 2000 ms waits, no timing, no test hook). */
+/* Fill *opt with the defaults (bf16 query as given, fp16 P', 2000 ms waits, no timing, no test hooks). */
 void pa_default_options(pa_options* opt);
 
 /* Create a handle bound to the current CUDA device.  head_dim must be 256 and
@@ -133,10 +137,26 @@ int pa_prefill_batch_gated(pa_handle h, int n_seq, const pa_seq* seqs, const voi
  * rows copied out on two copy streams the handle owns.  The result is the one
  * pa_prefill_batch gives on device copies of the same buffers.
  * Output rows that belong to no sequence are left as they were.  Pinned host
- * memory is fastest (pageable memory makes the copies synchronous). */
+ * memory is fastest (pageable memory makes the copies synchronous).
+ * Every call copies the whole pool, scales and block table in again (the
+ * handle keeps no copy of host data between calls).
+ * Waits: the attention launch of a chunk after the first waits on the device
+ * for a flag the copy stream writes once that chunk's rows are in; that wait
+ * has the same bound as every device wait (pa_options.wait_timeout_ms, 2 s by
+ * default), measured from the launch's start, so a copy link slower than
+ * about (chunk rows x n_q_heads x 512 bytes) per bound can end the call with
+ * PA_ETIMEOUT: raise wait_timeout_ms for slow links or pageable memory.
+ * Failure: once the first copy is issued, a failing CUDA call makes the
+ * function wait for both copy streams and `stream` before returning its
+ * error, so no copy reads the caller's buffers or writes `out` afterwards. */
 int pa_prefill_host(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* k_pool,
                     const int8_t* v_pool, const float* k_scale, const float* v_scale, const int32_t* block_table,
                     int n_sink_blk, int n_win_blk, float sm_scale, void* out, void* stream);
+
+/* Debug (tests): 1 if the handle's two copy streams (those of
+ * pa_prefill_host) have no work pending, 0 if either still has, PA_EINVAL
+ * for a NULL handle, PA_ECUDA if a stream reports an error.  Does not wait. */
+int pa_debug_copy_streams_idle(pa_handle h);
 
 /* Synchronise `stream`, then report and clear the first device-side error
  * recorded since the last call (PA_ETIMEOUT, PA_EBADPAGE) or PA_ECUDA. */
@@ -235,6 +255,20 @@ int pa_debug_maskset(pa_handle h, int n_seq, const pa_seq* seqs, int n_sink_blk,
                      int32_t* row_counts, int32_t* unit_blocks, int cap, int32_t* units_out, int units_cap,
                      int* n_units, void* stream);
 
+/* Debug (tests): the per-row int8 query grid of the fused prologue ("int8
+ * tensor-core prefill attention", section "Why the attention, and why tensor
+ * cores": Q is quantised per query row with one scale per row), run by the
+ * attention kernel's own quantiser on n_rows rows staged as its Q tile holds
+ * them.  Per row: absmax over the 256 values, scale = absmax / 127 and codes
+ * rint(q * (127 / absmax)) half to even, clamped to [-127, 127], every
+ * decision in fp32 (IEEE divisions); an all-zero row gets scale 0 and codes 0.
+ *   q_rows  device bf16 [n_rows][256], 16-byte aligned (caller-owned, read)
+ *   codes   device int8 [n_rows][256], 4-byte aligned (written)
+ *   scales  device fp32 [n_rows] (written)
+ * Synchronous on `stream`.  PA_EINVAL for a negative count, NULL or misaligned
+ * pointers; PA_ECUDA if the launch fails. */
+int pa_debug_qcodes(const void* q_rows, int n_rows, int8_t* codes, float* scales, void* stream);
+
 /* Allocation-free variant of pa_prefill (one sequence, default
  * containers).  The pages have no counterpart of this entry point: it exists
  * for callers that may not call cudaMalloc / cudaFree, for example an engine
@@ -253,11 +287,20 @@ int pa_debug_maskset(pa_handle h, int n_seq, const pa_seq* seqs, int n_sink_blk,
  *
  * All calls share the one array and each call clears what must start at
  * zero, so calls on different streams, or from different threads, that
- * overlap on the GPU race and corrupt each other: serialise them.  The first
- * call on a device looks up the array's device address (cudaGetSymbolAddress)
- * with that device current, so make the first call before any stream
- * capture.  The call is synchronous: it waits for `stream` and returns the
- * device-side status (PA_ETIMEOUT, PA_EBADPAGE) of this call. */
+ * overlap on the GPU race and corrupt each other: serialise them.
+ *
+ * Set-up: the first call on a device (and the first after that device's
+ * context was reset, which reloads the module) looks up the array's device
+ * address with cudaGetSymbolAddress and reads the device's compute capability
+ * and SM count, with that device current; that first call should come before
+ * any stream capture.  Later calls reuse what it found.
+ *
+ * The work list has the order pa_plan gives (longest units first).  The call
+ * is synchronous: after enqueuing its kernels on `stream` it reads this
+ * call's device-side status word on `stream` and waits for `stream` alone,
+ * returning PA_ETIMEOUT or PA_EBADPAGE from the device.  PA_EINVAL for the
+ * argument errors of pa_create / pa_prefill, including q_start + n_q or n_ctx
+ * above 2^30. */
 #define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
 int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_pages, int max_pages_per_seq, const void* q,
                        const int8_t* k_pool, const int8_t* v_pool, const float* k_scale, const float* v_scale,

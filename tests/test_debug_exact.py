@@ -102,3 +102,60 @@ def test_maskset_is_bit_exact(case):
             t = t0 + r // G
             if q_start <= t < q_start + n_q:
                 assert counts[u, r] == oracle.visible_count(t, wl.n_sink_blk, wl.n_win_blk), (case, u, r)
+
+
+def _bf16_bits(x):
+    b = np.asarray(x, dtype=np.float32).view(np.uint32)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)  # round to nearest even
+
+
+def _qcode_rows():
+    """bf16 query rows (bit patterns [n, 256]) that exercise the per-row int8
+    grid: random normal rows and rows with outliers; rows whose quotients
+    q * 127/absmax fall exactly on half-integers (absmax 127 gives 127/absmax
+    = 1, absmax 63.5 gives 2: ties to even, both signs, even and odd
+    integer parts); an all-zero row; rows holding +absmax and -absmax; a row
+    with one non-zero value; tiny and huge magnitudes."""
+    rng = np.random.default_rng(61)
+    rows = [rng.normal(size=(200, 256)).astype(np.float32)]
+    o = rng.normal(size=(40, 256)).astype(np.float32)
+    o[np.arange(40), rng.integers(0, 256, 40)] *= 40.0
+    rows.append(o)
+    k = rng.integers(0, 127, size=(8, 256)).astype(np.float32) + 0.5
+    k *= rng.choice([-1.0, 1.0], size=k.shape).astype(np.float32)
+    k[:, 0] = 127.0
+    rows.append(k)                                      # quotient = q exactly: k + 0.5 ties
+    rows.append(k / np.float32(2.0))                    # absmax 63.5: quotient 2 q, again k + 0.5
+    rows.append(np.zeros((1, 256), np.float32))         # all zero
+    pm = rng.normal(size=(2, 256)).astype(np.float32)
+    pm[:, 3], pm[:, 9] = 5.0, -5.0                      # +absmax and -absmax in one row
+    rows.append(pm)
+    one = np.zeros((2, 256), np.float32)
+    one[0, 17], one[1, 200] = -0.7, 3e-3
+    rows.append(one)
+    rows.append(rng.normal(size=(3, 256)).astype(np.float32) * np.float32([[1e-30], [1e30], [1e-3]]))
+    return _bf16_bits(np.concatenate(rows))
+
+
+def test_q_int8_codes_are_bit_exact():
+    """The attention prologue's int8 query grid (PA_Q_INT8), run by the kernel's
+    own quantiser, gives the oracle's codes and scales bit for bit: both decide
+    in fp32 with IEEE divisions.  More than 128 rows, so several CTAs and a
+    ragged last one."""
+    import torch
+
+    import windowed_prefill_attention_gb300 as pa
+    bits = _qcode_rows()
+    q = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    codes, scales = pa.pa_debug_qcodes(q)
+    codes, scales = codes.cpu().numpy(), scales.cpu().numpy()
+    for i in range(bits.shape[0]):
+        want_c, want_s = oracle.quantize_q_row(bits[i])
+        assert np.array_equal(codes[i], want_c), i
+        assert scales[i].view(np.uint32) == np.float32(want_s).view(np.uint32), i
+    # the half-way rows really are ties, decided to even
+    tie = bits[240:248]
+    assert np.all(np.abs(codes[240:248, 1:]) % 2 == 0)
+    assert np.all(np.abs(codes[248:256, 1:]) % 2 == 0)
+    assert tie.shape[0] == 8
+    assert not codes[256].any() and scales[256] == 0.0

@@ -75,3 +75,43 @@ def test_invalid_calls_are_rejected_before_launch():
         assert pa.pa_last_error(h) == pa.PA_OK
     finally:
         pa.pa_destroy(h)
+
+
+def test_host_path_drains_its_copies_before_returning_an_error():
+    """pa_prefill_host on the 32k workload (about 300 MB of pinned input, a
+    millisecond or more of copies) with the test hook that fails the call
+    while it is still enqueuing, after the pool's and the first chunks'
+    copies were issued: the call returns PA_ECUDA only once both copy streams
+    are idle, so none of them still reads the caller's buffers.  The handle
+    then serves a normal call with the same result as the device entry point."""
+    import torch
+
+    import windowed_prefill_attention_gb300 as pa
+    from synth import CONFIGS, make_inputs
+    inp = make_inputs(CONFIGS["32k"])
+    wl = inp.wl
+    pin = lambda a: torch.from_numpy(a).pin_memory()  # noqa: E731
+    hq = torch.from_numpy(inp.q.view(np.int16)).pin_memory()
+    hk, hv, hks, hvs, hbt = (pin(inp.k_pool), pin(inp.v_pool), pin(inp.k_scale), pin(inp.v_scale),
+                             pin(inp.block_table))
+    hout = torch.empty_like(hq).pin_memory()
+    args = (inp.seq_desc, hq, hk, hv, hks, hvs, hbt, wl.n_sink_blk, wl.n_win_blk, wl.sm_scale, hout)
+    h = pa.pa_create(wl.n_q_heads, wl.n_kv_heads, inp.k_pool.shape[0], inp.block_table.shape[1],
+                     debug_fail_host=True)
+    try:
+        for _ in range(2):
+            with pytest.raises(pa.PAError) as ei:
+                pa.pa_prefill_host(h, *args)
+            assert ei.value.code == pa.PA_ECUDA
+            assert pa.pa_debug_copy_streams_idle(h)
+    finally:
+        pa.pa_destroy(h)
+    h = pa.pa_create(wl.n_q_heads, wl.n_kv_heads, inp.k_pool.shape[0], inp.block_table.shape[1])
+    try:
+        pa.pa_prefill_host(h, *args)
+        assert pa.pa_debug_copy_streams_idle(h)
+    finally:
+        pa.pa_destroy(h)
+    b = hout.view(torch.bfloat16).float().numpy()
+    a, rc = run_gpu(inp)
+    assert rc == 0 and np.array_equal(a, b)

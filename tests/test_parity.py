@@ -127,6 +127,13 @@ EDGE = {
     "gqa_16": (Workload("e_g16", 32, 2, ((0, 500),), 1, 4, seed=42), 1, 4),
     "many_sequences": (Workload("e_many", 16, 2, ((0, 16), (100, 1), (7, 300), (2000, 64), (33, 33)), 1, 4,
                                 seed=43, outlier_frac=0.05), 1, 4),
+    # the widest groups pa_create accepts: 4, 2 and 1 tokens per CTA (Q boxes {64, G, 128 / G})
+    "gqa_32": (Workload("e_g32", 64, 2, ((0, 300),), 1, 4, seed=46, outlier_frac=0.02), 1, 4),
+    "gqa_64": (Workload("e_g64", 64, 1, ((5, 203),), 1, 3, seed=47), 1, 3),
+    "gqa_128": (Workload("e_g128", 128, 1, ((0, 150),), 1, 2, seed=48), 1, 2),
+    # the most kv heads pa_create accepts
+    "kv_heads_8": (Workload("e_h8", 64, 8, ((0, 400),), 1, 4, seed=49, outlier_frac=0.02), 1, 4),
+    "kv_heads_8_gqa_16": (Workload("e_h8g16", 128, 8, ((3, 120), (40, 77)), 2, 3, seed=50), 2, 3),
 }
 
 

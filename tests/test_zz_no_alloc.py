@@ -5,8 +5,11 @@ that has reserved nearly all device memory for its own KV-cache pool, or a
 latency-critical path where an allocation is not allowed).  Its scratch is a
 static device array shared by every call, so these tests call it several
 times in a row, on different shapes, and check each output against the
-handle-based pa_prefill within the tolerance the parity tests use.  The file
-is named so that pytest collects it last.
+handle-based entry point.  Both run the same widening and attention kernels
+on the same work units (each unit's output depends on that unit alone), so
+the outputs are equal bit for bit; a wrong stride in how the static array is
+carved up would show as a difference.  The file is named so that pytest
+collects it last.
 """
 import ctypes as C
 
@@ -56,6 +59,7 @@ def test_noalloc_matches_handle_entry_point_on_consecutive_calls():
             assert np.isfinite(got).all()
             mx, mean = norm_errors(got.astype(np.float64), ref.astype(np.float64))
             assert mx <= TOL_MAX and mean <= TOL_MEAN, (wl.name, mx, mean)
+            assert np.array_equal(got, ref), wl.name
 
 
 def test_noalloc_rejects_contexts_beyond_its_scratch():
@@ -71,3 +75,10 @@ def test_noalloc_rejects_contexts_beyond_its_scratch():
                                     ptr(d["block_table"]), 0, big, big, 0, 0, C.c_float(0.0625), ptr(d["q"]), None)
     assert rc == pa.PA_ENOSCRATCH
     assert "scratch" in pa.pa_strerror(rc)
+    # positions past 2^30 are rejected before any arithmetic on them
+    for q_start, n_q, n_ctx in ((2 ** 30 - 5, 10, 2 ** 30 + 5), (2 ** 31 - 8, 4, 2 ** 31 - 1)):
+        rc = pa._lib.pa_prefill_noalloc(wl.n_q_heads, wl.n_kv_heads, inp.k_pool.shape[0], 2 ** 27,
+                                        ptr(d["q"]), ptr(d["k_pool"]), ptr(d["v_pool"]), ptr(d["k_scale"]),
+                                        ptr(d["v_scale"]), ptr(d["block_table"]), q_start, n_q, n_ctx, 0, 0,
+                                        C.c_float(0.0625), ptr(d["q"]), None)
+        assert rc == pa.PA_EINVAL, (q_start, rc)

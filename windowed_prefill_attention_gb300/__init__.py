@@ -32,12 +32,12 @@ PA_P_F16, PA_P_U8 = 0, 1
 EXPORTED = ("pa_default_options", "pa_create", "pa_destroy", "pa_prefill", "pa_prefill_batch",
             "pa_prefill_batch_gated", "pa_prefill_host", "pa_kv_append", "pa_decode",
             "pa_last_error", "pa_timing", "pa_strerror", "pa_plan", "pa_host_chunks", "pa_debug_gather",
-            "pa_debug_maskset", "pa_prefill_noalloc")
+            "pa_debug_maskset", "pa_debug_qcodes", "pa_debug_copy_streams_idle", "pa_prefill_noalloc")
 
 
 class pa_options(C.Structure):
     _fields_ = [("q_mode", C.c_int), ("p_mode", C.c_int), ("wait_timeout_ms", C.c_int), ("record_timing", C.c_int),
-                ("debug_stall", C.c_int)]
+                ("debug_stall", C.c_int), ("debug_fail_host", C.c_int)]
 
 
 class pa_seq(C.Structure):
@@ -66,6 +66,8 @@ _lib.pa_host_chunks.argtypes = [_i, _i, _i, C.POINTER(pa_seq), _i, _vp, _i, C.PO
 _lib.pa_debug_gather.argtypes = ([_vp, _i, C.POINTER(pa_seq)] + [_vp] * 5 + [_i, _i, _i] + [_vp] * 5
                                  + [_i, C.POINTER(_i), _vp])
 _lib.pa_debug_maskset.argtypes = [_vp, _i, C.POINTER(pa_seq), _i, _i, _vp, _vp, _i, _vp, _i, C.POINTER(_i), _vp]
+_lib.pa_debug_qcodes.argtypes = [_vp, _i, _vp, _vp, _vp]
+_lib.pa_debug_copy_streams_idle.argtypes = [_vp]
 _lib.pa_prefill_noalloc.argtypes = [_i] * 4 + [_vp] * 6 + [_i] * 5 + [_f, _vp, _vp]
 
 
@@ -131,8 +133,10 @@ def pa_default_options() -> pa_options:
 
 
 def pa_create(n_q_heads, n_kv_heads, n_pool_pages, max_pages_per_seq, head_dim=256, page_size=16,
-              q_mode=PA_Q_BF16, p_mode=PA_P_F16, wait_timeout_ms=2000, record_timing=False, debug_stall=False):
-    o = pa_options(q_mode, p_mode, wait_timeout_ms, 1 if record_timing else 0, 1 if debug_stall else 0)
+              q_mode=PA_Q_BF16, p_mode=PA_P_F16, wait_timeout_ms=2000, record_timing=False, debug_stall=False,
+              debug_fail_host=False):
+    o = pa_options(q_mode, p_mode, wait_timeout_ms, 1 if record_timing else 0, 1 if debug_stall else 0,
+                   1 if debug_fail_host else 0)
     h = C.c_void_p()
     _check(_lib.pa_create(C.byref(h), n_q_heads, n_kv_heads, head_dim, page_size, n_pool_pages, max_pages_per_seq,
                           C.byref(o)), "pa_create")
@@ -215,6 +219,14 @@ def pa_prefill_noalloc(n_q_heads, n_kv_heads, n_pool_pages, max_pages_per_seq, q
                                    _stream(stream)), "pa_prefill_noalloc")
 
 
+def pa_debug_copy_streams_idle(h) -> bool:
+    """True if the handle's host-path copy streams have no work pending (does not wait)."""
+    r = _lib.pa_debug_copy_streams_idle(h)
+    if r < 0:
+        raise PAError(r, "pa_debug_copy_streams_idle")
+    return r == 1
+
+
 def pa_last_error(h, stream=None) -> int:
     """Synchronise and return the first device-side status since the last call (0 = fine)."""
     return _lib.pa_last_error(h, _stream(stream))
@@ -290,6 +302,17 @@ def pa_debug_maskset(h, seqs, n_sink_blk, n_win_blk, units_cap, cap, stream=None
                                  C.byref(n), _stream(stream)), "pa_debug_maskset")
     k = n.value
     return units[:k], counts[:k], blocks[:k]
+
+
+def pa_debug_qcodes(q_rows, stream=None):
+    """The attention prologue's int8 query grid on bf16 rows [n, 256]: (int8 codes [n, 256], fp32 scales [n])."""
+    import torch
+    n = int(q_rows.shape[0])
+    codes = torch.empty((n, 256), dtype=torch.int8, device=q_rows.device)
+    scales = torch.empty((n,), dtype=torch.float32, device=q_rows.device)
+    _check(_lib.pa_debug_qcodes(_dev(q_rows, torch.bfloat16, "q_rows"), n, C.c_void_p(codes.data_ptr()),
+                                C.c_void_p(scales.data_ptr()), _stream(stream)), "pa_debug_qcodes")
+    return codes, scales
 
 
 class Handle:

@@ -461,6 +461,14 @@ int launch_attention_plan(pa_handle h, const Plan& P, const SeqGeom* d_seqs, con
 // it: mark(0) before the pass, mark(1) after it, mark(2) after the attention.
 struct TimingMarks {
   cudaEvent_t e[3] = {nullptr, nullptr, nullptr};
+  bool queued = false;  // mark(2) handed the events to the pending list
+  // events of a call that failed before its last mark go back to the free list
+  void release(pa_handle h) {
+    if (queued) return;
+    for (auto& x : e)
+      if (x) h->ev_free.push_back(x);
+    e[0] = e[1] = e[2] = nullptr;
+  }
   int init(pa_handle h) {
     if (!h->opt.record_timing) return PA_OK;
     for (auto& x : e)
@@ -470,8 +478,10 @@ struct TimingMarks {
   int mark(pa_handle h, int i, cudaStream_t st) {
     if (!e[i]) return PA_OK;
     PA_CUDA(cudaEventRecord(e[i], st));
-    if (i == 2)
+    if (i == 2) {
       for (auto& x : e) h->ev_pending.push_back(x);
+      queued = true;
+    }
     return PA_OK;
   }
 };
@@ -484,12 +494,12 @@ int launch_plan(pa_handle h, const Plan& P, const SeqGeom* d_seqs, const Unit* d
                 int W, float sm_scale, void* out, cudaStream_t st, const void* gate) {
   TimingMarks tm;
   int rc;
-  if ((rc = tm.init(h)) || (rc = tm.mark(h, 0, st))) return rc;
-  if ((rc = launch_widen_plan(h, P, d_seqs, n_seq, kp, vp, ksc, vsc, bt, sm_scale, st))) return rc;
-  if ((rc = tm.mark(h, 1, st))) return rc;
-  if ((rc = launch_attention_plan(h, P, d_seqs, d_units, (int)P.units.size(), q, S, W, sm_scale, out, st, gate)))
-    return rc;
-  return tm.mark(h, 2, st);
+  if (!(rc = tm.init(h)) && !(rc = tm.mark(h, 0, st)) &&
+      !(rc = launch_widen_plan(h, P, d_seqs, n_seq, kp, vp, ksc, vsc, bt, sm_scale, st)) && !(rc = tm.mark(h, 1, st)) &&
+      !(rc = launch_attention_plan(h, P, d_seqs, d_units, (int)P.units.size(), q, S, W, sm_scale, out, st, gate)))
+    rc = tm.mark(h, 2, st);
+  if (rc) tm.release(h);
+  return rc;
 }
 
 int run(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* kp, const int8_t* vp,
@@ -515,6 +525,7 @@ void pa_default_options(pa_options* opt) {
   opt->wait_timeout_ms = 2000;
   opt->record_timing = 0;
   opt->debug_stall = 0;
+  opt->debug_fail_host = 0;
 }
 
 const char* pa_strerror(int code) {
@@ -752,59 +763,89 @@ int pa_prefill_host(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, c
   cudaEvent_t* ev_in = h->pipe_ev.data() + 3;           // chunk c's q rows are in
   cudaEvent_t* ev_done = h->pipe_ev.data() + 3 + n_ch;  // chunk c is computed
 
-  // inputs: after whatever the caller's stream did before
-  PA_CUDA(cudaEventRecord(ev_start, st));
-  PA_CUDA(cudaStreamWaitEvent(h->s_h2d, ev_start, 0));
-  for (int i = 1; i < 6; ++i) PA_CUDA(cudaMemcpyAsync(h->hb[i], src[i], bytes[i], cudaMemcpyHostToDevice, h->s_h2d));
-  PA_CUDA(cudaEventRecord(ev_pool, h->s_h2d));
-  for (int c = 0; c < n_ch; ++c) {
-    for (const pa_seq& pc : chunks[c]) {
-      const size_t off = (size_t)pc.q_off * row_bytes;
-      PA_CUDA(cudaMemcpyAsync(static_cast<char*>(h->hb[0]) + off, static_cast<const char*>(q) + off,
-                              (size_t)pc.n_q * row_bytes, cudaMemcpyHostToDevice, h->s_h2d));
-    }
-    PA_CUDA(cudaEventRecord(ev_in[c], h->s_h2d));
-    if (write_value && c > 0 &&
-        write_value(h->s_h2d, (CUdeviceptr)(h->d_qflags + c), epoch, CU_STREAM_WRITE_VALUE_DEFAULT) != CUDA_SUCCESS)
-      return PA_ECUDA;
-  }
-  // widen the whole pool once it is in, then compute each chunk once its rows
-  // are in; copy its output out behind it
-  PA_CUDA(cudaStreamWaitEvent(h->s_d2h, ev_start, 0));
-  PA_CUDA(cudaStreamWaitEvent(st, ev_pool, 0));
+  // From the first copy on, the caller's host buffers are in use by copies on
+  // the handle's streams: on any failure the call drains those streams (and
+  // `stream`) before it returns, so no copy still reads q or the pool, or
+  // writes out, once the caller gets control back.  Every chunk's row flag is
+  // written before the first chunk launch, so the drain always ends.
   TimingMarks tm;
-  if (!(rc = tm.init(h)) && !(rc = tm.mark(h, 0, st)))
-    rc = launch_widen_plan(h, P, h->d_pseqs, n_seq, static_cast<const int8_t*>(h->hb[1]),
-                           static_cast<const int8_t*>(h->hb[2]), static_cast<const float*>(h->hb[3]),
-                           static_cast<const float*>(h->hb[4]), static_cast<const int32_t*>(h->hb[5]), sm_scale, st);
-  if (!rc) rc = tm.mark(h, 1, st);
-  bool after_attn = false;  // the last launch on st is an attention launch of this call
-  for (int c = 0; c < n_ch && !rc; ++c) {
-    const bool on_device = write_value && c > 0 && after_attn;
-    if (!on_device) PA_CUDA(cudaStreamWaitEvent(st, ev_in[c], 0));
-    if (!cunits[c].empty()) {
-      if ((rc = launch_attention_plan(h, P, h->d_pseqs, h->d_punits + off_u[c], (int)cunits[c].size(), h->hb[0],
-                                      n_sink_blk, n_win_blk, sm_scale, h->hb[6], st, nullptr, on_device,
-                                      on_device ? h->d_qflags + c : nullptr, epoch)))
-        break;
-      after_attn = true;
+  auto enqueue = [&]() -> int {
+    // inputs: after whatever the caller's stream did before
+    PA_CUDA(cudaEventRecord(ev_start, st));
+    PA_CUDA(cudaStreamWaitEvent(h->s_h2d, ev_start, 0));
+    for (int i = 1; i < 6; ++i) PA_CUDA(cudaMemcpyAsync(h->hb[i], src[i], bytes[i], cudaMemcpyHostToDevice, h->s_h2d));
+    PA_CUDA(cudaEventRecord(ev_pool, h->s_h2d));
+    for (int c = 0; c < n_ch; ++c) {
+      for (const pa_seq& pc : chunks[c]) {
+        const size_t off = (size_t)pc.q_off * row_bytes;
+        PA_CUDA(cudaMemcpyAsync(static_cast<char*>(h->hb[0]) + off, static_cast<const char*>(q) + off,
+                                (size_t)pc.n_q * row_bytes, cudaMemcpyHostToDevice, h->s_h2d));
+      }
+      PA_CUDA(cudaEventRecord(ev_in[c], h->s_h2d));
+      // test hook: a failure of the enqueue after the pool and the first rows are in flight
+      if (h->opt.debug_fail_host && c == std::min(1, n_ch - 1)) return PA_ECUDA;
+      if (write_value && c > 0 &&
+          write_value(h->s_h2d, (CUdeviceptr)(h->d_qflags + c), epoch, CU_STREAM_WRITE_VALUE_DEFAULT) != CUDA_SUCCESS)
+        return PA_ECUDA;
     }
-    PA_CUDA(cudaEventRecord(ev_done[c], st));
-    PA_CUDA(cudaStreamWaitEvent(h->s_d2h, ev_done[c], 0));
-    for (const pa_seq& pc : chunks[c]) {
-      const size_t off = (size_t)pc.q_off * row_bytes;
-      PA_CUDA(cudaMemcpyAsync(static_cast<char*>(out) + off, static_cast<const char*>(h->hb[6]) + off,
-                              (size_t)pc.n_q * row_bytes, cudaMemcpyDeviceToHost, h->s_d2h));
+    // widen the whole pool once it is in, then compute each chunk once its rows
+    // are in; copy its output out behind it
+    PA_CUDA(cudaStreamWaitEvent(h->s_d2h, ev_start, 0));
+    PA_CUDA(cudaStreamWaitEvent(st, ev_pool, 0));
+    int r = PA_OK;
+    if (!(r = tm.init(h)) && !(r = tm.mark(h, 0, st)))
+      r = launch_widen_plan(h, P, h->d_pseqs, n_seq, static_cast<const int8_t*>(h->hb[1]),
+                            static_cast<const int8_t*>(h->hb[2]), static_cast<const float*>(h->hb[3]),
+                            static_cast<const float*>(h->hb[4]), static_cast<const int32_t*>(h->hb[5]), sm_scale, st);
+    if (!r) r = tm.mark(h, 1, st);
+    if (r) return r;
+    bool after_attn = false;  // the last launch on st is an attention launch of this call
+    for (int c = 0; c < n_ch; ++c) {
+      const bool on_device = write_value && c > 0 && after_attn;
+      if (!on_device) PA_CUDA(cudaStreamWaitEvent(st, ev_in[c], 0));
+      if (!cunits[c].empty()) {
+        if ((r = launch_attention_plan(h, P, h->d_pseqs, h->d_punits + off_u[c], (int)cunits[c].size(), h->hb[0],
+                                       n_sink_blk, n_win_blk, sm_scale, h->hb[6], st, nullptr, on_device,
+                                       on_device ? h->d_qflags + c : nullptr, epoch)))
+          return r;
+        after_attn = true;
+      }
+      PA_CUDA(cudaEventRecord(ev_done[c], st));
+      PA_CUDA(cudaStreamWaitEvent(h->s_d2h, ev_done[c], 0));
+      for (const pa_seq& pc : chunks[c]) {
+        const size_t off = (size_t)pc.q_off * row_bytes;
+        PA_CUDA(cudaMemcpyAsync(static_cast<char*>(out) + off, static_cast<const char*>(h->hb[6]) + off,
+                                (size_t)pc.n_q * row_bytes, cudaMemcpyDeviceToHost, h->s_d2h));
+      }
     }
+    if ((r = tm.mark(h, 2, st))) return r;
+    // the caller's stream waits for both copy streams
+    PA_CUDA(cudaEventRecord(ev_end, h->s_d2h));
+    PA_CUDA(cudaStreamWaitEvent(st, ev_end, 0));
+    PA_CUDA(cudaEventRecord(ev_start, h->s_h2d));
+    PA_CUDA(cudaStreamWaitEvent(st, ev_start, 0));
+    return PA_OK;
+  };
+  if ((rc = enqueue())) {
+    tm.release(h);
+    // errors of the drain itself are ignored: the first failure is reported
+    (void)cudaStreamSynchronize(h->s_h2d);
+    (void)cudaStreamSynchronize(h->s_d2h);
+    (void)cudaStreamSynchronize(st);
+    return rc;
   }
-  if (!rc) rc = tm.mark(h, 2, st);
-  // the caller's stream waits for both copy streams
-  PA_CUDA(cudaEventRecord(ev_end, h->s_d2h));
-  PA_CUDA(cudaStreamWaitEvent(st, ev_end, 0));
-  PA_CUDA(cudaEventRecord(ev_start, h->s_h2d));
-  PA_CUDA(cudaStreamWaitEvent(st, ev_start, 0));
-  const int le = pa_last_error(h, stream);
-  return rc ? rc : le;
+  return pa_last_error(h, stream);
+}
+
+int pa_debug_copy_streams_idle(pa_handle h) {
+  if (!h) return PA_EINVAL;
+  for (cudaStream_t s : {h->s_h2d, h->s_d2h}) {
+    if (!s) continue;
+    const cudaError_t e = cudaStreamQuery(s);
+    if (e == cudaErrorNotReady) return 0;
+    if (e != cudaSuccess) return PA_ECUDA;
+  }
+  return 1;
 }
 
 int pa_last_error(pa_handle h, void* stream) {
@@ -893,6 +934,16 @@ int pa_debug_gather(pa_handle h, int n_seq, const pa_seq* seqs, const int8_t* k_
   PA_CUDA(launch_debug_gather(widen_params(h, k_pool, v_pool, k_scale, v_scale, block_table, n_seq), seq, k_out,
                               v_out, ks_out, vs_out, tok_out, st));
   return pa_last_error(h, stream);
+}
+
+int pa_debug_qcodes(const void* q_rows, int n_rows, int8_t* codes, float* scales, void* stream) {
+  if (n_rows < 0 || (n_rows > 0 && (!q_rows || !codes || !scales))) return PA_EINVAL;
+  if (n_rows == 0) return PA_OK;
+  if (!aligned(q_rows, 16) || !aligned(codes, 4) || !aligned(scales, 4)) return PA_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  PA_CUDA(launch_debug_qcodes(static_cast<const __nv_bfloat16*>(q_rows), n_rows, codes, scales, st));
+  PA_CUDA(cudaStreamSynchronize(st));
+  return PA_OK;
 }
 
 int pa_kv_append(pa_handle h, const void* k_new, const void* v_new, int n_new, int tok_start,

@@ -664,7 +664,7 @@ __device__ __forceinline__ LaneRows lane_rows(const AttnParams& p, int t0, int g
 // Q on the pages' int8 grid (step a1), in place in shared memory: the row's
 // codes rint(q * 127/absmax) clamped to [-127, 127], held exactly as bf16;
 // returns s_q = absmax / 127 (sm_scale * log2(e) is in the K scales).
-__device__ __forceinline__ float q_codes_int8(const AttnParams& p, uint8_t* qs, int r) {
+__device__ __forceinline__ float q_codes_int8(uint8_t* qs, int r) {
   float absmax = 0.f;
 #pragma unroll 1
   for (int reg = 0; reg < 4; ++reg)
@@ -793,7 +793,7 @@ __device__ __forceinline__ void role_correction(const AttnParams& p, const Ctx& 
     const SeqGeom sg = p.seqs[un.seq];
     if (p.q_mode == 1) {  // the unit's Q codes, in place, before the MMA may read Q
       if (!(ok = c.warp_wait(B_QFULL, k_unit & 1, 40))) break;
-      c_rows[(k_unit & 1) * kRows + r] = q_codes_int8(p, sm + kSmQ, r);
+      c_rows[(k_unit & 1) * kRows + r] = q_codes_int8(sm + kSmQ, r);
       fence_proxy_async_shared();  // generic-proxy writes, read next by the tensor core
       __syncwarp();
       if (lane == 0) {
@@ -898,7 +898,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
+// Debug export (tests): the int8 query grid of the fused prologue, run by
+// q_codes_int8 itself on rows staged in the layout the Q TMA load writes
+// (four 64-dim regions of 128-byte rows, 128-byte swizzle), one thread per row
+// as in the correction warps.
+constexpr int kDbgQSmem = 4 * kRegionBytes + 1024;
+
+__global__ void __launch_bounds__(kRows) debug_qcodes_kernel(const __nv_bfloat16* q, int n, int8_t* codes,
+                                                             float* scales) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
+  const int r = threadIdx.x;
+  const int row = blockIdx.x * kRows + r;
+  const uint4* src = reinterpret_cast<const uint4*>(q + (size_t)row * kHeadDim);
+#pragma unroll 4
+  for (int pc = 0; pc < 32; ++pc) *swz(sm + (pc >> 3) * kRegionBytes, r, pc & 7) = row < n ? src[pc] : make_uint4(0, 0, 0, 0);
+  const float s = q_codes_int8(sm, r);
+  if (row >= n) return;
+  uint32_t* dst = reinterpret_cast<uint32_t*>(codes + (size_t)row * kHeadDim);
+#pragma unroll 4
+  for (int pc = 0; pc < 32; ++pc) {
+    const uint4 v = *swz(sm + (pc >> 3) * kRegionBytes, r, pc & 7);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t b[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {  // two bf16 codes (exact integers) -> two int8 bytes
+      const int lo = (int)__uint_as_float(w[e] << 16), hi = (int)__uint_as_float(w[e] & 0xffff0000u);
+      b[e] = ((uint32_t)lo & 0xffu) | (((uint32_t)hi & 0xffu) << 8);
+    }
+    dst[2 * pc] = b[0] | (b[1] << 16);
+    dst[2 * pc + 1] = b[2] | (b[3] << 16);
+  }
+  scales[row] = s;
+}
+
 }  // namespace
+
+cudaError_t launch_debug_qcodes(const __nv_bfloat16* q, int n, int8_t* codes, float* scales, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(debug_qcodes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDbgQSmem);
+  if (e != cudaSuccess) return e;
+  debug_qcodes_kernel<<<(n + kRows - 1) / kRows, kRows, kDbgQSmem, st>>>(q, n, codes, scales);
+  return cudaGetLastError();
+}
 
 int attention_pairs(int n_sm) {
   static int max_pairs = -1;

@@ -131,6 +131,9 @@ int attention_pairs(int n_sm);
 // Debug exports (tests only).
 cudaError_t launch_debug_gather(const WidenParams& p, int seq, int8_t* k_out, int8_t* v_out, float* ks_out,
                                 float* vs_out, int32_t* tok_out, cudaStream_t st);
+// The int8 query grid of the attention prologue on n rows of 256 bf16 values:
+// codes int8 [n][256], scales fp32 [n].
+cudaError_t launch_debug_qcodes(const __nv_bfloat16* q, int n, int8_t* codes, float* scales, cudaStream_t st);
 cudaError_t launch_debug_maskset(const SeqGeom* seqs, const Unit* units, int n_units, int UT, int G, int S, int W,
                                  int32_t* row_counts, int32_t* unit_blocks, int cap, cudaStream_t st);
 

@@ -32,38 +32,93 @@ constexpr size_t kHeaderBytes = 4096;            // error word, V-scale maxima, 
 constexpr size_t kUnitsBytes = 1u << 20;         // work list
 constexpr int kMaxUnits = (int)(kUnitsBytes / sizeof(Unit));
 constexpr size_t kWidenedOffset = kHeaderBytes + kUnitsBytes;
+// First tokens of units (one per UT query tokens) the ordering kernel ranks in
+// shared memory; the widened-row limit keeps every call below it.
+constexpr int kMaxT0 = 16384;
+constexpr int kPlanThreads = 256;
 
-// Device address of the scratch, resolved once per device with that device current.
-void* scratch_address(int device, int* rc) {
-  static std::mutex mu;
-  static void* addr[64] = {nullptr};
-  std::lock_guard<std::mutex> lock(mu);
-  if (device < 0 || device >= 64) {
-    *rc = PA_ECUDA;
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <typename F>
+F driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
     return nullptr;
-  }
-  if (!addr[device]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-      *rc = PA_ECUDA;
-      return nullptr;
-    }
-    addr[device] = p;
-  }
-  *rc = PA_OK;
-  return addr[device];
+  return reinterpret_cast<F>(p);
 }
 
-// Writes the sequence geometry and the work list (units ordered by
-// decreasing first token: for one sequence the later query blocks see the
-// full window, so this is the longest-first order) and clears the words that
-// must start at zero.
-__global__ void noalloc_plan_kernel(SeqGeom sg, int S, int W, int HKV, int UT, int n_t0, int t_first, SeqGeom* seq_out,
-                                    Unit* units, unsigned int* vsmax, int* err) {
-  const int n_units = n_t0 * HKV;
-  for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < n_units; u += gridDim.x * blockDim.x) {
-    const int t0 = t_first + (n_t0 - 1 - u / HKV) * UT;
-    units[u] = Unit{0, u % HKV, t0, unit_geom(t0, UT, sg, S, W).n_tiles};
+// Per device: the scratch's device address and the attributes a call needs,
+// looked up once with that device current, and again if the device's context
+// was replaced since (a reset reloads the module, which may move the array).
+struct DeviceSetup {
+  unsigned long long ctx_id = 0;  // unique id of the context the entry was made in (0: none yet)
+  void* addr = nullptr;
+  int n_sm = 0;
+  bool sm103 = false;
+};
+
+int device_setup(int device, DeviceSetup* out) {
+  static std::mutex mu;
+  static DeviceSetup table[64];
+  static CtxGetCurrentFn get_ctx = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    get_ctx = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  });
+  if (device < 0 || device >= 64 || !get_ctx || !get_id) return PA_ECUDA;
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return PA_ECUDA;
+  if (!ctx) {  // no context current yet: cudaSetDevice makes the device's primary context current
+    if (cudaSetDevice(device) != cudaSuccess || get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return PA_ECUDA;
+  }
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return PA_ECUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  DeviceSetup& e = table[device];
+  if (e.ctx_id != id || !e.addr) {
+    DeviceSetup n;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n.n_sm, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+      return PA_ECUDA;
+    n.sm103 = major == 10 && minor == 3;
+    if (n.sm103 && (cudaGetSymbolAddress(&n.addr, g_noalloc_scratch) != cudaSuccess || !n.addr)) return PA_ECUDA;
+    n.ctx_id = id;
+    e = n;
+  }
+  *out = e;
+  return PA_OK;
+}
+
+// The work list in the handle planner's order: units by decreasing key tiles,
+// ties by increasing first token, then kv head (a stable sort of the list
+// made in token order).  For one sequence every kv head of a first token has
+// the same tiles, so each first token t0_i = t_first + i UT is ranked among
+// all n_t0 of them (tiles held in shared memory) and its HKV units take
+// consecutive places.  Also writes the sequence geometry and clears the
+// words that must start at zero.
+__global__ void __launch_bounds__(kPlanThreads) noalloc_plan_kernel(SeqGeom sg, int S, int W, int HKV, int UT,
+                                                                    int n_t0, int t_first, SeqGeom* seq_out,
+                                                                    Unit* units, unsigned int* vsmax, int* err) {
+  __shared__ uint16_t tiles[kMaxT0];
+  for (int j = threadIdx.x; j < n_t0; j += kPlanThreads)
+    tiles[j] = (uint16_t)unit_geom(t_first + j * UT, UT, sg, S, W).n_tiles;
+  __syncthreads();
+  const int i = blockIdx.x * kPlanThreads + threadIdx.x;
+  if (i < n_t0) {
+    const int ti = tiles[i];
+    int rank = 0;
+    for (int j = 0; j < n_t0; ++j) {
+      const int tj = tiles[j];
+      rank += (tj > ti || (tj == ti && j < i)) ? 1 : 0;
+    }
+    for (int g = 0; g < HKV; ++g) units[rank * HKV + g] = Unit{0, g, t_first + i * UT, ti};
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     *seq_out = sg;
@@ -113,8 +168,11 @@ extern "C" int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_page
   const int G = n_q_heads / n_kv_heads;
   if (G > kRows || kRows % G) return PA_EINVAL;
   if (n_pool_pages <= 0 || max_pages_per_seq <= 0 || n_sink_blk < 0) return PA_EINVAL;
-  if (n_q < 1 || q_start < 0 || n_ctx < q_start + n_q || (long long)n_ctx > (long long)max_pages_per_seq * kPage)
+  if (n_q < 1 || q_start < 0 || (long long)n_ctx < (long long)q_start + n_q ||
+      (long long)n_ctx > (long long)max_pages_per_seq * kPage)
     return PA_EINVAL;
+  // positions stay far from int overflow in the unit and tile arithmetic
+  if ((long long)q_start + n_q > (1LL << 30) || (long long)n_ctx > (1LL << 30)) return PA_EINVAL;
   if (!q || !k_pool || !v_pool || !k_scale || !v_scale || !block_table || !out) return PA_EINVAL;
   if (!aligned_to(q, 16) || !aligned_to(k_pool, 16) || !aligned_to(v_pool, 16) || !aligned_to(out, 16) ||
       !aligned_to(k_scale, 4) || !aligned_to(v_scale, 4) || !aligned_to(block_table, 4))
@@ -137,16 +195,15 @@ extern "C" int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_page
   // size limits of the static scratch: a clear error, never an overflow
   const long long row_bytes = (long long)n_kv_heads * (2 * kHeadDim * 2LL + 2 * sizeof(float));  // bf16 K + fp16 V^T, two scales
   const long long cap_rows = ((long long)PA_NOALLOC_SCRATCH_BYTES - (long long)kWidenedOffset) / row_bytes / 64 * 64;
-  if (n_rows > cap_rows || (long long)n_t0 * n_kv_heads > kMaxUnits) return PA_ENOSCRATCH;
+  if (n_rows > cap_rows || (long long)n_t0 * n_kv_heads > kMaxUnits || n_t0 > kMaxT0) return PA_ENOSCRATCH;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PA_ECUDA;
-  cudaDeviceProp prop;
-  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return PA_ECUDA;
-  if (prop.major != 10 || prop.minor != 3) return PA_EARCH;
-  int rc = PA_OK;
-  unsigned char* base = static_cast<unsigned char*>(scratch_address(dev, &rc));
+  DeviceSetup ds;
+  int rc = device_setup(dev, &ds);
   if (rc) return rc;
+  if (!ds.sm103) return PA_EARCH;
+  unsigned char* base = static_cast<unsigned char*>(ds.addr);
 
   // carve the scratch
   const int cap = (int)cap_rows;  // row stride of the widened buffers
@@ -175,8 +232,8 @@ extern "C" int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_page
     return rc;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  noalloc_plan_kernel<<<(n_t0 * n_kv_heads + 255) / 256, 256, 0, st>>>(sg, n_sink_blk, n_win_blk, n_kv_heads, UT, n_t0,
-                                                                       t_first, seq_dev, units, vsmax, err);
+  noalloc_plan_kernel<<<(n_t0 + kPlanThreads - 1) / kPlanThreads, kPlanThreads, 0, st>>>(
+      sg, n_sink_blk, n_win_blk, n_kv_heads, UT, n_t0, t_first, seq_dev, units, vsmax, err);
   if (cudaGetLastError() != cudaSuccess) return PA_ECUDA;
 
   WidenParams wp{};
@@ -226,12 +283,13 @@ extern "C" int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_page
   a.wait_ns = 2000ull * 1000000ull;
   a.q_ready = nullptr;
   a.debug_stall = 0;
-  if (launch_attention(a, m, prop.multiProcessorCount, st) != cudaSuccess) return PA_ECUDA;
+  if (launch_attention(a, m, ds.n_sm, st) != cudaSuccess) return PA_ECUDA;
 
-  // synchronous: report this call's device-side status
-  if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ECUDA;
+  // synchronous: report this call's device-side status, read on `stream`
+  // behind the kernels (no other stream is waited for)
   int e = 0;
-  if (cudaMemcpy(&e, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ECUDA;
+  if (cudaMemcpyAsync(&e, err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return PA_ECUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ECUDA;
   if (e & DEV_ERR_TIMEOUT) return PA_ETIMEOUT;
   if (e & DEV_ERR_BAD_PAGE) return PA_EBADPAGE;
   return e ? PA_ECUDA : PA_OK;
