@@ -89,6 +89,31 @@ def measured_peaks():
         return FALLBACK_BF16_TFLOPS, "fallback bf16"
 
 
+def measured_int8_peak():
+    """The dense int8 tensor rate of this GPU, measured now: sm_103a has no
+    integer tcgen05 MMA, so it is the rate of the warp-level mma.sync s8
+    instruction (libpa_peak.so; the best of 1, 2 and 4 blocks per SM, each run
+    about 40 ms).  Returns (TOPS, note) or (None, why)."""
+    import ctypes as C
+    path = os.path.join(ROOT, "windowed_prefill_attention_gb300", "libpa_peak.so")
+    try:
+        lib = C.CDLL(path)
+    except OSError as e:
+        return None, "libpa_peak.so not loadable: %s" % e
+    lib.pa_peak_mma_sync.argtypes = [C.c_int, C.c_int, C.c_longlong, C.POINTER(C.c_double), C.POINTER(C.c_double)]
+    best = None
+    for bps in (1, 2, 4):
+        tops, ms = C.c_double(), C.c_double()
+        iters = 2000
+        if lib.pa_peak_mma_sync(0, bps, iters, C.byref(tops), C.byref(ms)) != 0:
+            return None, "probe failed"
+        iters = max(2000, int(iters * 40.0 / max(ms.value, 1e-3)))
+        if lib.pa_peak_mma_sync(0, bps, iters, C.byref(tops), C.byref(ms)) != 0:
+            return None, "probe failed"
+        best = tops.value if best is None else max(best, tops.value)
+    return best, "measured now: mma.sync.m16n8k32 s8 (no integer tcgen05 MMA on sm_103a), best of 1/2/4 blocks per SM"
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "windowed_prefill_attention_gb300", "csrc")
@@ -348,6 +373,7 @@ def run_ours(args, wl):
     finally:
         pa.pa_destroy(he)
     e2e_value = world * ops / e2e_s / 1e12
+    int8_peak, int8_src = measured_int8_peak()
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -368,7 +394,9 @@ def run_ours(args, wl):
         "roofline": {"bound": "tensor", "kernel": "attention_kernel", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_src,
                      "traffic": profiled_traffic(wl.name), "launch_ms": attn_avg_ms,
-                     "widen_launch_ms": widen_ms / max(1, n_calls)},
+                     "widen_launch_ms": widen_ms / max(1, n_calls),
+                     "peak_int8": int8_peak, "frac_int8": achieved / int8_peak if int8_peak else None,
+                     "peak_int8_source": int8_src},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp)
@@ -506,6 +534,136 @@ def run_decode(args, wl):
                      "traffic": profiled_traffic(wl.name, "decode_split_kernel"), "bytes_per_step": nbytes}}), flush=True)
 
 
+# --sweep: every benchmark workload in the default containers, then the 32k
+# workload on the pages' own grids (int8 Q per row, u8 P per row and tile)
+SWEEP = (("tiny", {}), ("4k", {}), ("32k", {}), ("64k", {}), ("chunked", {}),
+         ("32k", {"q_mode": 1}), ("32k", {"p_mode": 1}), ("32k", {"q_mode": 1, "p_mode": 1}))
+
+
+def _mode_name(opts):
+    return "%s Q, %s P'" % ("int8" if opts.get("q_mode") == 1 else "bf16", "u8" if opts.get("p_mode") == 1 else "fp16")
+
+
+def _sweep_rows(inp, n_tokens, seed):
+    """(global row, q head) pairs: every row of a small workload, else every
+    head of n_tokens uniformly drawn tokens plus each sequence's first and
+    last 4 tokens."""
+    n, hq = inp.q.shape[0], inp.q.shape[1]
+    if n * hq <= 4096:
+        toks = np.arange(n)
+    else:
+        rng = np.random.default_rng(seed)
+        t = set(rng.choice(n, size=min(n, n_tokens), replace=False).tolist())
+        for q_off, _, n_q, _ in inp.seq_desc.tolist():
+            t.update(range(q_off, q_off + min(4, n_q)))
+            t.update(range(q_off + max(0, n_q - 4), q_off + n_q))
+        toks = np.array(sorted(t))
+    tt, hh = np.meshgrid(toks.astype(np.int32), np.arange(hq, dtype=np.int32), indexing="ij")
+    return np.stack([tt.ravel(), hh.ravel()], 1)
+
+
+def run_sweep(args):
+    """One JSON line per (workload, precision mode): device-timed TOPS, tokens/s
+    and the attention kernel's roofline fraction (bf16 and int8 peaks),
+    algorithmic HBM bytes per second, and the parity of the same call against
+    the fp64 oracle on sampled rows, with the oracle's time on the host cores."""
+    import torch
+
+    import oracle
+    import windowed_prefill_attention_gb300 as pa
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    peak, peak_src = measured_peaks()
+    int8_peak, int8_src = measured_int8_peak()
+    flush = L2Flush(dev)
+    cores = len(os.sched_getaffinity(0))
+    cache = {}
+    for name, opts in SWEEP:
+        wl = CONFIGS[name]
+        if name not in cache:
+            cache.clear()
+            cache[name] = make_inputs(wl)
+        inp = cache[name]
+        q = torch.from_numpy(inp.q.view(np.int16)).view(torch.bfloat16).to(dev)
+        kp, vp = torch.from_numpy(inp.k_pool).to(dev), torch.from_numpy(inp.v_pool).to(dev)
+        ks, vs = torch.from_numpy(inp.k_scale).to(dev), torch.from_numpy(inp.v_scale).to(dev)
+        bt = torch.from_numpy(inp.block_table).to(dev)
+        out = torch.empty_like(q)
+        seqs, S, W, sm = inp.seq_desc, wl.n_sink_blk, wl.n_win_blk, wl.sm_scale
+        h = pa.pa_create(wl.n_q_heads, wl.n_kv_heads, inp.k_pool.shape[0], inp.block_table.shape[1],
+                         record_timing=True, **opts)
+        try:
+            def step():
+                pa.pa_prefill_batch(h, seqs, q, kp, vp, ks, vs, bt, S, W, sm, out)
+            for _ in range(args.warmup):
+                flush()
+                step()
+            if pa.pa_last_error(h) != 0:
+                raise RuntimeError("device error in warm-up (%s)" % name)
+            pa.pa_timing(h, reset=True)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            sampler = ClockSampler(0)
+            torch.cuda.synchronize()
+            sampler.start()
+            time.sleep(0.2)
+            for a, b in ev:
+                flush()
+                a.record()
+                step()
+                b.record()
+            torch.cuda.synchronize()
+            clocks = sampler.stop()
+            rc = pa.pa_last_error(h)
+            if rc != 0:
+                raise RuntimeError("device error in timed steps (%s): %s" % (name, pa.pa_strerror(rc)))
+            step_ms = float(sum(a.elapsed_time(b) for a, b in ev)) / args.steps
+            widen_ms, attn_ms, n_calls = pa.pa_timing(h, reset=True)
+            _, _, n_rows = pa.pa_plan(wl.n_q_heads, wl.n_kv_heads, seqs, S, W)
+        finally:
+            pa.pa_destroy(h)
+        got = out.float().cpu().numpy()
+        ops = algorithmic_ops(wl)
+        attn_ms_avg = attn_ms / max(1, n_calls)
+        achieved = ops / (attn_ms_avg / 1e3) / 1e12
+        # algorithmic bytes: q read, out written, each stored (visible) key's K and V codes and scales
+        nbytes = 2 * wl.total_q * wl.n_q_heads * HEAD_DIM * 2 + n_rows * wl.n_kv_heads * (2 * HEAD_DIM + 8)
+        # parity on sampled rows against the fp64 definition; the oracle timed on all host cores
+        rows = _sweep_rows(inp, 160, seed=17)
+        prob = oracle.Problem.from_inputs(inp)
+        t0 = time.perf_counter()
+        ref = oracle.exact(prob, rows, n_threads=cores)
+        t_oracle = time.perf_counter() - t0
+        g = got[rows[:, 0], rows[:, 1]].astype(np.float64)
+        err = np.abs(g - ref) / np.maximum(1.0, np.abs(ref))
+        pairs_rows = sum(_row_count(inp, int(i), wl) for i in rows[:, 0])
+        total_pairs = ops // (4 * HEAD_DIM)
+        line = {
+            "metric": METRIC, "value": ops / (step_ms / 1e3) / 1e12, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16" if not opts else _mode_name(opts), "data": "synthetic",
+            "config": dict(workload_config(wl, L2_NOTE), precision_mode=_mode_name(opts)),
+            "sweep": True,
+            "tokens_per_s": wl.total_q / (step_ms / 1e3),
+            "algorithmic_ops_per_step": ops,
+            "hbm_gbs_algorithmic": nbytes / (step_ms / 1e3) / 1e9, "algorithmic_bytes_per_step": nbytes,
+            "clocks": clocks, "gpu_launches": 2 * args.steps,
+            "roofline": {"bound": "tensor", "kernel": "attention_kernel", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_src,
+                         "launch_ms": attn_ms_avg, "widen_launch_ms": widen_ms / max(1, n_calls),
+                         "peak_int8": int8_peak, "frac_int8": achieved / int8_peak if int8_peak else None,
+                         "peak_int8_source": int8_src},
+            "parity": {"rows": int(rows.shape[0]), "max_norm_err": float(err.max()),
+                       "mean_norm_err": float(err.mean()),
+                       "l1_ratio": float(np.abs(g - ref).sum() / np.abs(ref).sum()),
+                       "bound": "max <= 3e-2, mean <= 1e-2 (normalised by max(1, |ref|))"},
+            "oracle": {"rows": int(rows.shape[0]), "seconds": t_oracle, "cores": cores,
+                       "full_workload_seconds_est": t_oracle * total_pairs / max(1, pairs_rows),
+                       "kind": "fp64 oracle (definition), as it stands"},
+        }
+        print(json.dumps(line), flush=True)
+
+
 def _row_count_decode(ctx, S, W):
     """Visible keys of a context's last token: the mask's closed form."""
     t = ctx - 1
@@ -526,9 +684,13 @@ def main():
     ap.add_argument("--gate", action="store_true", help="fuse the output gate out * sigmoid(q_gate) (extra row)")
     ap.add_argument("--op", choices=["prefill", "kv_append", "decode"], default="prefill",
                     help="kv_append / decode: time that step alone (extra rows)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="one line per workload and precision mode, with parity against the oracle (extra rows)")
     args = ap.parse_args()
     wl = CONFIGS[args.config]
-    if args.impl == "reference":
+    if args.sweep and args.impl == "ours":
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args, wl)
     elif args.op == "kv_append":
         run_kv_append(args, wl)

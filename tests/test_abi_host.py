@@ -25,10 +25,10 @@ def pa():
     return mod
 
 
-def header_symbols():
-    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+def header_symbols(header="pa.h"):
+    text = open(os.path.join(ROOT, "include", header)).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
 
 
 def test_library_exports_every_declared_symbol(pa):
@@ -38,6 +38,22 @@ def test_library_exports_every_declared_symbol(pa):
     for n in names:
         assert hasattr(lib, n), n
     assert set(pa.EXPORTED) == set(names)
+
+
+def test_peak_probe_library_exports_its_header(pa):
+    """libpa_peak.so (the tensor-core throughput probe the benchmark's int8
+    roofline uses) loads and exports what include/pa_peak.h declares."""
+    lib = C.CDLL(os.path.join(os.path.dirname(LIB), "libpa_peak.so"))
+    names = header_symbols("pa_peak.h")
+    assert names == ["pa_peak_mma_sync"]
+    for n in names:
+        assert hasattr(lib, n), n
+    # bad arguments are rejected before any CUDA call (no GPU needed)
+    lib.pa_peak_mma_sync.argtypes = [C.c_int, C.c_int, C.c_longlong, C.c_void_p, C.c_void_p]
+    t = C.c_double()
+    assert lib.pa_peak_mma_sync(7, 1, 10, C.byref(t), None) == -1
+    assert lib.pa_peak_mma_sync(0, 0, 10, C.byref(t), None) == -1
+    assert lib.pa_peak_mma_sync(0, 1, 10, None, None) == -1
 
 
 def test_binding_constants_match_the_header(pa):

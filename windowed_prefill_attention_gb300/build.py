@@ -9,6 +9,10 @@ SOURCES = [os.path.join(CSRC, f) for f in ("pa_api.cu", "pa_kernels.cu", "pa_att
 HEADERS = [os.path.join(CSRC, f) for f in ("pa_internal.h", "pa_ptx.cuh", "pa_tiles.cuh")] + [
     os.path.join(HERE, "..", "include", "pa.h")]
 LIB = os.path.join(HERE, "libpa.so")
+# the tensor-core throughput probe the benchmark's roofline uses (its own library)
+PEAK_SOURCES = [os.path.join(CSRC, "pa_peak.cu")]
+PEAK_HEADERS = [os.path.join(HERE, "..", "include", "pa_peak.h")]
+PEAK_LIB = os.path.join(HERE, "libpa_peak.so")
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-shared", "--threads", "0"]
@@ -19,20 +23,29 @@ def nvcc() -> str:
     return cand if os.path.exists(cand) else "nvcc"
 
 
-def stale() -> bool:
-    if not os.path.exists(LIB):
+def stale(lib, sources, headers) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
-    return any(os.path.getmtime(f) > t for f in SOURCES + HEADERS)
+    t = os.path.getmtime(lib)
+    return any(os.path.getmtime(f) > t for f in sources + headers)
+
+
+def _compile(lib, sources, verbose):
+    tmp = lib + ".tmp%d" % os.getpid()
+    cmd = [nvcc()] + NVCC_FLAGS + (["-Xptxas", "-v"] if verbose else []) + sources + ["-o", tmp]
+    return subprocess.Popen(cmd), tmp, lib
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not stale():
-        return LIB
-    tmp = LIB + ".tmp%d" % os.getpid()
-    cmd = [nvcc()] + NVCC_FLAGS + (["-Xptxas", "-v"] if verbose else []) + SOURCES + ["-o", tmp]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
+    jobs = []
+    if force or stale(LIB, SOURCES, HEADERS):
+        jobs.append(_compile(LIB, SOURCES, verbose))
+    if force or stale(PEAK_LIB, PEAK_SOURCES, PEAK_HEADERS):
+        jobs.append(_compile(PEAK_LIB, PEAK_SOURCES, verbose))
+    for proc, tmp, lib in jobs:
+        if proc.wait() != 0:
+            raise subprocess.CalledProcessError(proc.returncode, "nvcc -> " + os.path.basename(lib))
+        os.replace(tmp, lib)
     return LIB
 
 
