@@ -578,7 +578,8 @@ def run_sweep(args):
     flush = L2Flush(dev)
     cores = len(os.sched_getaffinity(0))
     cache = {}
-    for name, opts in SWEEP:
+    entries = SWEEP if args.only is None else (SWEEP[args.only],)
+    for name, opts in entries:
         wl = CONFIGS[name]
         if name not in cache:
             cache.clear()
@@ -686,6 +687,8 @@ def main():
                     help="kv_append / decode: time that step alone (extra rows)")
     ap.add_argument("--sweep", action="store_true",
                     help="one line per workload and precision mode, with parity against the oracle (extra rows)")
+    ap.add_argument("--only", type=int, default=None,
+                    help="with --sweep: run only this entry of the sweep (0-based; for per-workload ncu captures)")
     args = ap.parse_args()
     wl = CONFIGS[args.config]
     if args.sweep and args.impl == "ours":
