@@ -527,11 +527,11 @@ def run_decode(args, wl):
         "config": {"workload": wl.name, "op": "decode", "n_seq": n_seq, "context": ctx, "n_q_heads": hq,
                    "n_kv_heads": hkv, "n_sink_blk": S, "n_win_blk": W, "visible_keys_per_seq": keys,
                    "l2": L2_NOTE},
-        "tokens_per_s": n_seq / (ms / 1e3), "gpu_launches": 2 * args.steps, "clocks": clocks,
-        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel + decode_combine_kernel", "achieved": gbs,
+        "tokens_per_s": n_seq / (ms / 1e3), "gpu_launches": args.steps, "clocks": clocks,
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": gbs,
                      "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                      "peak_source": "measured copy bandwidth (MEASURED_PEAKS.json)",
-                     "traffic": profiled_traffic(wl.name, "decode_split_kernel"), "bytes_per_step": nbytes}}), flush=True)
+                     "traffic": profiled_traffic(wl.name, "decode_kernel"), "bytes_per_step": nbytes}}), flush=True)
 
 
 # --sweep: every benchmark workload in the default containers, then the 32k

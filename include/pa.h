@@ -199,13 +199,18 @@ int pa_kv_append(pa_handle h, const void* k_new, const void* v_new, int n_new, i
  * cores" and "Relation to open PRs").  seqs[s] must have n_q == 1 and q_start
  * == n_ctx - 1: the token is the context's last; its row in q and out is
  * seqs[s].q_off; block_table row s holds its pages.  Layouts as pa_prefill_batch
- * (q, out bf16 [rows][n_q_heads][256]).  The visible blocks are split into
- * groups of 16 computed in parallel and merged; q, the pool and P' stay in
- * exact or fp16 containers (the bf16 query scaled per row by a power of two,
- * codes as exact fp16, P' = p * v_scale in fp16, fp32 accumulation).
- * Needs n_q_heads / n_kv_heads <= 8 (PA_EINVAL otherwise).  Asynchronous;
- * device errors (PA_EBADPAGE for a page entry outside the pool, whose block is
- * skipped) through pa_last_error. */
+ * (q, out bf16 [rows][n_q_heads][256]).  The visible 16-token blocks of all
+ * (sequence, kv head) pairs are split into equal runs computed in parallel
+ * and merged on the device; q, the pool and P' stay in exact or fp16
+ * containers (the bf16 query scaled per row by a power of two, codes as exact
+ * fp16, P' = p * v_scale in fp16, fp32 accumulation).  One launch per 512
+ * sequences, the sequence table carried in its parameters (no host-to-device
+ * copy, no host wait).  Needs n_q_heads / n_kv_heads <= 8, k_scale and
+ * v_scale 16-byte aligned, and fewer than 2^30 visible blocks x kv heads per
+ * 512 sequences (PA_EINVAL otherwise).  Calls on one handle share its work
+ * buffers: issue them on one stream (calls that overlap on the GPU race).
+ * Asynchronous; device errors (PA_EBADPAGE for a page entry outside the pool,
+ * whose block is skipped) through pa_last_error. */
 int pa_decode(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* k_pool, const int8_t* v_pool,
               const float* k_scale, const float* v_scale, const int32_t* block_table, int n_sink_blk, int n_win_blk,
               float sm_scale, void* out, void* stream);

@@ -50,6 +50,12 @@ CASES = {
     "gqa4": _decode_wl("dec_g4", 8, 2, (6000,), 1, 256, 47),
     "many": _decode_wl("dec_many", 16, 2, tuple(int(x) for x in np.random.default_rng(48).integers(1, 20000, 40)),
                        1, 256, 48),
+    # window off on long contexts: each (sequence, kv head) pair spans dozens of CTAs and partials
+    "long_pairs": _decode_wl("dec_long", 8, 2, (40000, 36001, 1), 1, 0, 50),
+    # more than one launch's table (512 sequences): short contexts, many pairs per CTA
+    "over_512": _decode_wl("dec_600", 4, 2, tuple(int(x) for x in np.random.default_rng(51).integers(1, 300, 600)),
+                           1, 8, 51, outliers=0.0),
+    "kv_heads_8": _decode_wl("dec_h8", 8, 8, (5000, 129, 70000), 1, 256, 52),
 }
 
 

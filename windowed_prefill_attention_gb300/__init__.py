@@ -90,10 +90,9 @@ def _check(code: int, where: str) -> int:
 def _seqs(seqs):
     """[(q_off, q_start, n_q, n_ctx), ...] or an int array [n, 4] -> ctypes array."""
     arr = np.asarray(seqs, dtype=np.int64).reshape(-1, 4)
-    out = (pa_seq * arr.shape[0])()
-    for i, (a, b, c, d) in enumerate(arr.tolist()):
-        out[i] = pa_seq(a, b, c, d)
-    return out
+    if arr.size and (int(arr.min()) < -2**31 or int(arr.max()) >= 2**31):
+        raise ValueError("sequence fields must fit int32")
+    return (pa_seq * arr.shape[0]).from_buffer_copy(np.ascontiguousarray(arr, dtype=np.int32))
 
 
 def _dev(t, dtype, name):

@@ -182,15 +182,15 @@ struct pa_ctx {
   int kv_rows = -1;
   int kv_cap = -1;
 
-  // decode: per-sequence table (pinned staging, like the plan) and partials
-  DecSeq* d_dec = nullptr;
-  int dec_cap = 0;
+  // decode: partials, the pairs' tickets (zeroed once; the kernel leaves them
+  // at zero), the pool's tensor maps (cached by pool pointers)
+  DecodeMaps dec_maps{};
+  const void* dec_kp = nullptr;
+  const void* dec_vp = nullptr;
   float* d_part = nullptr;
   int part_cap = 0;
-  void* h_dec = nullptr;
-  size_t h_dec_cap = 0;
-  cudaEvent_t dec_done = nullptr;
-  bool dec_recorded = false;
+  unsigned int* d_tickets = nullptr;
+  int tickets_cap = 0;
 
   // host-buffer path staging
   void* hb[7] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
@@ -586,16 +586,14 @@ int pa_create(pa_handle* out, int n_q_heads, int n_kv_heads, int head_dim, int p
 void pa_destroy(pa_handle h) {
   if (!h) return;
   cudaDeviceSynchronize();
-  void* ptrs[] = {h->kw, h->vt, h->ks, h->vs, h->vsmax, h->d_seqs, h->d_units, h->d_err, h->d_qflags, h->d_dec,
-                  h->d_part};
+  void* ptrs[] = {h->kw, h->vt, h->ks, h->vs, h->vsmax, h->d_seqs, h->d_units, h->d_err, h->d_qflags, h->d_part,
+                  h->d_tickets};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (int i = 0; i < 7; ++i)
     if (h->hb[i]) cudaFree(h->hb[i]);
   if (h->h_stage) cudaFreeHost(h->h_stage);
   if (h->upload_done) cudaEventDestroy(h->upload_done);
-  if (h->h_dec) cudaFreeHost(h->h_dec);
-  if (h->dec_done) cudaEventDestroy(h->dec_done);
   for (cudaEvent_t e : h->ev_free) cudaEventDestroy(e);
   for (cudaEvent_t e : h->ev_pending) cudaEventDestroy(e);
   for (cudaEvent_t e : h->pipe_ev) cudaEventDestroy(e);
@@ -979,58 +977,70 @@ int pa_decode(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const i
   int rc = check_inputs(h, q, k_pool, v_pool, k_scale, v_scale, block_table, out);
   if (rc) return rc;
   if (n_seq <= 0 || !seqs || h->G > 8 || !(sm_scale == sm_scale) || sm_scale < 0.f) return PA_EINVAL;
-  std::vector<DecSeq> tab((size_t)n_seq);
-  int max_splits = 1;
+  if (!aligned(k_scale, 16) || !aligned(v_scale, 16)) return PA_EINVAL;  // pages' scales are bulk-copied
+  std::vector<int> n_vis((size_t)n_seq);
   for (int s = 0; s < n_seq; ++s) {
     const pa_seq& q1 = seqs[s];
     if (q1.n_q != 1 || q1.q_off < 0 || q1.n_ctx < 1 || q1.q_start != q1.n_ctx - 1) return PA_EINVAL;
     if ((q1.n_ctx + kPage - 1) / kPage > h->max_pages) return PA_EINVAL;
-    DecSeq& d = tab[(size_t)s];
-    d.q_row = q1.q_off;
-    d.t = q1.n_ctx - 1;
-    d.bt_row = s;
-    const int last = d.t / kPage;
-    d.lo = n_win_blk > 0 ? std::max(0, last + 1 - n_win_blk) : 0;
-    d.n_sink = n_win_blk > 0 ? std::min(std::max(n_sink_blk, 0), d.lo) : 0;
-    d.n_vis = d.n_sink + (last - d.lo + 1);
+    // the prefill's block mask for the query at t = n_ctx - 1: sink blocks, then the window run up to t's block
+    const int last = (q1.n_ctx - 1) / kPage;
+    const int lo = n_win_blk > 0 ? std::max(0, last + 1 - n_win_blk) : 0;
+    const int n_sink = n_win_blk > 0 ? std::min(std::max(n_sink_blk, 0), lo) : 0;
+    n_vis[(size_t)s] = n_sink + (last - lo + 1);
   }
-  // blocks per split (one CTA): the size whose grid best fills whole waves of
-  // the SMs, each CTA costing its blocks plus a fixed ~8 blocks' worth
-  // (query load, combining its warps, writing its partial)
-  const long long slots = (long long)h->n_sm * decode_ctas_per_sm();
-  int per_split = kDecMaxSplitBlocks;
-  long long best = -1;
-  for (int ps = 16; ps <= kDecMaxSplitBlocks; ++ps) {
-    long long ctas = 0;
-    for (const DecSeq& d : tab) ctas += (long long)h->HKV * ((d.n_vis + ps - 1) / ps);
-    const long long cost = (ctas + slots - 1) / slots * (ps + 8);
-    if (best < 0 || cost < best) {
-      best = cost;
-      per_split = ps;
+  // Launches of up to kDecParamSeqs sequences, their table in the launch's
+  // parameters.  Work split: the launch's pairs' blocks end to end, per_cta
+  // blocks per CTA so that the grid is one wave of equal CTAs when 128-block
+  // CTAs would fit in one wave, else whole waves.
+  struct Launch {
+    int s0, n, total, per_cta, n_cta, max_slots;
+  };
+  std::vector<Launch> launches;
+  const long long slots = (long long)h->n_sm * decode_ctas_per_sm(h->HKV);
+  size_t part_need = 0;
+  for (int s0 = 0; s0 < n_seq; s0 += kDecParamSeqs) {
+    Launch L{};
+    L.s0 = s0;
+    L.n = std::min(kDecParamSeqs, n_seq - s0);
+    long long vis = 0;
+    int nv_max = 1;
+    for (int i = 0; i < L.n; ++i) {
+      vis += n_vis[(size_t)(s0 + i)];
+      nv_max = std::max(nv_max, n_vis[(size_t)(s0 + i)]);
     }
+    const long long total = vis * h->HKV;
+    if (total >= (1ll << 30)) return PA_EINVAL;
+    const long long full = (total + kDecMaxCtaBlocks - 1) / kDecMaxCtaBlocks;
+    const long long waves = std::max(1ll, (full + slots - 1) / slots);
+    L.total = (int)total;
+    L.per_cta = (int)std::max(1ll, (total + waves * slots - 1) / (waves * slots));
+    L.n_cta = (int)((total + L.per_cta - 1) / L.per_cta);
+    L.max_slots = (nv_max - 1 + L.per_cta - 1) / L.per_cta + 1;  // CTA runs a pair's blocks can meet
+    part_need = std::max(part_need, (size_t)L.n * h->HKV * L.max_slots * h->G * kDecPartStride);
+    launches.push_back(L);
   }
-  for (DecSeq& d : tab) {
-    d.per_split = per_split;
-    d.n_splits = (d.n_vis + per_split - 1) / per_split;
-    max_splits = std::max(max_splits, d.n_splits);
-  }
-  if ((rc = grow(h->d_dec, h->dec_cap, (size_t)n_seq))) return rc;
-  if ((rc = grow(h->d_part, h->part_cap, (size_t)n_seq * h->HQ * max_splits * kDecPartStride))) return rc;
-  const size_t bytes = tab.size() * sizeof(DecSeq);
+  if (part_need > (size_t)INT32_MAX) return PA_EINVAL;
+  if ((rc = grow(h->d_part, h->part_cap, part_need))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (!h->dec_done) PA_CUDA(cudaEventCreateWithFlags(&h->dec_done, cudaEventDisableTiming));
-  if (h->dec_recorded) PA_CUDA(cudaEventSynchronize(h->dec_done));  // never overwrite staging a copy may read
-  if (h->h_dec_cap < bytes) {
-    if (h->h_dec) cudaFreeHost(h->h_dec);
-    h->h_dec = nullptr;
-    h->h_dec_cap = 0;
-    PA_CUDA(cudaMallocHost(&h->h_dec, bytes));
-    h->h_dec_cap = bytes;
+  if (h->tickets_cap < kDecParamSeqs * h->HKV) {
+    if ((rc = grow(h->d_tickets, h->tickets_cap, (size_t)kDecParamSeqs * h->HKV))) return rc;
+    PA_CUDA(cudaMemsetAsync(h->d_tickets, 0, (size_t)h->tickets_cap * sizeof(unsigned int), st));
   }
-  std::memcpy(h->h_dec, tab.data(), bytes);
-  PA_CUDA(cudaMemcpyAsync(h->d_dec, h->h_dec, bytes, cudaMemcpyHostToDevice, st));
-  PA_CUDA(cudaEventRecord(h->dec_done, st));
-  h->dec_recorded = true;
+  if (k_pool != h->dec_kp || v_pool != h->dec_vp) {
+    // the pool as uint8 [n_pool * 16][HKV][256]; a box is one kv head's 16 token rows of half the dims
+    const uint64_t dims[3] = {(uint64_t)kHeadDim, (uint64_t)h->HKV, (uint64_t)h->n_pool * kPage};
+    const uint64_t strides[2] = {(uint64_t)kHeadDim, (uint64_t)h->HKV * kHeadDim};
+    const uint32_t box[3] = {128, 1, (uint32_t)kPage};
+    h->dec_kp = h->dec_vp = nullptr;
+    if ((rc = encode(&h->dec_maps.k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, k_pool, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B)) ||
+        (rc = encode(&h->dec_maps.v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, v_pool, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B)))
+      return rc;
+    h->dec_kp = k_pool;
+    h->dec_vp = v_pool;
+  }
   DecodeParams p{};
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.out = static_cast<__nv_bfloat16*>(out);
@@ -1041,15 +1051,31 @@ int pa_decode(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const i
   p.block_table = block_table;
   p.bt_stride = h->max_pages;
   p.n_pool = h->n_pool;
-  p.seqs = h->d_dec;
+  p.S = n_sink_blk;
+  p.W = n_win_blk;
   p.HQ = h->HQ;
   p.HKV = h->HKV;
   p.G = h->G;
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.part = h->d_part;
-  p.max_splits = max_splits;
+  p.tickets = h->d_tickets;
   p.err = h->d_err;
-  PA_CUDA(launch_decode(p, n_seq, st));
+  p.wait_ns = (unsigned long long)h->opt.wait_timeout_ms * 1000000ull;
+  DecodeSeqs tab;
+  for (const Launch& L : launches) {
+    int vstart = 0;
+    for (int i = 0; i < L.n; ++i) {
+      const pa_seq& q1 = seqs[L.s0 + i];
+      tab.seq[i] = make_int4(q1.q_off, q1.n_ctx, vstart, 0);
+      vstart += n_vis[(size_t)(L.s0 + i)];
+    }
+    p.n_seq = L.n;
+    p.bt_row0 = L.s0;
+    p.total = L.total;
+    p.per_cta = L.per_cta;
+    p.max_slots = L.max_slots;
+    PA_CUDA(launch_decode(p, tab, h->dec_maps, L.n_cta, st));
+  }
   return PA_OK;
 }
 

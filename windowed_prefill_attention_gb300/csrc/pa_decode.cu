@@ -8,24 +8,37 @@
 //
 // Decode reads every visible K/V code once and does 2 x G x 256 flops per
 // code (G = q heads per kv head, <= 8): it is bound by HBM, not the tensor
-// core.  So the int8 pool is read directly (no widening pass), a CTA takes 64
-// blocks (1024 keys) of one (sequence, kv head), and the small products run
-// on warp-level MMAs (mma.sync m16n8k16, fp16 containers, fp32 accumulate) in
-// the transposed orientation, S^T = K Q^T and O^T = V^T P^T, so that keys and
-// head dims fill M = 16 and the G query rows fill N = 8 with no padding.  In
-// both the thread holds rows 2t, 2t+1 (t = lane % 4): the online-softmax state
-// stays in registers.  Codes become exact fp16 pairs with one byte permute and
-// one subtraction; the query enters as fp16 through a per-row power-of-two
-// scale (lossless for bf16 input); P' = p * v_scale is normalised by the
-// largest V scale the warp has met so far (a running power of two, rescaled
-// like the running max) so that it stays in fp16's normal range.
+// core.  So the int8 pool is read directly (no widening pass) and the small
+// products run on warp-level MMAs (mma.sync m16n8k16, fp16 containers, fp32
+// accumulate) in the transposed orientation, S^T = K Q^T and O^T = V^T P^T,
+// so that keys and head dims fill M = 16 and the G query rows fill N = 8 with
+// no padding.  In both the thread holds rows 2t, 2t+1 (t = lane % 4): the
+// online-softmax state stays in registers.  Codes become exact fp16 pairs
+// with byte permutes and one subtraction; the query enters as fp16 through a
+// per-row power-of-two scale (lossless for bf16 input); P' = p * v_scale is
+// normalised by the largest V scale the warp has met so far (a running power
+// of two, rescaled like the running max) so that it stays in fp16's normal
+// range.
 //
-// decode_split_kernel   one CTA per (sequence, kv head, split): 4 warps take
-//                       the split's blocks in turn (two cp.async stages per
-//                       warp), then combine in shared memory into one partial
-//                       (row max, row sum, unnormalised O) per q head
-// decode_combine_kernel one CTA per (sequence, q head): merges the splits'
-//                       partials and writes bf16
+// Data movement: each warp owns a ring of kDecStages block slots in shared
+// memory; one lane fills them with TMA copies (a kv head's 16 token rows of a
+// K page and of a V page, each as two 128-byte-swizzled halves, plus the
+// page's scales by a bulk copy), completing on the slot's mbarrier, so a
+// warp has kDecStages blocks (kDecStages x 8 KB) in flight while it computes.
+// Operand layout: the head dims of a block are permuted (the sum over dims in
+// S^T is the same in any order; Q takes the same permutation, O^T is put back
+// in order when written), so that every thread reads its K and V operands as
+// 16-byte words of the swizzled rows instead of gathering bytes.
+//
+// Work split: the launch's (sequence, kv head) pairs laid end to end give one
+// list of visible blocks; CTA c takes blocks [c B, c B + B) of it, B chosen so
+// that the grid is one wave of equal CTAs (or whole waves of 128-block CTAs).
+// A CTA's run covers one or more segments (the part of a run that falls in
+// one pair).  Per segment its 4 warps take the blocks in turn, then combine in
+// shared memory: a segment that is a whole pair writes bf16 out directly;
+// otherwise it writes a partial (row max, row sum, unnormalised O per q head)
+// and adds its block count to the pair's ticket, and the CTA that completes
+// the count merges the pair's partials and writes bf16 out.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -39,18 +52,24 @@ namespace pa {
 namespace {
 
 constexpr int kDecWarps = 4;
-constexpr int kRowPitch = 272;                       // staged code row: 256 B + 16 (bank spread, 16-B aligned)
-constexpr int kStagePage = kPage * kRowPitch;        // 4352
-constexpr int kStageBuf = 2 * kStagePage + 128;      // K page, V page, 16 K + 16 V scales
-constexpr int kSmQF = 0;                             // Q fragments [16 k-steps][32 lanes] x 8 B
-constexpr int kSmRowC = kSmQF + 16 * 32 * 8;         // c_row[8] floats
-constexpr int kSmRed = kSmRowC + 128;                // reduction scratch (32 floats)
-constexpr int kStages = 2;                           // copies in flight per warp: kStages - 1 blocks ahead
-constexpr int kSmWarp = kSmRed + 128;                // per warp: kStages stage buffers
-constexpr int kDecSmem = kSmWarp + kDecWarps * kStages * kStageBuf;
-// combine area (aliases the stage buffers once every copy has landed)
-constexpr int kCombFloats = 8 + 8 + 256 * 8;         // per warp: m[8], l[8], O^T[256][8]
-static_assert(kDecWarps * kCombFloats * 4 <= kDecWarps * kStages * kStageBuf, "combine area fits the stage buffers");
+constexpr int kDecStages = 2;                        // block slots (copies in flight) per warp
+constexpr int kHalfBytes = kPage * 128;              // 16 rows x 128 dims (one TMA box)
+constexpr int kBlockBytes = 4 * kHalfBytes;          // K halves 0, 1, then V halves 0, 1
+constexpr int kSlotsBytes = kDecWarps * kDecStages * kBlockBytes;
+// Shared memory from a 1024-byte aligned base: the block slots, then per slot
+// the page's scales (K: 16 tokens x HKV floats, then V likewise), the Q
+// fragments [16 k-steps][32 lanes] x 8 B (between segments: the combine
+// area, 128 dims x 8 rows of fp32), small per-row values, the slots' barriers.
+__host__ __device__ constexpr int dec_scale_bytes(int HKV) { return 2 * kPage * HKV * 4; }
+__host__ __device__ constexpr int dec_sm_scales() { return kSlotsBytes; }
+__host__ __device__ constexpr int dec_sm_qf(int HKV) { return kSlotsBytes + kDecWarps * kDecStages * dec_scale_bytes(HKV); }
+__host__ __device__ constexpr int dec_sm_misc(int HKV) { return dec_sm_qf(HKV) + 16 * 32 * 8; }
+__host__ __device__ constexpr int dec_sm_bars(int HKV) { return dec_sm_misc(HKV) + 512; }
+__host__ __device__ constexpr int dec_smem(int HKV) { return dec_sm_bars(HKV) + kDecWarps * kDecStages * 8 + 1024; }
+// misc floats: row factors of Q [0, 8), per-warp row max / row sum [8, 72),
+// the segment's row max / row sum [72, 88), the "last segment" flag at 88
+constexpr int kMiscRowc = 0, kMiscWarp = 8, kMiscSeg = 72, kMiscFlag = 88;
+constexpr uint64_t kDecDrainNs = 200000000ull;
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -66,13 +85,16 @@ __device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
   return y;
 }
-// Two int8 codes (bytes 0 and 1 of w) -> the f16 pair holding them exactly:
-// byte b -> bits 0x64 | (b ^ 0x80) = 1024 + 128 + b as fp16, minus 1152.
-__device__ __forceinline__ uint32_t codes2_to_f16x2(uint32_t w) {
-  const uint32_t u = __byte_perm(w ^ 0x8080u, 0x6464u, 0x5140u);
+// Codes held as (b ^ 0x80) in the low bytes of fp16 0x64__ are 1152 + b: the
+// pair minus 1152 is the pair of codes, exactly.
+__device__ __forceinline__ uint32_t f16x2_minus_1152(uint32_t u) {
   const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&u), __half2half2(__ushort_as_half(0x6480u)));
   return *reinterpret_cast<const uint32_t*>(&h);
 }
+// Bytes 0, 1 (lo) or 2, 3 (hi) of a word of flipped codes (x = w ^ 0x80808080)
+// as the fp16 pair 1152 + code (before the subtraction).
+__device__ __forceinline__ uint32_t expand_lo(uint32_t x) { return __byte_perm(x, 0x64646464u, 0x5140); }
+__device__ __forceinline__ uint32_t expand_hi(uint32_t x) { return __byte_perm(x, 0x64646464u, 0x7362); }
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -82,283 +104,522 @@ __device__ __forceinline__ float ex2f(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
 }
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+// 16-byte chunk c (0..7) of row r of a 128-byte-swizzled box: chunks are
+// permuted by the row index mod 8, as the TMA copy writes them.
+__device__ __forceinline__ uint32_t swz128(uint32_t half_base, int r, int c) {
+  return half_base + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
+// A sequence's decode geometry (from the launch's table entry).
+struct DecSeq {
+  int q_row;   // row of the query token in q / out
+  int t;       // its position in the context (n_ctx - 1)
+  int vstart;  // visible blocks of the launch's earlier sequences (per kv head)
+  int n_sink;  // sink blocks listed ahead of the window run
+  int lo;      // first block of the window run (0 with the window off)
+  int n_vis;   // visible blocks
+};
+__device__ __forceinline__ DecSeq dec_seq(const DecodeParams& p, const DecodeSeqs& tab, int s) {
+  const int4 e = tab.seq[s];
+  DecSeq d;
+  d.q_row = e.x;
+  d.t = e.y - 1;
+  d.vstart = e.z;
+  const int last = d.t / kPage;
+  d.lo = p.W > 0 ? max(0, last + 1 - p.W) : 0;
+  d.n_sink = p.W > 0 ? min(max(p.S, 0), d.lo) : 0;
+  d.n_vis = d.n_sink + (last - d.lo + 1);
+  return d;
+}
 // Logical key block of the b-th visible block of a sequence.
 __device__ __forceinline__ int dec_block(const DecSeq& d, int b) { return b < d.n_sink ? b : d.lo + (b - d.n_sink); }
 
-__global__ void __launch_bounds__(kDecWarps * 32) decode_split_kernel(const DecodeParams p) {
-  extern __shared__ __align__(128) uint8_t dsm[];
-  const int sp = blockIdx.x % p.max_splits;
-  const int g = (blockIdx.x / p.max_splits) % p.HKV;
-  const int s = blockIdx.x / (p.max_splits * p.HKV);
-  const DecSeq ds = p.seqs[s];
-  if (sp >= ds.n_splits) return;  // the whole CTA
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gq = lane >> 2, tq = lane & 3;
-  const int blk0 = sp * ds.per_split, blk1 = min(ds.n_vis, blk0 + ds.per_split);
-  uint2* qf = reinterpret_cast<uint2*>(dsm + kSmQF);
-  float* c_rows = reinterpret_cast<float*>(dsm + kSmRowC);
-
-  // 1. The kv head's G query rows -> fp16 B fragments of Q^T, each row scaled
-  // by the power of two that puts its absmax in [64, 128).  Thread: row r,
-  // dims [16 c, 16 c + 16).  Rows >= G are zero.
-  {
-    const int r = threadIdx.x >> 4, c = threadIdx.x & 15;
-    float v[16];
-    float am = 0.f;
-    if (r < p.G) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)ds.q_row * p.HQ + (size_t)g * p.G + r) * kHeadDim +
-                                                        c * 16);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint4 w = src[h];
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          v[8 * h + 2 * e] = __uint_as_float(ww[e] << 16);
-          v[8 * h + 2 * e + 1] = __uint_as_float(ww[e] & 0xffff0000u);
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < 16; ++e) am = fmaxf(am, fabsf(v[e]));
-    } else {
-#pragma unroll
-      for (int e = 0; e < 16; ++e) v[e] = 0.f;
-    }
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-    const int k = am > 0.f ? min(127, 133 - (int)((__float_as_uint(am) >> 23) & 0xff)) : 0;
-    const float mul = __uint_as_float((uint32_t)(127 + k) << 23);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {  // dims 16c + 2i, +1: k-step c, column pair 2i
-      const uint32_t pr = pack_f16x2(v[2 * i] * mul, v[2 * i + 1] * mul);
-      uint2* slot = &qf[c * 32 + 4 * r + (i & 3)];
-      if (i < 4) slot->x = pr;
-      else slot->y = pr;
-    }
-    if (c == 0) c_rows[r] = r < p.G ? __uint_as_float((uint32_t)(127 - k) << 23) * p.sm_scale_log2 : 0.f;
+// Position of the pairs in the launch's block list: pair (s, g) starts at
+// HKV vstart(s) + g n_vis(s).
+struct PairPos {
+  int s, g, start;
+  DecSeq d;
+};
+// The pair that holds block x (0 <= x < total): the last sequence whose first
+// block is at or before x (binary search over the table), then the kv head.
+__device__ __forceinline__ PairPos dec_locate(const DecodeParams& p, const DecodeSeqs& tab, int x) {
+  int lo = 0, hi = p.n_seq - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.HKV * tab.seq[mid].z <= x) lo = mid;
+    else hi = mid - 1;
   }
-  __syncthreads();
-  const float c_lo = c_rows[2 * tq], c_hi = c_rows[2 * tq + 1];
-
-  // 2. This warp's blocks: blk0 + warp, + 4, ...  P' = p * v_scale * 2^-ev
-  // with ev the exponent of the largest V scale the warp has met so far
-  // (2^(ev-1) <= max < 2^ev, so P' <= 1); when a block raises it, O is
-  // rescaled by the exact power of two, like the running max.
-  const uint32_t stage0 = smem_u32(dsm + kSmWarp + warp * kStages * kStageBuf);
-  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
-  int ev = -100;
-  float o[16][4];
-#pragma unroll
-  for (int mt = 0; mt < 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-
-  // blocks of this warp: blk0 + warp + 4 i, i = 0 .. n_mine-1 (n_mine <= 32);
-  // lane i holds block i's pool page, read once up front
-  const int n_mine = blk1 > blk0 + warp ? (blk1 - blk0 - warp + kDecWarps - 1) / kDecWarps : 0;
-  const int my_page = lane < n_mine ? p.block_table[(size_t)ds.bt_row * p.bt_stride +
-                                                    dec_block(ds, blk0 + warp + kDecWarps * lane)]
-                                    : -1;
-  // copy block i's K and V codes (16 rows of 256 B each) and scales
-  auto issue = [&](int i, uint32_t buf) -> bool {
-    const int phys = __shfl_sync(0xffffffffu, my_page, i);
-    if (phys < 0 || phys >= p.n_pool) return false;
-    const size_t row0 = (size_t)phys * kPage * p.HKV + g;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {  // 16 rows x 16 chunks of 16 B, K then V
-      const int ch = lane + 32 * i, key = ch >> 4, cc = ch & 15;
-      const size_t src = (row0 + (size_t)key * p.HKV) * kHeadDim + cc * 16;
-      cp_async16(buf + key * kRowPitch + cc * 16, p.k_pool + src);
-      cp_async16(buf + kStagePage + key * kRowPitch + cc * 16, p.v_pool + src);
-    }
-    const float* sc = lane < 16 ? p.k_scale : p.v_scale;
-    cp_async4(buf + 2 * kStagePage + lane * 4, sc + row0 + (size_t)(lane & 15) * p.HKV);
-    return true;
-  };
-
-  // block i goes to stage i % kStages
-  uint32_t live_bits = 0;  // bit i: block i's page entry was in range
-#pragma unroll
-  for (int i = 0; i < kStages - 1; ++i) {
-    if (i < n_mine && issue(i, stage0 + i * kStageBuf)) live_bits |= 1u << i;
-    cp_async_commit();
-  }
-  for (int it = 0; it < n_mine; ++it) {
-    const int b = blk0 + warp + kDecWarps * it;
-    const uint32_t buf = stage0 + (it % kStages) * kStageBuf;
-    const int ia = it + kStages - 1;  // the block whose copy goes out now
-    if (ia < n_mine && issue(ia, stage0 + (ia % kStages) * kStageBuf)) live_bits |= 1u << ia;
-    cp_async_commit();
-    cp_async_wait<kStages - 1>();
-    __syncwarp();
-    const bool live = (live_bits >> it) & 1u;
-    if (!live) {
-      if (lane == 0) atomicCAS(p.err, 0, DEV_ERR_BAD_PAGE);
-    } else {
-      const uint8_t* kb = dsm + (buf - smem_u32(dsm));
-      const uint8_t* vb = kb + kStagePage;
-      const float* scl = reinterpret_cast<const float*>(kb + 2 * kStagePage);
-      // S^T = K Q^T: keys gq, gq+8 x rows 2tq, 2tq+1
-      float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};  // even / odd k-steps
-#pragma unroll
-      for (int kk = 0; kk < 16; ++kk) {
-        const int d0 = 16 * kk + 2 * tq;
-        uint32_t a[4];
-        a[0] = codes2_to_f16x2(*reinterpret_cast<const uint16_t*>(kb + gq * kRowPitch + d0));
-        a[1] = codes2_to_f16x2(*reinterpret_cast<const uint16_t*>(kb + (gq + 8) * kRowPitch + d0));
-        a[2] = codes2_to_f16x2(*reinterpret_cast<const uint16_t*>(kb + gq * kRowPitch + d0 + 8));
-        a[3] = codes2_to_f16x2(*reinterpret_cast<const uint16_t*>(kb + (gq + 8) * kRowPitch + d0 + 8));
-        const uint2 bq = qf[kk * 32 + lane];
-        if (kk & 1) mma16816(sacc2, a, bq.x, bq.y);
-        else mma16816(sacc, a, bq.x, bq.y);
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sacc[e] += sacc2[e];
-      // scores in log2 units; keys past the query position masked
-      const int lb = dec_block(ds, b);
-      const bool v0 = lb * kPage + gq <= ds.t, v1 = lb * kPage + gq + 8 <= ds.t;
-      const float ks0 = scl[gq], ks1 = scl[gq + 8];
-      const float y0 = v0 ? sacc[0] * ks0 * c_lo : -INFINITY, y1 = v0 ? sacc[1] * ks0 * c_hi : -INFINITY;
-      const float y2 = v1 ? sacc[2] * ks1 * c_lo : -INFINITY, y3 = v1 ? sacc[3] * ks1 * c_hi : -INFINITY;
-      float bm_lo = fmaxf(y0, y2), bm_hi = fmaxf(y1, y3);
-#pragma unroll
-      for (int x = 4; x < 32; x <<= 1) {
-        bm_lo = fmaxf(bm_lo, __shfl_xor_sync(0xffffffffu, bm_lo, x));
-        bm_hi = fmaxf(bm_hi, __shfl_xor_sync(0xffffffffu, bm_hi, x));
-      }
-      const float mn_lo = fmaxf(m_lo, bm_lo), mn_hi = fmaxf(m_hi, bm_hi);  // finite: key 0 of a block is visible
-      // the block's largest V scale (scale slots 16..31 hold them)
-      float bv = (lane >= 16 && lb * kPage + (lane - 16) <= ds.t) ? scl[lane] : 0.f;
-#pragma unroll
-      for (int x = 16; x > 0; x >>= 1) bv = fmaxf(bv, __shfl_xor_sync(0xffffffffu, bv, x));
-      const int evb = bv > 0.f ? max(-100, min(100, (int)((__float_as_uint(bv) >> 23) & 0xff) - 126)) : -100;
-      // 2^(ev - evb) when the block raises ev; past 2^-126 the older terms are below fp32 resolution
-      const int dev = evb - ev;
-      const float vfix = dev <= 0 ? 1.f : (dev > 126 ? 0.f : __uint_as_float((uint32_t)(127 - dev) << 23));
-      ev = max(ev, evb);
-      const float vnorm = __uint_as_float((uint32_t)(127 - ev) << 23);
-      const float al_lo = ex2f(m_lo - mn_lo), al_hi = ex2f(m_hi - mn_hi);
-      m_lo = mn_lo;
-      m_hi = mn_hi;
-      const float p0 = ex2f(y0 - mn_lo), p1 = ex2f(y1 - mn_hi), p2 = ex2f(y2 - mn_lo), p3 = ex2f(y3 - mn_hi);
-      l_lo = l_lo * al_lo + (p0 + p2);
-      l_hi = l_hi * al_hi + (p1 + p3);
-      if (__any_sync(0xffffffffu, al_lo != 1.f || al_hi != 1.f || vfix != 1.f)) {
-        const float f_lo = al_lo * vfix, f_hi = al_hi * vfix;
-#pragma unroll
-        for (int mt = 0; mt < 16; ++mt) {
-          o[mt][0] *= f_lo;
-          o[mt][1] *= f_hi;
-          o[mt][2] *= f_lo;
-          o[mt][3] *= f_hi;
-        }
-      }
-      // P' = p * v_scale * 2^-ev (masked keys: 0, whatever their scale slot
-      // holds), as the B fragments of P^T
-      const float vs0 = v0 ? scl[16 + gq] * vnorm : 0.f, vs1 = v1 ? scl[16 + gq + 8] * vnorm : 0.f;
-      const uint32_t pb0 = transpose8x8(pack_f16x2(v0 ? p0 * vs0 : 0.f, v0 ? p1 * vs0 : 0.f));
-      const uint32_t pb1 = transpose8x8(pack_f16x2(v1 ? p2 * vs1 : 0.f, v1 ? p3 * vs1 : 0.f));
-      // O^T += V^T P^T: dims 16 mt + gq (+8) x rows 2tq, 2tq+1
-#pragma unroll
-      for (int mt = 0; mt < 16; ++mt) {
-        const int d = 16 * mt + gq;
-        const uint8_t* r0 = vb + (2 * tq) * kRowPitch + d;
-        const uint8_t* r8 = r0 + 8 * kRowPitch;
-        uint32_t a[4];
-        a[0] = codes2_to_f16x2((uint32_t)r0[0] | ((uint32_t)r0[kRowPitch] << 8));
-        a[1] = codes2_to_f16x2((uint32_t)r0[8] | ((uint32_t)r0[kRowPitch + 8] << 8));
-        a[2] = codes2_to_f16x2((uint32_t)r8[0] | ((uint32_t)r8[kRowPitch] << 8));
-        a[3] = codes2_to_f16x2((uint32_t)r8[8] | ((uint32_t)r8[kRowPitch + 8] << 8));
-        mma16816(o[mt], a, pb0, pb1);
-      }
-    }
-    __syncwarp();  // every lane is done with this buffer before it is refilled
-  }
-  cp_async_wait<0>();
-  // row sums over the warp's lanes that share tq
-#pragma unroll
-  for (int x = 4; x < 32; x <<= 1) {
-    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, x);
-    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, x);
-  }
-  __syncthreads();  // every warp's copies have landed: the stage area becomes the combine area
-
-  // 3. Combine the four warps in shared memory into the split's partial.
-  float* comb = reinterpret_cast<float*>(dsm + kSmWarp);
-  float* mine = comb + warp * kCombFloats;
-  if (gq == 0) {
-    mine[2 * tq] = m_lo;
-    mine[2 * tq + 1] = m_hi;
-    mine[8 + 2 * tq] = l_lo;
-    mine[8 + 2 * tq + 1] = l_hi;
-  }
-  const float vden = __uint_as_float((uint32_t)(127 + max(ev, -126)) << 23);  // O back to true V units: x 2^ev
-#pragma unroll
-  for (int mt = 0; mt < 16; ++mt) {
-    const int d = 16 * mt + gq;
-    *reinterpret_cast<float2*>(mine + 16 + d * 8 + 2 * tq) = make_float2(o[mt][0] * vden, o[mt][1] * vden);
-    *reinterpret_cast<float2*>(mine + 16 + (d + 8) * 8 + 2 * tq) = make_float2(o[mt][2] * vden, o[mt][3] * vden);
-  }
-  __syncthreads();
-  for (int r = 0; r < p.G; ++r) {
-    float mx = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) mx = fmaxf(mx, comb[w * kCombFloats + r]);
-    float wt[kDecWarps];
-    float ls = 0.f;
-#pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) {
-      const float mw = comb[w * kCombFloats + r];
-      wt[w] = mw == -INFINITY ? 0.f : ex2f(mw - mx);
-      ls += wt[w] * comb[w * kCombFloats + 8 + r];
-    }
-    float* part = p.part + (((size_t)s * p.HQ + (size_t)g * p.G + r) * p.max_splits + sp) * kDecPartStride;
-    if (threadIdx.x == 0) {
-      part[0] = mx;
-      part[1] = ls;
-    }
-    for (int d = threadIdx.x; d < kHeadDim; d += kDecWarps * 32) {
-      float acc = 0.f;
-#pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) acc += wt[w] * comb[w * kCombFloats + 16 + d * 8 + r];
-      part[4 + d] = acc;
-    }
+  PairPos r;
+  r.s = lo;
+  r.d = dec_seq(p, tab, lo);
+  r.g = (x - p.HKV * r.d.vstart) / r.d.n_vis;
+  r.start = p.HKV * r.d.vstart + r.g * r.d.n_vis;
+  return r;
+}
+__device__ __forceinline__ void dec_next_pair(const DecodeParams& p, const DecodeSeqs& tab, PairPos& r) {
+  r.start += r.d.n_vis;
+  if (++r.g == p.HKV) {
+    r.g = 0;
+    ++r.s;
+    r.d = dec_seq(p, tab, r.s);
   }
 }
 
-__global__ void __launch_bounds__(kHeadDim) decode_combine_kernel(const DecodeParams p) {
-  const int s = blockIdx.x / p.HQ, h = blockIdx.x % p.HQ;
-  const DecSeq ds = p.seqs[s];
-  const float* part = p.part + ((size_t)s * p.HQ + h) * p.max_splits * kDecPartStride;
-  float mx = -INFINITY;
-  for (int i = 0; i < ds.n_splits; ++i) mx = fmaxf(mx, part[i * kDecPartStride]);
-  float l = 0.f, acc = 0.f;
-  const int d = threadIdx.x;
-  for (int i = 0; i < ds.n_splits; ++i) {
-    const float w = ex2f(part[i * kDecPartStride] - mx);
-    l += w * part[i * kDecPartStride + 1];
-    acc += w * part[i * kDecPartStride + 4 + d];
+// The kv head's G query rows -> fp16 B fragments of Q^T, each row scaled by
+// the power of two that puts its absmax in [64, 128).  Thread: row r, dims
+// [16 c, 16 c + 16).  Rows >= G are zero.  Dims are permuted as the K operand
+// is: k-step 4 j + m, lane (row, t) holds dims 64 j + 16 t + 4 m + {0, 1} and
+// + {2, 3}.  Row factors (2^-k * sm_scale * log2 e) go to c_rows.
+__device__ __forceinline__ void dec_load_q(const DecodeParams& p, int q_row, int g, uint2* qf, float* c_rows) {
+  const int r = threadIdx.x >> 4, c = threadIdx.x & 15;
+  float v[16];
+  float am = 0.f;
+  if (r < p.G) {
+    const uint4* src =
+        reinterpret_cast<const uint4*>(p.q + ((size_t)q_row * p.HQ + (size_t)g * p.G + r) * kHeadDim + c * 16);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 w = src[h];
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[8 * h + 2 * e] = __uint_as_float(ww[e] << 16);
+        v[8 * h + 2 * e + 1] = __uint_as_float(ww[e] & 0xffff0000u);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 16; ++e) am = fmaxf(am, fabsf(v[e]));
+  } else {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = 0.f;
   }
-  p.out[((size_t)ds.q_row * p.HQ + h) * kHeadDim + d] = __float2bfloat16_rn(l > 0.f ? acc / l : 0.f);
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+  const int k = am > 0.f ? min(127, 133 - (int)((__float_as_uint(am) >> 23) & 0xff)) : 0;
+  const float mul = __uint_as_float((uint32_t)(127 + k) << 23);
+#pragma unroll
+  for (int m = 0; m < 4; ++m)  // dims 16 c + 4 m + {0..3}: k-step 4 (c / 4) + m, lane (r, c % 4)
+    qf[(4 * (c >> 2) + m) * 32 + 4 * r + (c & 3)] =
+        make_uint2(pack_f16x2(v[4 * m] * mul, v[4 * m + 1] * mul), pack_f16x2(v[4 * m + 2] * mul, v[4 * m + 3] * mul));
+  if (c == 0) c_rows[r] = r < p.G ? __uint_as_float((uint32_t)(127 - k) << 23) * p.sm_scale_log2 : 0.f;
+}
+
+__global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(const __grid_constant__ DecodeParams p,
+                                                                const __grid_constant__ DecodeSeqs tab,
+                                                                const __grid_constant__ CUtensorMap km,
+                                                                const __grid_constant__ CUtensorMap vm) {
+  extern __shared__ uint8_t draw[];
+  uint8_t* dsm = draw + ((1024u - (smem_u32(draw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(dsm);
+  const int HKV = p.HKV;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  uint2* qf = reinterpret_cast<uint2*>(dsm + dec_sm_qf(HKV));
+  float* comb = reinterpret_cast<float*>(dsm + dec_sm_qf(HKV));  // between segments
+  float* misc = reinterpret_cast<float*>(dsm + dec_sm_misc(HKV));
+  const uint32_t bars = sbase + dec_sm_bars(HKV);
+  const WaitCtl wc{p.err, p.wait_ns};
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kDecWarps * kDecStages; ++i) mbar_init(bars + 8 * i, 1);
+    fence_mbar_init();
+    tma_prefetch_map(&km);
+    tma_prefetch_map(&vm);
+  }
+  // this CTA's run of the launch's block list
+  const int x0 = (int)blockIdx.x * p.per_cta, x1 = min(p.total, x0 + p.per_cta);
+  PairPos pp = dec_locate(p, tab, x0);
+
+  // 1. This warp's blocks: x0 + warp + 4 i, i < n_mine (<= 32).  Lane i looks
+  // up block i's pool page and kv head once, walking the pairs from the
+  // run's first.  Block i goes to slot i % kDecStages, whose barrier
+  // completes once its copies landed.
+  const int n_mine = x1 > x0 + warp ? (x1 - x0 - warp + kDecWarps - 1) / kDecWarps : 0;
+  int my_page = -1, my_g = 0;
+  if (lane < n_mine) {
+    const int x = x0 + warp + kDecWarps * lane;
+    PairPos q = pp;
+    while (x >= q.start + q.d.n_vis) dec_next_pair(p, tab, q);
+    my_g = q.g;
+    my_page = p.block_table[(size_t)(p.bt_row0 + q.s) * p.bt_stride + dec_block(q.d, x - q.start)];
+  }
+  const uint32_t slot0 = sbase + (uint32_t)(warp * kDecStages * kBlockBytes);
+  const uint32_t scl0 = sbase + (uint32_t)(dec_sm_scales() + warp * kDecStages * dec_scale_bytes(HKV));
+  const uint32_t bar0 = bars + (uint32_t)(warp * kDecStages * 8);
+  const uint32_t tx_bytes = (uint32_t)(kBlockBytes + dec_scale_bytes(HKV));
+  __syncthreads();  // the slots' barriers exist before any copy completes on them
+
+  // copy block i (a warp-wide call: page and kv head come from lane i); a
+  // page entry outside the pool copies nothing and completes the slot's phase
+  auto issue = [&](int i) {
+    const int phys = __shfl_sync(0xffffffffu, my_page, i);
+    const int gi = __shfl_sync(0xffffffffu, my_g, i);
+    if (lane != 0) return;
+    const int st = i % kDecStages;
+    const uint32_t bar = bar0 + 8 * st;
+    if (phys < 0 || phys >= p.n_pool) {
+      mbar_arrive(bar);
+      return;
+    }
+    const uint32_t dst = slot0 + (uint32_t)(st * kBlockBytes);
+    mbar_expect_tx(bar, tx_bytes);
+    tma_load_3d(dst, &km, bar, 0, gi, phys * kPage);
+    tma_load_3d(dst + kHalfBytes, &km, bar, 128, gi, phys * kPage);
+    tma_load_3d(dst + 2 * kHalfBytes, &vm, bar, 0, gi, phys * kPage);
+    tma_load_3d(dst + 3 * kHalfBytes, &vm, bar, 128, gi, phys * kPage);
+    const size_t so = (size_t)phys * kPage * HKV;
+    const uint32_t sd = scl0 + (uint32_t)(st * dec_scale_bytes(HKV));
+    bulk_load(sd, p.k_scale + so, (uint32_t)(kPage * HKV * 4), bar);
+    bulk_load(sd + kPage * HKV * 4, p.v_scale + so, (uint32_t)(kPage * HKV * 4), bar);
+  };
+  // the first copies go out before the query setup, which they overlap
+  int issued = min(kDecStages, n_mine);
+  for (int i = 0; i < issued; ++i) issue(i);
+
+  int it = 0;         // this warp's next block
+  int waited = 0;     // blocks whose slot phase this warp has waited for
+  bool ok = true;     // false once a wait gave up: the warp computes nothing more
+  for (int x = x0; x < x1;) {  // segments
+    const int seg_end = min(x1, pp.start + pp.d.n_vis);
+    const DecSeq ds = pp.d;
+    const int g = pp.g;
+    dec_load_q(p, ds.q_row, g, qf, misc + kMiscRowc);
+    __syncthreads();
+    const float c_lo = misc[kMiscRowc + 2 * tq], c_hi = misc[kMiscRowc + 2 * tq + 1];
+
+    float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+    // P' = p * v_scale * 2^-ev with ev the exponent of the largest V scale the
+    // warp has met so far in the segment (2^(ev-1) <= max < 2^ev, so P' <= 1);
+    // when a block raises it, O is rescaled by the exact power of two, like
+    // the running max.
+    int ev = -100;
+    float o[16][4];
+#pragma unroll
+    for (int mt = 0; mt < 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+    // 2. The segment's blocks of this warp, in turn, as their copies land.
+    for (; it < n_mine && x0 + warp + kDecWarps * it < seg_end; ++it) {
+      const int st = it % kDecStages;
+      if (ok && !__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * st, (uint32_t)(it / kDecStages) & 1u, wc, 60)))
+        ok = false;
+      if (!ok) continue;
+      ++waited;
+      const int b = x0 + warp + kDecWarps * it - pp.start;
+      const int phys = __shfl_sync(0xffffffffu, my_page, it);
+      if (phys < 0 || phys >= p.n_pool) {
+        if (lane == 0) atomicCAS(p.err, 0, DEV_ERR_BAD_PAGE);
+      } else {
+        const uint32_t kb = slot0 + (uint32_t)(st * kBlockBytes), vb = kb + 2 * kHalfBytes;
+        const float* kscl = reinterpret_cast<const float*>(dsm + (scl0 - sbase) + st * dec_scale_bytes(HKV)) + g;
+        const float* vscl = kscl + kPage * HKV;
+        // S^T = K Q^T: keys gq, gq+8 x rows 2tq, 2tq+1.  Dims group j (64 dims,
+        // 4 k-steps): this thread's 16 bytes of rows gq and gq+8, dims
+        // 64 j + 16 tq + [0, 16); k-step 4 j + m takes word m (dims + 4m .. + 3).
+        float sacc[4][4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) sacc[m][0] = sacc[m][1] = sacc[m][2] = sacc[m][3] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t hb = kb + (uint32_t)((j >> 1) * kHalfBytes);
+          const int c = 4 * (j & 1) + tq;
+          const uint4 r0 = lds128(swz128(hb, gq, c)), r1 = lds128(swz128(hb, gq + 8, c));
+          const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w1[4] = {r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const uint32_t x0w = w0[m] ^ 0x80808080u, x1w = w1[m] ^ 0x80808080u;
+            uint32_t a[4];
+            a[0] = f16x2_minus_1152(expand_lo(x0w));
+            a[1] = f16x2_minus_1152(expand_lo(x1w));
+            a[2] = f16x2_minus_1152(expand_hi(x0w));
+            a[3] = f16x2_minus_1152(expand_hi(x1w));
+            const uint2 bq = qf[(4 * j + m) * 32 + lane];
+            mma16816(sacc[m], a, bq.x, bq.y);  // four independent chains
+          }
+        }
+        float sc[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[e] = (sacc[0][e] + sacc[1][e]) + (sacc[2][e] + sacc[3][e]);
+        // scores in log2 units; keys past the query position masked
+        const int lb = dec_block(ds, b);
+        const bool v0 = lb * kPage + gq <= ds.t, v1 = lb * kPage + gq + 8 <= ds.t;
+        const float ks0 = kscl[gq * HKV], ks1 = kscl[(gq + 8) * HKV];
+        const float y0 = v0 ? sc[0] * ks0 * c_lo : -INFINITY, y1 = v0 ? sc[1] * ks0 * c_hi : -INFINITY;
+        const float y2 = v1 ? sc[2] * ks1 * c_lo : -INFINITY, y3 = v1 ? sc[3] * ks1 * c_hi : -INFINITY;
+        float bm_lo = fmaxf(y0, y2), bm_hi = fmaxf(y1, y3);
+        // the block's largest V scale (lanes 16..31: the V scales of keys 0..15)
+        float bv = (lane >= 16 && lb * kPage + (lane - 16) <= ds.t) ? vscl[(lane - 16) * HKV] : 0.f;
+#pragma unroll
+        for (int sh = 4; sh < 32; sh <<= 1) {
+          bm_lo = fmaxf(bm_lo, __shfl_xor_sync(0xffffffffu, bm_lo, sh));
+          bm_hi = fmaxf(bm_hi, __shfl_xor_sync(0xffffffffu, bm_hi, sh));
+          bv = fmaxf(bv, __shfl_xor_sync(0xffffffffu, bv, sh));
+        }
+        bv = fmaxf(bv, __shfl_xor_sync(0xffffffffu, bv, 2));
+        bv = fmaxf(bv, __shfl_xor_sync(0xffffffffu, bv, 1));
+        const float mn_lo = fmaxf(m_lo, bm_lo), mn_hi = fmaxf(m_hi, bm_hi);  // finite: key 0 of a block is visible
+        const int evb = bv > 0.f ? max(-100, min(100, (int)((__float_as_uint(bv) >> 23) & 0xff) - 126)) : -100;
+        // 2^(ev - evb) when the block raises ev; past 2^-126 the older terms are below fp32 resolution
+        const int dev = evb - ev;
+        const float vfix = dev <= 0 ? 1.f : (dev > 126 ? 0.f : __uint_as_float((uint32_t)(127 - dev) << 23));
+        ev = max(ev, evb);
+        const float vnorm = __uint_as_float((uint32_t)(127 - ev) << 23);
+        const float al_lo = ex2f(m_lo - mn_lo), al_hi = ex2f(m_hi - mn_hi);
+        m_lo = mn_lo;
+        m_hi = mn_hi;
+        const float p0 = ex2f(y0 - mn_lo), p1 = ex2f(y1 - mn_hi), p2 = ex2f(y2 - mn_lo), p3 = ex2f(y3 - mn_hi);
+        l_lo = l_lo * al_lo + (p0 + p2);
+        l_hi = l_hi * al_hi + (p1 + p3);
+        if (__any_sync(0xffffffffu, al_lo != 1.f || al_hi != 1.f || vfix != 1.f)) {
+          const float f_lo = al_lo * vfix, f_hi = al_hi * vfix;
+#pragma unroll
+          for (int mt = 0; mt < 16; ++mt) {
+            o[mt][0] *= f_lo;
+            o[mt][1] *= f_hi;
+            o[mt][2] *= f_lo;
+            o[mt][3] *= f_hi;
+          }
+        }
+        // P' = p * v_scale * 2^-ev (masked keys: 0, whatever their scale slot
+        // holds), as the B fragments of P^T
+        const float vs0 = v0 ? vscl[gq * HKV] * vnorm : 0.f, vs1 = v1 ? vscl[(gq + 8) * HKV] * vnorm : 0.f;
+        const uint32_t pb0 = transpose8x8(pack_f16x2(v0 ? p0 * vs0 : 0.f, v0 ? p1 * vs0 : 0.f));
+        const uint32_t pb1 = transpose8x8(pack_f16x2(v1 ? p2 * vs1 : 0.f, v1 ? p3 * vs1 : 0.f));
+        // O^T += V^T P^T.  Dims are permuted: row gq of m-tile mt is dim
+        // 32 gq + 2 mt, row gq + 8 is dim 32 gq + 2 mt + 1, so this thread's A
+        // operands come from dims [32 gq, 32 gq + 32) of keys 2tq, 2tq+1, 2tq+8,
+        // 2tq+9: words i (dims 32 gq + 4 i .. + 3) feed m-tiles 2i and 2i+1.
+        // Bytes of a key pair are interleaved first ([k.d, k'.d, k.d+1, k'.d+1]),
+        // then each half widens to the fp16 pair (key, key') of one dim.
+        const uint32_t vh = vb + (uint32_t)((gq >> 2) * kHalfBytes);
+        const int key[4] = {2 * tq, 2 * tq + 1, 2 * tq + 8, 2 * tq + 9};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // dims 32 gq + 16 h .. + 15: words i = 4 h .. 4 h + 3
+          uint32_t w[4][4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 r = lds128(swz128(vh, key[k], 2 * (gq & 3) + h));
+            w[k][0] = r.x, w[k][1] = r.y, w[k][2] = r.z, w[k][3] = r.w;
+          }
+#pragma unroll
+          for (int ii = 0; ii < 4; ++ii) {
+            const int i = 4 * h + ii;
+            const uint32_t lo01 = __byte_perm(w[0][ii], w[1][ii], 0x5140) ^ 0x80808080u;  // dims + 0, + 1
+            const uint32_t hi01 = __byte_perm(w[0][ii], w[1][ii], 0x7362) ^ 0x80808080u;  // dims + 2, + 3
+            const uint32_t lo89 = __byte_perm(w[2][ii], w[3][ii], 0x5140) ^ 0x80808080u;
+            const uint32_t hi89 = __byte_perm(w[2][ii], w[3][ii], 0x7362) ^ 0x80808080u;
+            uint32_t a[4];
+            // m-tile 2i: dims + 0 (row gq) and + 1 (row gq + 8); keys (2tq, 2tq+1) and (2tq+8, 2tq+9)
+            a[0] = f16x2_minus_1152(expand_lo(lo01));
+            a[1] = f16x2_minus_1152(expand_hi(lo01));
+            a[2] = f16x2_minus_1152(expand_lo(lo89));
+            a[3] = f16x2_minus_1152(expand_hi(lo89));
+            mma16816(o[2 * i], a, pb0, pb1);
+            // m-tile 2i+1: dims + 2 and + 3
+            a[0] = f16x2_minus_1152(expand_lo(hi01));
+            a[1] = f16x2_minus_1152(expand_hi(hi01));
+            a[2] = f16x2_minus_1152(expand_lo(hi89));
+            a[3] = f16x2_minus_1152(expand_hi(hi89));
+            mma16816(o[2 * i + 1], a, pb0, pb1);
+          }
+        }
+      }
+      __syncwarp();  // every lane is done with this slot before it is refilled
+      if (it + kDecStages < n_mine) {
+        issue(it + kDecStages);
+        ++issued;
+      }
+    }
+    // row sums over the warp's lanes that share tq
+#pragma unroll
+    for (int sh = 4; sh < 32; sh <<= 1) {
+      l_lo += __shfl_xor_sync(0xffffffffu, l_lo, sh);
+      l_hi += __shfl_xor_sync(0xffffffffu, l_hi, sh);
+    }
+    float* wml = misc + kMiscWarp;
+    if (gq == 0) {
+      wml[warp * 16 + 2 * tq] = m_lo;
+      wml[warp * 16 + 2 * tq + 1] = m_hi;
+      wml[warp * 16 + 8 + 2 * tq] = l_lo;
+      wml[warp * 16 + 8 + 2 * tq + 1] = l_hi;
+    }
+    __syncthreads();  // every warp is done with the segment: its Q fragments area becomes the combine area
+
+    // 3. Combine the warps: this thread's rows 2tq, 2tq+1; the segment's row
+    // max and sum; each warp's factor (2^(m_w - max) and O back to true V
+    // units, x 2^ev).  A warp without blocks here has m = -inf and O = 0.
+    float f[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int r = 2 * tq + e;
+      float mx = -INFINITY, ls = 0.f;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) mx = fmaxf(mx, wml[w * 16 + r]);
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) {
+        const float mw = wml[w * 16 + r];
+        ls += mw == -INFINITY ? 0.f : ex2f(mw - mx) * wml[w * 16 + 8 + r];
+      }
+      const float mine = e ? m_hi : m_lo;
+      f[e] = mine == -INFINITY ? 0.f : ex2f(mine - mx) * __uint_as_float((uint32_t)(127 + max(ev, -126)) << 23);
+      if (warp == 0 && gq == 0) {
+        misc[kMiscSeg + r] = mx;
+        misc[kMiscSeg + 8 + r] = ls;
+      }
+    }
+    const int pair = pp.s * HKV + g;
+    const bool whole = x == pp.start && seg_end == pp.start + ds.n_vis;
+    const int slot = (int)blockIdx.x - pp.start / p.per_cta;
+    float* part = p.part + ((size_t)pair * p.max_slots + slot) * p.G * kDecPartStride;
+    __nv_bfloat16* out = p.out + ((size_t)ds.q_row * p.HQ + (size_t)g * p.G) * kHeadDim;
+    // Two rounds of 128 dims through the combine area, word (2 jj + e) * 32 +
+    // 4 gq + tq for row 2tq + e, dim 32 gq + 16 h + jj (jj = 2 (mt - 8 h) + {0, 1}):
+    // warp 0 stores, then warps 1, 2, 3 add in turn (a fixed order: the same
+    // inputs give the same bits); then thread (gq = t % 8, jj = t / 8) reads
+    // its dim's 8 rows as two float4.
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) {
+        if (warp == w) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float* oo = o[8 * h + q];
+            float* cw = comb + (4 * q) * 32 + 4 * gq + tq;  // jj = 2q: words 2jj, 2jj+1; jj = 2q+1: 2jj+2, 2jj+3
+            const float v0 = oo[0] * f[0], v1 = oo[1] * f[1], v2 = oo[2] * f[0], v3 = oo[3] * f[1];
+            if (w == 0) {
+              cw[0] = v0;
+              cw[32] = v1;
+              cw[64] = v2;
+              cw[96] = v3;
+            } else {
+              cw[0] += v0;
+              cw[32] += v1;
+              cw[64] += v2;
+              cw[96] += v3;
+            }
+          }
+        }
+        __syncthreads();
+      }
+      {
+        const int rg = threadIdx.x & 7, jj = threadIdx.x >> 3;
+        const int d = 32 * rg + 16 * h + jj;
+        const float4 ev4 = *reinterpret_cast<const float4*>(comb + (2 * jj) * 32 + 4 * rg);      // rows 0, 2, 4, 6
+        const float4 od4 = *reinterpret_cast<const float4*>(comb + (2 * jj + 1) * 32 + 4 * rg);  // rows 1, 3, 5, 7
+        const float val[8] = {ev4.x, od4.x, ev4.y, od4.y, ev4.z, od4.z, ev4.w, od4.w};
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          if (r >= p.G) break;
+          if (whole) out[(size_t)r * kHeadDim + d] = __float2bfloat16_rn(val[r] / misc[kMiscSeg + 8 + r]);
+          else part[(size_t)r * kDecPartStride + 4 + d] = val[r];
+        }
+        if (!whole && h == 0 && threadIdx.x < p.G) {
+          part[(size_t)threadIdx.x * kDecPartStride] = misc[kMiscSeg + threadIdx.x];
+          part[(size_t)threadIdx.x * kDecPartStride + 1] = misc[kMiscSeg + 8 + threadIdx.x];
+        }
+      }
+      __syncthreads();
+    }
+
+    // 4. A partial: count its blocks in; the CTA that completes the pair
+    // merges every partial of it (ordered by the fences around the ticket).
+    if (!whole) {
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const unsigned int n = (unsigned int)(seg_end - x);
+        const unsigned int before = atomicAdd(&p.tickets[pair], n);
+        const bool last = before + n == (unsigned int)ds.n_vis;
+        if (last) p.tickets[pair] = 0;  // every other CTA of the pair has counted in: reset for the next launch
+        reinterpret_cast<int*>(misc)[kMiscFlag] = last ? 1 : 0;
+      }
+      __syncthreads();
+      if (reinterpret_cast<const int*>(misc)[kMiscFlag]) {
+        // thread (row t / 16, dims 16 (t % 16) .. + 15): the pair's partials
+        // four at a time (all their loads in flight together), merged online
+        __threadfence();
+        const int r = threadIdx.x >> 4, dc = (threadIdx.x & 15) * 16;
+        if (r < p.G) {
+          const int n_sl = (pp.start + ds.n_vis - 1) / p.per_cta - pp.start / p.per_cta + 1;
+          const size_t sstride = (size_t)p.G * kDecPartStride;
+          const float* pr = p.part + (size_t)pair * p.max_slots * sstride + (size_t)r * kDecPartStride;
+          float mx = -INFINITY, l = 0.f;
+          float acc[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+          for (int k0 = 0; k0 < n_sl; k0 += 4) {
+            float mk[4], lk[4];
+            float4 ok[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const bool have = k0 + u < n_sl;
+              const float* ps = pr + (size_t)(have ? k0 + u : k0) * sstride;
+              mk[u] = have ? __ldcg(ps) : -INFINITY;
+              lk[u] = __ldcg(ps + 1);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) ok[u][e] = __ldcg(reinterpret_cast<const float4*>(ps + 4 + dc) + e);
+            }
+            float mn = mx;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) mn = fmaxf(mn, mk[u]);
+            const float al = mx == -INFINITY ? 0.f : ex2f(mx - mn);
+            l *= al;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) acc[e] *= al;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float w = mk[u] == -INFINITY ? 0.f : ex2f(mk[u] - mn);
+              l += w * lk[u];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                acc[4 * e] += w * ok[u][e].x;
+                acc[4 * e + 1] += w * ok[u][e].y;
+                acc[4 * e + 2] += w * ok[u][e].z;
+                acc[4 * e + 3] += w * ok[u][e].w;
+              }
+            }
+            mx = mn;
+          }
+          const float il = l > 0.f ? 1.f / l : 0.f;
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * e] * il, acc[2 * e + 1] * il);
+            pk[e] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(out + (size_t)r * kHeadDim + dc);
+          dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+    }
+    x = seg_end;
+    if (x < x1) dec_next_pair(p, tab, pp);
+    __syncthreads();  // the combine area is free before the next segment's Q fragments
+  }
+  // every copy this warp issued lands before the CTA exits (after a wait gave
+  // up some were never waited for; bounded)
+  if (lane == 0)
+    for (int i = waited; i < issued; ++i)
+      (void)mbar_wait_drain(bar0 + 8 * (i % kDecStages), (uint32_t)(i / kDecStages) & 1u, kDecDrainNs);
+  __syncwarp();
 }
 
 }  // namespace
 
-int decode_ctas_per_sm() {
-  static int n = 0;
+int decode_ctas_per_sm(int HKV) {
+  static int cached[9] = {0};
+  if (HKV < 1 || HKV > 8) return 1;
+  int& n = cached[HKV];
   if (n <= 0) {
-    if (cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel, kDecWarps * 32, kDecSmem) != cudaSuccess)
+    if (cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dec_smem(8)) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel, kDecWarps * 32, dec_smem(HKV)) !=
+            cudaSuccess)
       n = 0;
     if (n <= 0) {
       (void)cudaGetLastError();
@@ -368,12 +629,11 @@ int decode_ctas_per_sm() {
   return n;
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int n_seq, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
+cudaError_t launch_decode(const DecodeParams& p, const DecodeSeqs& seqs, const DecodeMaps& m, int n_cta,
+                          cudaStream_t st) {
+  const cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dec_smem(8));
   if (e != cudaSuccess) return e;
-  decode_split_kernel<<<n_seq * p.HKV * p.max_splits, kDecWarps * 32, kDecSmem, st>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  decode_combine_kernel<<<n_seq * p.HQ, kHeadDim, 0, st>>>(p);
+  decode_kernel<<<n_cta, kDecWarps * 32, dec_smem(p.HKV), st>>>(p, seqs, m.k, m.v);
   return cudaGetLastError();
 }
 

@@ -89,18 +89,18 @@ struct KvAppendParams {
 };
 cudaError_t launch_kv_append(const KvAppendParams& p, cudaStream_t st);
 
-// Decode: one query token per sequence, split over its visible blocks.
-constexpr int kDecMaxSplitBlocks = 128;  // 16-token blocks per split (one CTA) at most: 32 per warp
-constexpr int kDecPartStride = 260;  // floats per partial: row max (log2), row sum, 2 pad, O[256]
-struct DecSeq {
-  int q_row;     // row of the query token in q / out
-  int t;         // its position in the context (n_ctx - 1)
-  int bt_row;    // block-table row
-  int n_sink;    // sink blocks listed ahead of the window run
-  int lo;        // first block of the window run (0 with the window off)
-  int n_vis;     // visible blocks
-  int n_splits;  // ceil(n_vis / per_split)
-  int per_split; // blocks per split (the last split may have fewer)
+// Decode: one query token per sequence.  The launch's (sequence, kv head)
+// pairs laid end to end give a list of visible 16-token blocks; each CTA takes
+// an equal run of it (per_cta blocks, so every CTA of a one-wave grid does the
+// same work), which may cover the end of one pair and the start of the next.
+constexpr int kDecMaxCtaBlocks = 128;  // blocks per CTA at most: 32 per warp
+constexpr int kDecPartStride = 260;    // floats per partial row: max (log2), sum, 2 pad, O[256]
+constexpr int kDecParamSeqs = 512;     // sequences per launch, their table carried in the launch's parameters
+// One launch's sequences, passed by value (no upload per call):
+// {row of the token in q / out, context length, visible blocks of the launch's
+// earlier sequences (per kv head), 0}; the token is the context's last.
+struct DecodeSeqs {
+  int4 seq[kDecParamSeqs];
 };
 struct DecodeParams {
   const __nv_bfloat16* q;  // [rows][HQ][256]
@@ -111,16 +111,29 @@ struct DecodeParams {
   const float* v_scale;
   const int32_t* block_table;
   int bt_stride, n_pool;
-  const DecSeq* seqs;
+  int n_seq;               // sequences of this launch (<= kDecParamSeqs)
+  int bt_row0;             // block-table row of the launch's first sequence
+  int S, W;                // sink blocks, window blocks (W <= 0: no window)
   int HQ, HKV, G;
+  int total;               // visible blocks of all pairs of the launch
+  int per_cta;             // blocks per CTA (<= kDecMaxCtaBlocks)
+  int max_slots;           // partial slots per pair
   float sm_scale_log2;
-  float* part;  // [n_seq][HQ][max_splits][kDecPartStride]
-  int max_splits;
+  float* part;             // [n_seq * HKV][max_slots][G][kDecPartStride]
+  unsigned int* tickets;   // [n_seq * HKV] blocks merged so far; 0 between launches (the merging CTA resets it)
   int* err;
+  unsigned long long wait_ns;  // bound on every wait for a copy
 };
-cudaError_t launch_decode(const DecodeParams& p, int n_seq, cudaStream_t st);
-// Split-kernel CTAs that fit on one SM at a time (occupancy, cached).
-int decode_ctas_per_sm();
+// The pool as the decode kernel's TMA copies see it: uint8 [n_pool * 16][HKV][256],
+// box {128, 1, 16} (one kv head's 16 tokens of a page, half the dims), 128-byte swizzle.
+struct DecodeMaps {
+  CUtensorMap k;
+  CUtensorMap v;
+};
+cudaError_t launch_decode(const DecodeParams& p, const DecodeSeqs& seqs, const DecodeMaps& m, int n_cta,
+                          cudaStream_t st);
+// Decode CTAs that fit on one SM at a time for HKV kv heads (occupancy, cached).
+int decode_ctas_per_sm(int HKV);
 // overlap_prev: the launch may start while the previous attention launch on
 // `st` is still running (it must read nothing that launch writes).
 cudaError_t launch_attention(const AttnParams& p, const AttnMaps& m, int n_sm, cudaStream_t st,
