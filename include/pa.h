@@ -205,9 +205,8 @@ int pa_kv_append(pa_handle h, const void* k_new, const void* v_new, int n_new, i
  * containers (the bf16 query scaled per row by a power of two, codes as exact
  * fp16, P' = p * v_scale in fp16, fp32 accumulation).  One launch per 512
  * sequences, the sequence table carried in its parameters (no host-to-device
- * copy, no host wait).  Needs n_q_heads / n_kv_heads <= 8, k_scale and
- * v_scale 16-byte aligned, and fewer than 2^30 visible blocks x kv heads per
- * 512 sequences (PA_EINVAL otherwise).  Calls on one handle share its work
+ * copy, no host wait).  Needs n_q_heads / n_kv_heads <= 8 and fewer than
+ * 2^30 visible blocks x kv heads per 512 sequences (PA_EINVAL otherwise).  Calls on one handle share its work
  * buffers: issue them on one stream (calls that overlap on the GPU race).
  * Asynchronous; device errors (PA_EBADPAGE for a page entry outside the pool,
  * whose block is skipped) through pa_last_error. */

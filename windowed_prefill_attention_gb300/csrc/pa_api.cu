@@ -189,7 +189,7 @@ struct pa_ctx {
   const void* dec_vp = nullptr;
   float* d_part = nullptr;
   int part_cap = 0;
-  unsigned int* d_tickets = nullptr;
+  unsigned long long* d_tickets = nullptr;
   int tickets_cap = 0;
 
   // host-buffer path staging
@@ -250,6 +250,12 @@ int grow_bytes(void*& p, size_t& cap, size_t need) {
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// A decode launch's CTA runs: first block, its sequence, the CTA's partial slot in its pair.
+struct DecRuns {
+  std::vector<int> x0, seq, slot;
+  int max_slots = 1;
+};
 
 int encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
            const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle sw) {
@@ -971,13 +977,58 @@ int pa_kv_append(pa_handle h, const void* k_new, const void* v_new, int n_new, i
   return PA_OK;
 }
 
+namespace {
+// Cost-balanced decode runs over a launch's pair list (block counts `len`,
+// HKV pairs per sequence).  A CTA costs its blocks plus kDecSegCost for every
+// pair after its first: a run that crosses into another pair waits for all
+// its warps, combines them, loads the next pair's query rows and refills its
+// copies (measured at 64 sequences x 32k context: such CTAs ended ~10 us,
+// about 16 blocks' worth, after the others).  Greedy packing under `budget`;
+// false if it needs more than max_ctas CTAs.
+constexpr int kDecSegCost = 16;
+bool decode_pack(const std::vector<int>& len, int HKV, long long total, long long budget, long long max_ctas,
+                 DecRuns& r) {
+  r.x0.clear();
+  r.seq.clear();
+  r.slot.clear();
+  r.max_slots = 1;
+  std::vector<int> first_cta(len.size(), 0);
+  size_t pi = 0;
+  long long pstart = 0, x = 0;
+  int cta = 0;
+  while (x < total) {
+    if (cta >= max_ctas) return false;
+    r.x0.push_back((int)x);
+    r.seq.push_back((int)(pi / (size_t)HKV));
+    r.slot.push_back(x == pstart ? 0 : cta - first_cta[pi]);
+    long long cost = 0;
+    bool first = true;
+    while (x < total) {
+      const long long pend = pstart + len[pi];
+      const long long extra = first ? 0 : kDecSegCost;
+      if (cost + extra >= budget) break;
+      if (x == pstart) first_cta[pi] = cta;
+      const long long take = std::min(pend - x, budget - cost - extra);
+      cost += extra + take;
+      x += take;
+      first = false;
+      if (x < pend) break;  // the budget ran out inside the pair
+      r.max_slots = std::max(r.max_slots, cta - first_cta[pi] + 1);
+      ++pi;
+      pstart = pend;
+    }
+    ++cta;
+  }
+  return true;
+}
+}  // namespace
+
 int pa_decode(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* k_pool, const int8_t* v_pool,
               const float* k_scale, const float* v_scale, const int32_t* block_table, int n_sink_blk, int n_win_blk,
               float sm_scale, void* out, void* stream) {
   int rc = check_inputs(h, q, k_pool, v_pool, k_scale, v_scale, block_table, out);
   if (rc) return rc;
   if (n_seq <= 0 || !seqs || h->G > 8 || !(sm_scale == sm_scale) || sm_scale < 0.f) return PA_EINVAL;
-  if (!aligned(k_scale, 16) || !aligned(v_scale, 16)) return PA_EINVAL;  // pages' scales are bulk-copied
   std::vector<int> n_vis((size_t)n_seq);
   for (int s = 0; s < n_seq; ++s) {
     const pa_seq& q1 = seqs[s];
@@ -990,14 +1041,17 @@ int pa_decode(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const i
     n_vis[(size_t)s] = n_sink + (last - lo + 1);
   }
   // Launches of up to kDecParamSeqs sequences, their table in the launch's
-  // parameters.  Work split: the launch's pairs' blocks end to end, per_cta
-  // blocks per CTA so that the grid is one wave of equal CTAs when 128-block
-  // CTAs would fit in one wave, else whole waves.
+  // parameters.  Work split: the launch's pairs' blocks end to end; one wave
+  // of cost-balanced runs listed in the parameters when runs of at most 128
+  // blocks fit in one wave, else whole waves of equal runs of per_cta blocks.
   struct Launch {
     int s0, n, total, per_cta, n_cta, max_slots;
+    bool listed;
+    DecRuns runs;
   };
   std::vector<Launch> launches;
   const long long slots = (long long)h->n_sm * decode_ctas_per_sm(h->HKV);
+  const long long wave = std::min<long long>(slots, kDecParamCtas);
   size_t part_need = 0;
   for (int s0 = 0; s0 < n_seq; s0 += kDecParamSeqs) {
     Launch L{};
@@ -1005,27 +1059,45 @@ int pa_decode(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const i
     L.n = std::min(kDecParamSeqs, n_seq - s0);
     long long vis = 0;
     int nv_max = 1;
+    std::vector<int> len;
     for (int i = 0; i < L.n; ++i) {
-      vis += n_vis[(size_t)(s0 + i)];
-      nv_max = std::max(nv_max, n_vis[(size_t)(s0 + i)]);
+      const int nv = n_vis[(size_t)(s0 + i)];
+      vis += nv;
+      nv_max = std::max(nv_max, nv);
+      for (int g = 0; g < h->HKV; ++g) len.push_back(nv);
     }
     const long long total = vis * h->HKV;
     if (total >= (1ll << 30)) return PA_EINVAL;
-    const long long full = (total + kDecMaxCtaBlocks - 1) / kDecMaxCtaBlocks;
-    const long long waves = std::max(1ll, (full + slots - 1) / slots);
     L.total = (int)total;
-    L.per_cta = (int)std::max(1ll, (total + waves * slots - 1) / (waves * slots));
-    L.n_cta = (int)((total + L.per_cta - 1) / L.per_cta);
-    L.max_slots = (nv_max - 1 + L.per_cta - 1) / L.per_cta + 1;  // CTA runs a pair's blocks can meet
+    if (total <= wave * kDecMaxCtaBlocks && decode_pack(len, h->HKV, total, kDecMaxCtaBlocks, wave, L.runs)) {
+      long long lo = std::max(1ll, (total + wave - 1) / wave), hi = kDecMaxCtaBlocks;
+      while (lo < hi) {  // the smallest budget that packs into one wave
+        const long long mid = (lo + hi) / 2;
+        if (decode_pack(len, h->HKV, total, mid, wave, L.runs)) hi = mid;
+        else lo = mid + 1;
+      }
+      (void)decode_pack(len, h->HKV, total, lo, wave, L.runs);
+      L.listed = true;
+      L.per_cta = (int)lo;
+      L.n_cta = (int)L.runs.x0.size();
+      L.max_slots = L.runs.max_slots;
+    } else {
+      const long long full = (total + kDecMaxCtaBlocks - 1) / kDecMaxCtaBlocks;
+      const long long waves = std::max(1ll, (full + slots - 1) / slots);
+      L.listed = false;
+      L.per_cta = (int)std::max(1ll, (total + waves * slots - 1) / (waves * slots));
+      L.n_cta = (int)((total + L.per_cta - 1) / L.per_cta);
+      L.max_slots = (nv_max - 1 + L.per_cta - 1) / L.per_cta + 1;  // CTA runs a pair's blocks can meet
+    }
     part_need = std::max(part_need, (size_t)L.n * h->HKV * L.max_slots * h->G * kDecPartStride);
-    launches.push_back(L);
+    launches.push_back(std::move(L));
   }
   if (part_need > (size_t)INT32_MAX) return PA_EINVAL;
   if ((rc = grow(h->d_part, h->part_cap, part_need))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (h->tickets_cap < kDecParamSeqs * h->HKV) {
     if ((rc = grow(h->d_tickets, h->tickets_cap, (size_t)kDecParamSeqs * h->HKV))) return rc;
-    PA_CUDA(cudaMemsetAsync(h->d_tickets, 0, (size_t)h->tickets_cap * sizeof(unsigned int), st));
+    PA_CUDA(cudaMemsetAsync(h->d_tickets, 0, (size_t)h->tickets_cap * sizeof(unsigned long long), st));
   }
   if (k_pool != h->dec_kp || v_pool != h->dec_vp) {
     // the pool as uint8 [n_pool * 16][HKV][256]; a box is one kv head's 16 token rows of half the dims
@@ -1074,6 +1146,13 @@ int pa_decode(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const i
     p.total = L.total;
     p.per_cta = L.per_cta;
     p.max_slots = L.max_slots;
+    p.runs_listed = L.listed ? 1 : 0;
+    if (L.listed)
+      for (int c = 0; c < L.n_cta; ++c) {
+        tab.cta_x0[c] = L.runs.x0[(size_t)c];
+        tab.cta_seq[c] = (uint16_t)L.runs.seq[(size_t)c];
+        tab.cta_slot[c] = (uint16_t)L.runs.slot[(size_t)c];
+      }
     PA_CUDA(launch_decode(p, tab, h->dec_maps, L.n_cta, st));
   }
   return PA_OK;

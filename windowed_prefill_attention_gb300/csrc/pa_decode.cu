@@ -22,9 +22,12 @@
 //
 // Data movement: each warp owns a ring of kDecStages block slots in shared
 // memory; one lane fills them with TMA copies (a kv head's 16 token rows of a
-// K page and of a V page, each as two 128-byte-swizzled halves, plus the
-// page's scales by a bulk copy), completing on the slot's mbarrier, so a
-// warp has kDecStages blocks (kDecStages x 8 KB) in flight while it computes.
+// K page and of a V page, each as two 128-byte-swizzled halves), completing
+// on the slot's mbarrier, so a warp has kDecStages blocks (kDecStages x 8 KB)
+// in flight while it computes.  The page's 16 K and 16 V scales of the head
+// come with them by 4-byte asynchronous copies, one per lane, into a 128-byte
+// scale slot, tracked by the same mbarrier (cheaper than two more small bulk
+// copies per block).
 // Operand layout: the head dims of a block are permuted (the sum over dims in
 // S^T is the same in any order; Q takes the same permutation, O^T is put back
 // in order when written), so that every thread reads its K and V operands as
@@ -52,20 +55,26 @@ namespace pa {
 namespace {
 
 constexpr int kDecWarps = 4;
-constexpr int kDecStages = 2;                        // block slots (copies in flight) per warp
+constexpr int kDecStages = 3;                        // block slots (copies in flight) per warp
 constexpr int kHalfBytes = kPage * 128;              // 16 rows x 128 dims (one TMA box)
 constexpr int kBlockBytes = 4 * kHalfBytes;          // K halves 0, 1, then V halves 0, 1
 constexpr int kSlotsBytes = kDecWarps * kDecStages * kBlockBytes;
-// Shared memory from a 1024-byte aligned base: the block slots, then per slot
-// the page's scales (K: 16 tokens x HKV floats, then V likewise), the Q
+// Shared memory from a 1024-byte aligned base: the block slots, the Q
 // fragments [16 k-steps][32 lanes] x 8 B (between segments: the combine
-// area, 128 dims x 8 rows of fp32), small per-row values, the slots' barriers.
-__host__ __device__ constexpr int dec_scale_bytes(int HKV) { return 2 * kPage * HKV * 4; }
-__host__ __device__ constexpr int dec_sm_scales() { return kSlotsBytes; }
-__host__ __device__ constexpr int dec_sm_qf(int HKV) { return kSlotsBytes + kDecWarps * kDecStages * dec_scale_bytes(HKV); }
-__host__ __device__ constexpr int dec_sm_misc(int HKV) { return dec_sm_qf(HKV) + 16 * 32 * 8; }
-__host__ __device__ constexpr int dec_sm_bars(int HKV) { return dec_sm_misc(HKV) + 512; }
-__host__ __device__ constexpr int dec_smem(int HKV) { return dec_sm_bars(HKV) + kDecWarps * kDecStages * 8 + 1024; }
+// area, 128 dims x 8 rows of fp32), small per-row values, the slots' barriers
+// and the query rows' barrier, the slots' scales (lane l < 16: K scale of key
+// l; 16 + l: V scale), and the raw bf16 query rows of the next segment
+// (copied while the current one runs).
+constexpr int kSmQf = kSlotsBytes;
+constexpr int kSmMisc = kSmQf + 16 * 32 * 8;
+constexpr int kSmBars = kSmMisc + 512;
+constexpr int kSmQBar = kSmBars + kDecWarps * kDecStages * 8;
+constexpr int kSmScales = kSmQBar + 16;
+constexpr int kSmQRaw = kSmScales + kDecWarps * kDecStages * 128;
+constexpr int kDecSmem = kSmQRaw + 8 * kHeadDim * 2 + 1024;
+// Arrivals per slot phase: the copying lane's (with the byte count), then
+// each lane's once its scale copy has landed.
+constexpr int kSlotArrivals = 1 + 32;
 // misc floats: row factors of Q [0, 8), per-warp row max / row sum [8, 72),
 // the segment's row max / row sum [72, 88), the "last segment" flag at 88
 constexpr int kMiscRowc = 0, kMiscWarp = 8, kMiscSeg = 72, kMiscFlag = 88;
@@ -149,6 +158,7 @@ struct PairPos {
 // block is at or before x (binary search over the table), then the kv head.
 __device__ __forceinline__ PairPos dec_locate(const DecodeParams& p, const DecodeSeqs& tab, int x) {
   int lo = 0, hi = p.n_seq - 1;
+  if (p.runs_listed) lo = hi = tab.cta_seq[blockIdx.x];  // x is this CTA's first block: the host found its sequence
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (p.HKV * tab.seq[mid].z <= x) lo = mid;
@@ -170,18 +180,17 @@ __device__ __forceinline__ void dec_next_pair(const DecodeParams& p, const Decod
   }
 }
 
-// The kv head's G query rows -> fp16 B fragments of Q^T, each row scaled by
+// The kv head's G query rows (raw bf16 in shared memory) -> fp16 B fragments of Q^T, each row scaled by
 // the power of two that puts its absmax in [64, 128).  Thread: row r, dims
 // [16 c, 16 c + 16).  Rows >= G are zero.  Dims are permuted as the K operand
 // is: k-step 4 j + m, lane (row, t) holds dims 64 j + 16 t + 4 m + {0, 1} and
 // + {2, 3}.  Row factors (2^-k * sm_scale * log2 e) go to c_rows.
-__device__ __forceinline__ void dec_load_q(const DecodeParams& p, int q_row, int g, uint2* qf, float* c_rows) {
+__device__ __forceinline__ void dec_load_q(const DecodeParams& p, const uint8_t* raw, uint2* qf, float* c_rows) {
   const int r = threadIdx.x >> 4, c = threadIdx.x & 15;
   float v[16];
   float am = 0.f;
   if (r < p.G) {
-    const uint4* src =
-        reinterpret_cast<const uint4*>(p.q + ((size_t)q_row * p.HQ + (size_t)g * p.G + r) * kHeadDim + c * 16);
+    const uint4* src = reinterpret_cast<const uint4*>(raw + r * kHeadDim * 2 + c * 32);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const uint4 w = src[h];
@@ -219,19 +228,28 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(const __grid_con
   const int HKV = p.HKV;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
-  uint2* qf = reinterpret_cast<uint2*>(dsm + dec_sm_qf(HKV));
-  float* comb = reinterpret_cast<float*>(dsm + dec_sm_qf(HKV));  // between segments
-  float* misc = reinterpret_cast<float*>(dsm + dec_sm_misc(HKV));
-  const uint32_t bars = sbase + dec_sm_bars(HKV);
+  uint2* qf = reinterpret_cast<uint2*>(dsm + kSmQf);
+  float* comb = reinterpret_cast<float*>(dsm + kSmQf);  // between segments
+  float* misc = reinterpret_cast<float*>(dsm + kSmMisc);
+  const uint32_t bars = sbase + kSmBars;
   const WaitCtl wc{p.err, p.wait_ns};
+  const uint32_t qbar = sbase + kSmQBar;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kDecWarps * kDecStages; ++i) mbar_init(bars + 8 * i, 1);
+    mbar_init(qbar, 1);
+    for (int i = 0; i < kDecWarps * kDecStages; ++i) mbar_init(bars + 8 * i, kSlotArrivals);
     fence_mbar_init();
     tma_prefetch_map(&km);
     tma_prefetch_map(&vm);
   }
   // this CTA's run of the launch's block list
-  const int x0 = (int)blockIdx.x * p.per_cta, x1 = min(p.total, x0 + p.per_cta);
+  int x0, x1;
+  if (p.runs_listed) {
+    x0 = tab.cta_x0[blockIdx.x];
+    x1 = blockIdx.x + 1 < gridDim.x ? tab.cta_x0[blockIdx.x + 1] : p.total;
+  } else {
+    x0 = (int)blockIdx.x * p.per_cta;
+    x1 = min(p.total, x0 + p.per_cta);
+  }
   PairPos pp = dec_locate(p, tab, x0);
 
   // 1. This warp's blocks: x0 + warp + 4 i, i < n_mine (<= 32).  Lane i looks
@@ -248,37 +266,53 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(const __grid_con
     my_page = p.block_table[(size_t)(p.bt_row0 + q.s) * p.bt_stride + dec_block(q.d, x - q.start)];
   }
   const uint32_t slot0 = sbase + (uint32_t)(warp * kDecStages * kBlockBytes);
-  const uint32_t scl0 = sbase + (uint32_t)(dec_sm_scales() + warp * kDecStages * dec_scale_bytes(HKV));
   const uint32_t bar0 = bars + (uint32_t)(warp * kDecStages * 8);
-  const uint32_t tx_bytes = (uint32_t)(kBlockBytes + dec_scale_bytes(HKV));
+  const uint32_t tx_bytes = (uint32_t)kBlockBytes;
   __syncthreads();  // the slots' barriers exist before any copy completes on them
 
+  const uint32_t scl0 = sbase + (uint32_t)(kSmScales + warp * kDecStages * 128);
   // copy block i (a warp-wide call: page and kv head come from lane i); a
   // page entry outside the pool copies nothing and completes the slot's phase
+  // at once.  Lane l < 16 copies the K scale of key l, lane 16 + l the V scale.
   auto issue = [&](int i) {
     const int phys = __shfl_sync(0xffffffffu, my_page, i);
     const int gi = __shfl_sync(0xffffffffu, my_g, i);
-    if (lane != 0) return;
     const int st = i % kDecStages;
     const uint32_t bar = bar0 + 8 * st;
-    if (phys < 0 || phys >= p.n_pool) {
+    if (phys < 0 || phys >= p.n_pool) {  // every lane arrives without a scale, lane 0 also for the copies
       mbar_arrive(bar);
+      if (lane == 0) mbar_arrive(bar);
       return;
     }
-    const uint32_t dst = slot0 + (uint32_t)(st * kBlockBytes);
-    mbar_expect_tx(bar, tx_bytes);
-    tma_load_3d(dst, &km, bar, 0, gi, phys * kPage);
-    tma_load_3d(dst + kHalfBytes, &km, bar, 128, gi, phys * kPage);
-    tma_load_3d(dst + 2 * kHalfBytes, &vm, bar, 0, gi, phys * kPage);
-    tma_load_3d(dst + 3 * kHalfBytes, &vm, bar, 128, gi, phys * kPage);
-    const size_t so = (size_t)phys * kPage * HKV;
-    const uint32_t sd = scl0 + (uint32_t)(st * dec_scale_bytes(HKV));
-    bulk_load(sd, p.k_scale + so, (uint32_t)(kPage * HKV * 4), bar);
-    bulk_load(sd + kPage * HKV * 4, p.v_scale + so, (uint32_t)(kPage * HKV * 4), bar);
+    if (lane == 0) {
+      const uint32_t dst = slot0 + (uint32_t)(st * kBlockBytes);
+      mbar_expect_tx(bar, tx_bytes);
+      tma_load_3d(dst, &km, bar, 0, gi, phys * kPage);
+      tma_load_3d(dst + kHalfBytes, &km, bar, 128, gi, phys * kPage);
+      tma_load_3d(dst + 2 * kHalfBytes, &vm, bar, 0, gi, phys * kPage);
+      tma_load_3d(dst + 3 * kHalfBytes, &vm, bar, 128, gi, phys * kPage);
+    }
+    const float* src = (lane < 16 ? p.k_scale : p.v_scale) + ((size_t)phys * kPage + (lane & 15)) * HKV + gi;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(scl0 + (uint32_t)(st * 128 + lane * 4)), "l"(src)
+                 : "memory");
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
   };
   // the first copies go out before the query setup, which they overlap
   int issued = min(kDecStages, n_mine);
   for (int i = 0; i < issued; ++i) issue(i);
+  // a pair's G query rows (contiguous) into the raw area (thread 0)
+  auto issue_q = [&](const PairPos& q) {
+    const uint32_t bytes = (uint32_t)(p.G * kHeadDim * 2);
+    mbar_expect_tx(qbar, bytes);
+    bulk_load(sbase + kSmQRaw, p.q + ((size_t)q.d.q_row * p.HQ + (size_t)q.g * p.G) * kHeadDim, bytes, qbar);
+  };
+  bool q_pending = false;  // thread 0: a query copy not yet waited for
+  bool q_broken = false;   // thread 0: a wait for one gave up
+  if (threadIdx.x == 0) {
+    issue_q(pp);
+    q_pending = true;
+  }
+  uint32_t q_phase = 0;
 
   int it = 0;         // this warp's next block
   int waited = 0;     // blocks whose slot phase this warp has waited for
@@ -287,8 +321,22 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(const __grid_con
     const int seg_end = min(x1, pp.start + pp.d.n_vis);
     const DecSeq ds = pp.d;
     const int g = pp.g;
-    dec_load_q(p, ds.q_row, g, qf, misc + kMiscRowc);
-    __syncthreads();
+    // this segment's query rows (copied during the previous segment)
+    const bool q_ok = mbar_wait(qbar, q_phase & 1u, wc, 61);
+    ++q_phase;
+    if (threadIdx.x == 0) {
+      if (q_ok) q_pending = false;
+      else q_broken = true;  // a copy may still be on its way: issue no other (one in flight at most)
+    }
+    if (!__all_sync(0xffffffffu, q_ok)) ok = false;
+    dec_load_q(p, dsm + kSmQRaw, qf, misc + kMiscRowc);
+    __syncthreads();  // the raw rows are read: the next segment's may come in
+    if (threadIdx.x == 0 && seg_end < x1 && !q_broken) {
+      PairPos nx = pp;
+      dec_next_pair(p, tab, nx);
+      issue_q(nx);
+      q_pending = true;
+    }
     const float c_lo = misc[kMiscRowc + 2 * tq], c_hi = misc[kMiscRowc + 2 * tq + 1];
 
     float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
@@ -314,8 +362,6 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(const __grid_con
         if (lane == 0) atomicCAS(p.err, 0, DEV_ERR_BAD_PAGE);
       } else {
         const uint32_t kb = slot0 + (uint32_t)(st * kBlockBytes), vb = kb + 2 * kHalfBytes;
-        const float* kscl = reinterpret_cast<const float*>(dsm + (scl0 - sbase) + st * dec_scale_bytes(HKV)) + g;
-        const float* vscl = kscl + kPage * HKV;
         // S^T = K Q^T: keys gq, gq+8 x rows 2tq, 2tq+1.  Dims group j (64 dims,
         // 4 k-steps): this thread's 16 bytes of rows gq and gq+8, dims
         // 64 j + 16 tq + [0, 16); k-step 4 j + m takes word m (dims + 4m .. + 3).
@@ -346,12 +392,13 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(const __grid_con
         // scores in log2 units; keys past the query position masked
         const int lb = dec_block(ds, b);
         const bool v0 = lb * kPage + gq <= ds.t, v1 = lb * kPage + gq + 8 <= ds.t;
-        const float ks0 = kscl[gq * HKV], ks1 = kscl[(gq + 8) * HKV];
+        const float* scl = reinterpret_cast<const float*>(dsm + kSmScales) + (warp * kDecStages + st) * 32;
+        const float ks0 = scl[gq], ks1 = scl[gq + 8], vsc0 = scl[16 + gq], vsc1 = scl[24 + gq];
         const float y0 = v0 ? sc[0] * ks0 * c_lo : -INFINITY, y1 = v0 ? sc[1] * ks0 * c_hi : -INFINITY;
         const float y2 = v1 ? sc[2] * ks1 * c_lo : -INFINITY, y3 = v1 ? sc[3] * ks1 * c_hi : -INFINITY;
         float bm_lo = fmaxf(y0, y2), bm_hi = fmaxf(y1, y3);
         // the block's largest V scale (lanes 16..31: the V scales of keys 0..15)
-        float bv = (lane >= 16 && lb * kPage + (lane - 16) <= ds.t) ? vscl[(lane - 16) * HKV] : 0.f;
+        float bv = (lane >= 16 && lb * kPage + (lane - 16) <= ds.t) ? scl[lane] : 0.f;
 #pragma unroll
         for (int sh = 4; sh < 32; sh <<= 1) {
           bm_lo = fmaxf(bm_lo, __shfl_xor_sync(0xffffffffu, bm_lo, sh));
@@ -385,7 +432,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(const __grid_con
         }
         // P' = p * v_scale * 2^-ev (masked keys: 0, whatever their scale slot
         // holds), as the B fragments of P^T
-        const float vs0 = v0 ? vscl[gq * HKV] * vnorm : 0.f, vs1 = v1 ? vscl[(gq + 8) * HKV] * vnorm : 0.f;
+        const float vs0 = v0 ? vsc0 * vnorm : 0.f, vs1 = v1 ? vsc1 * vnorm : 0.f;
         const uint32_t pb0 = transpose8x8(pack_f16x2(v0 ? p0 * vs0 : 0.f, v0 ? p1 * vs0 : 0.f));
         const uint32_t pb1 = transpose8x8(pack_f16x2(v1 ? p2 * vs1 : 0.f, v1 ? p3 * vs1 : 0.f));
         // O^T += V^T P^T.  Dims are permuted: row gq of m-tile mt is dim
@@ -472,7 +519,8 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(const __grid_con
     }
     const int pair = pp.s * HKV + g;
     const bool whole = x == pp.start && seg_end == pp.start + ds.n_vis;
-    const int slot = (int)blockIdx.x - pp.start / p.per_cta;
+    // a later segment of the run starts its pair: the pair's first CTA
+    const int slot = x != x0 ? 0 : (p.runs_listed ? (int)tab.cta_slot[blockIdx.x] : (int)blockIdx.x - pp.start / p.per_cta);
     float* part = p.part + ((size_t)pair * p.max_slots + slot) * p.G * kDecPartStride;
     __nv_bfloat16* out = p.out + ((size_t)ds.q_row * p.HQ + (size_t)g * p.G) * kHeadDim;
     // Two rounds of 128 dims through the combine area, word (2 jj + e) * 32 +
@@ -526,25 +574,29 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(const __grid_con
     }
 
     // 4. A partial: count its blocks in; the CTA that completes the pair
-    // merges every partial of it (ordered by the fences around the ticket).
+    // merges every partial of it.  Ordering: the CTA's partial writes come
+    // before the barrier the loop above ended with, thread 0's fence makes
+    // them visible at device scope before its ticket add (release), and its
+    // fence after the add orders the merge's reads after it (acquire).
     if (!whole) {
-      __threadfence();
-      __syncthreads();
       if (threadIdx.x == 0) {
-        const unsigned int n = (unsigned int)(seg_end - x);
-        const unsigned int before = atomicAdd(&p.tickets[pair], n);
-        const bool last = before + n == (unsigned int)ds.n_vis;
+        __threadfence();
+        // blocks, and (from the pair's last CTA) the partial count
+        const unsigned long long add = (unsigned long long)(seg_end - x) +
+            (seg_end == pp.start + ds.n_vis ? (unsigned long long)(slot + 1) << 32 : 0ull);
+        const unsigned long long now = atomicAdd(&p.tickets[pair], add) + add;
+        const bool last = (uint32_t)now == (uint32_t)ds.n_vis;
         if (last) p.tickets[pair] = 0;  // every other CTA of the pair has counted in: reset for the next launch
-        reinterpret_cast<int*>(misc)[kMiscFlag] = last ? 1 : 0;
+        __threadfence();
+        reinterpret_cast<int*>(misc)[kMiscFlag] = last ? (int)(now >> 32) : 0;
       }
       __syncthreads();
-      if (reinterpret_cast<const int*>(misc)[kMiscFlag]) {
+      const int n_sl = reinterpret_cast<const int*>(misc)[kMiscFlag];
+      if (n_sl > 0) {
         // thread (row t / 16, dims 16 (t % 16) .. + 15): the pair's partials
         // four at a time (all their loads in flight together), merged online
-        __threadfence();
         const int r = threadIdx.x >> 4, dc = (threadIdx.x & 15) * 16;
         if (r < p.G) {
-          const int n_sl = (pp.start + ds.n_vis - 1) / p.per_cta - pp.start / p.per_cta + 1;
           const size_t sstride = (size_t)p.G * kDecPartStride;
           const float* pr = p.part + (size_t)pair * p.max_slots * sstride + (size_t)r * kDecPartStride;
           float mx = -INFINITY, l = 0.f;
@@ -603,6 +655,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(const __grid_con
   }
   // every copy this warp issued lands before the CTA exits (after a wait gave
   // up some were never waited for; bounded)
+  if (threadIdx.x == 0 && q_pending) (void)mbar_wait_drain(qbar, (q_phase - 1u) & 1u, kDecDrainNs);
   if (lane == 0)
     for (int i = waited; i < issued; ++i)
       (void)mbar_wait_drain(bar0 + 8 * (i % kDecStages), (uint32_t)(i / kDecStages) & 1u, kDecDrainNs);
@@ -616,10 +669,8 @@ int decode_ctas_per_sm(int HKV) {
   if (HKV < 1 || HKV > 8) return 1;
   int& n = cached[HKV];
   if (n <= 0) {
-    if (cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dec_smem(8)) !=
-            cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel, kDecWarps * 32, dec_smem(HKV)) !=
-            cudaSuccess)
+    if (cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel, kDecWarps * 32, kDecSmem) != cudaSuccess)
       n = 0;
     if (n <= 0) {
       (void)cudaGetLastError();
@@ -631,9 +682,9 @@ int decode_ctas_per_sm(int HKV) {
 
 cudaError_t launch_decode(const DecodeParams& p, const DecodeSeqs& seqs, const DecodeMaps& m, int n_cta,
                           cudaStream_t st) {
-  const cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dec_smem(8));
+  const cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
   if (e != cudaSuccess) return e;
-  decode_kernel<<<n_cta, kDecWarps * 32, dec_smem(p.HKV), st>>>(p, seqs, m.k, m.v);
+  decode_kernel<<<n_cta, kDecWarps * 32, kDecSmem, st>>>(p, seqs, m.k, m.v);
   return cudaGetLastError();
 }
 

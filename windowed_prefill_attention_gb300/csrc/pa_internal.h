@@ -91,16 +91,21 @@ cudaError_t launch_kv_append(const KvAppendParams& p, cudaStream_t st);
 
 // Decode: one query token per sequence.  The launch's (sequence, kv head)
 // pairs laid end to end give a list of visible 16-token blocks; each CTA takes
-// an equal run of it (per_cta blocks, so every CTA of a one-wave grid does the
-// same work), which may cover the end of one pair and the start of the next.
+// a run of it, which may cover the end of one pair and the start of the next:
+// runs of equal cost listed in the launch's parameters (one-wave grids), else
+// equal runs of per_cta blocks.
 constexpr int kDecMaxCtaBlocks = 128;  // blocks per CTA at most: 32 per warp
 constexpr int kDecPartStride = 260;    // floats per partial row: max (log2), sum, 2 pad, O[256]
 constexpr int kDecParamSeqs = 512;     // sequences per launch, their table carried in the launch's parameters
 // One launch's sequences, passed by value (no upload per call):
 // {row of the token in q / out, context length, visible blocks of the launch's
 // earlier sequences (per kv head), 0}; the token is the context's last.
+constexpr int kDecParamCtas = 512;    // CTA runs the launch's parameters can carry
 struct DecodeSeqs {
   int4 seq[kDecParamSeqs];
+  int cta_x0[kDecParamCtas];          // first block of CTA c's run (the run ends where CTA c + 1's starts)
+  uint16_t cta_seq[kDecParamCtas];    // sequence of that block
+  uint16_t cta_slot[kDecParamCtas];   // CTA c's partial slot in that block's pair (CTAs before it in the pair)
 };
 struct DecodeParams {
   const __nv_bfloat16* q;  // [rows][HQ][256]
@@ -116,11 +121,15 @@ struct DecodeParams {
   int S, W;                // sink blocks, window blocks (W <= 0: no window)
   int HQ, HKV, G;
   int total;               // visible blocks of all pairs of the launch
-  int per_cta;             // blocks per CTA (<= kDecMaxCtaBlocks)
+  int per_cta;             // blocks per CTA (<= kDecMaxCtaBlocks) when runs_listed is 0
   int max_slots;           // partial slots per pair
+  int runs_listed;         // DecodeSeqs::cta_* hold every CTA's run
   float sm_scale_log2;
   float* part;             // [n_seq * HKV][max_slots][G][kDecPartStride]
-  unsigned int* tickets;   // [n_seq * HKV] blocks merged so far; 0 between launches (the merging CTA resets it)
+  // [n_seq * HKV] per pair: low 32 bits the blocks of the partials written so
+  // far, high 32 bits its partial count (added by the CTA that holds its last
+  // block); 0 between launches (the merging CTA resets it)
+  unsigned long long* tickets;
   int* err;
   unsigned long long wait_ns;  // bound on every wait for a copy
 };
