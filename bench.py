@@ -401,6 +401,18 @@ def run_ours(args, wl):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp)
     pa.pa_destroy(h)
+    if world == 1 and not args.no_extra_rows and args.config == "32k" and not args.gate:
+        # the next rows' steps on the same workload, briefly (the --op lines in full)
+        short = argparse.Namespace(steps=20, warmup=3, gpus=1)
+        extra = {}
+        for name, fn in (("kv_append", lambda: measure_kv_append(short, wl, inp)),
+                         ("decode", lambda: measure_decode(short, wl))):
+            r = fn()
+            extra[name] = {k: r[k] for k in ("metric", "value", "unit", "ms_per_step", "steps", "warmup", "config",
+                                             "clocks", "gpu_launches")}
+            extra[name]["roofline"] = {k: r["roofline"][k] for k in ("bound", "kernel", "achieved", "peak", "unit",
+                                                                    "frac", "traffic")}
+        line["extra_rows"] = extra
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -408,6 +420,10 @@ def run_ours(args, wl):
 
 
 def run_kv_append(args, wl):
+    print(json.dumps(measure_kv_append(args, wl)), flush=True)
+
+
+def measure_kv_append(args, wl, inp=None):
     """KV append (the step before the path): every query token's K and V rows of
     the workload quantised into the pool.  HBM-bound; algorithmic bytes per
     (token, kv head) = bf16 K and V read (2 x 512) + int8 codes written
@@ -416,7 +432,8 @@ def run_kv_append(args, wl):
 
     import windowed_prefill_attention_gb300 as pa
     torch.cuda.set_device(0)
-    inp = make_inputs(wl)
+    if inp is None:
+        inp = make_inputs(wl)
     dev = torch.device("cuda", 0)
     hkv = wl.n_kv_heads
     q_off, q_start, n_q, n_ctx = inp.seq_desc[0].tolist()
@@ -453,7 +470,7 @@ def run_kv_append(args, wl):
     nbytes = n_q * hkv * 1544
     gbs = nbytes / (ms / 1e3) / 1e9
     peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["hbm_gbs"])
-    print(json.dumps({
+    return {
         "metric": "kv append GB/s (algorithmic bytes)", "value": gbs, "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16->int8", "data": "synthetic",
@@ -462,10 +479,14 @@ def run_kv_append(args, wl):
         "gpu_launches": args.steps, "clocks": clocks,
         "roofline": {"bound": "hbm", "kernel": "kv_append_kernel", "achieved": gbs, "peak": peak, "unit": "GB/s",
                      "frac": gbs / peak, "peak_source": "measured copy bandwidth (MEASURED_PEAKS.json)",
-                     "traffic": profiled_traffic(wl.name, "kv_append_kernel"), "bytes_per_launch": nbytes}}), flush=True)
+                     "traffic": profiled_traffic(wl.name, "kv_append_kernel"), "bytes_per_launch": nbytes}}
 
 
 def run_decode(args, wl):
+    print(json.dumps(measure_decode(args, wl)), flush=True)
+
+
+def measure_decode(args, wl):
     """Split-KV decode: one new token for each of N_DECODE_SEQS sequences whose
     context is the workload's (the 32k workload: 64 x 32768 tokens, GQA 16:2,
     1 sink block + 256-block window).  HBM-bound; algorithmic bytes per step =
@@ -520,7 +541,7 @@ def run_decode(args, wl):
     nbytes = n_seq * hkv * keys * (2 * HEAD_DIM + 8) + 2 * n_seq * hq * HEAD_DIM * 2
     gbs = nbytes / (ms / 1e3) / 1e9
     peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["hbm_gbs"])
-    print(json.dumps({
+    return {
         "metric": "decode GB/s (visible K/V read)", "value": gbs, "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8 codes, fp16/fp32 arithmetic", "data": "synthetic",
@@ -531,7 +552,7 @@ def run_decode(args, wl):
         "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": gbs,
                      "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                      "peak_source": "measured copy bandwidth (MEASURED_PEAKS.json)",
-                     "traffic": profiled_traffic(wl.name, "decode_kernel"), "bytes_per_step": nbytes}}), flush=True)
+                     "traffic": profiled_traffic(wl.name, "decode_kernel"), "bytes_per_step": nbytes}}
 
 
 # --sweep: every benchmark workload in the default containers, then the 32k
@@ -682,6 +703,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="32k", choices=sorted(CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-rows", action="store_true",
+                    help="skip the short kv_append and decode measurements added to the default line")
     ap.add_argument("--gate", action="store_true", help="fuse the output gate out * sigmoid(q_gate) (extra row)")
     ap.add_argument("--op", choices=["prefill", "kv_append", "decode"], default="prefill",
                     help="kv_append / decode: time that step alone (extra rows)")
