@@ -56,6 +56,8 @@ CASES = {
     "over_512": _decode_wl("dec_600", 4, 2, tuple(int(x) for x in np.random.default_rng(51).integers(1, 300, 600)),
                            1, 8, 51, outliers=0.0),
     "kv_heads_8": _decode_wl("dec_h8", 8, 8, (5000, 129, 70000), 1, 256, 52),
+    # ~43.8k visible blocks: more than one wave of 128-block runs holds, so equal runs over several waves
+    "multi_wave": _decode_wl("dec_waves", 8, 1, (70000,) * 9 + (69999,), 1, 0, 53, outliers=0.0),
 }
 
 
