@@ -405,18 +405,77 @@ def run_ours(args, wl):
         # the next rows' steps on the same workload, briefly (the --op lines in full)
         short = argparse.Namespace(steps=20, warmup=3, gpus=1)
         extra = {}
-        for name, fn in (("kv_append", lambda: measure_kv_append(short, wl, inp)),
+        for name, fn in (("gated_prefill", lambda: measure_gated(short, wl, inp)),
+                         ("kv_append", lambda: measure_kv_append(short, wl, inp)),
                          ("decode", lambda: measure_decode(short, wl))):
             r = fn()
             extra[name] = {k: r[k] for k in ("metric", "value", "unit", "ms_per_step", "steps", "warmup", "config",
                                              "clocks", "gpu_launches")}
             extra[name]["roofline"] = {k: r["roofline"][k] for k in ("bound", "kernel", "achieved", "peak", "unit",
                                                                     "frac", "traffic")}
+        torch.cuda.empty_cache()
         line["extra_rows"] = extra
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def measure_gated(args, wl, inp):
+    """The prefill step with the output gate out * sigmoid(q_gate) fused into
+    the attention epilogue (the gate read adds total_q x HQ x 256 bf16 values):
+    the default metric, and the attention kernel against the measured bf16 peak."""
+    import torch
+
+    import windowed_prefill_attention_gb300 as pa
+    from synth import make_gate
+    dev = torch.device("cuda", 0)
+    q = torch.from_numpy(inp.q.view(np.int16)).view(torch.bfloat16).to(dev)
+    kp, vp = torch.from_numpy(inp.k_pool).to(dev), torch.from_numpy(inp.v_pool).to(dev)
+    ks, vs = torch.from_numpy(inp.k_scale).to(dev), torch.from_numpy(inp.v_scale).to(dev)
+    bt = torch.from_numpy(inp.block_table).to(dev)
+    gate = torch.from_numpy(make_gate(inp).view(np.int16)).view(torch.bfloat16).to(dev)
+    out = torch.empty_like(q)
+    flush = L2Flush(dev)
+    h = pa.pa_create(wl.n_q_heads, wl.n_kv_heads, inp.k_pool.shape[0], inp.block_table.shape[1], record_timing=True)
+    seqs, S, W, sm = inp.seq_desc, wl.n_sink_blk, wl.n_win_blk, wl.sm_scale
+    step = lambda: pa.pa_prefill_batch(h, seqs, q, kp, vp, ks, vs, bt, S, W, sm, out, q_gate=gate)  # noqa: E731
+    try:
+        for _ in range(args.warmup):
+            flush()
+            step()
+        pa.pa_timing(h, reset=True)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        sampler = ClockSampler(0)
+        torch.cuda.synchronize()
+        sampler.start()
+        time.sleep(0.2)
+        for i in range(args.steps):
+            flush()
+            starts[i].record()
+            step()
+            ends[i].record()
+        torch.cuda.synchronize()
+        clocks = sampler.stop()
+        rc = pa.pa_last_error(h)
+        if rc != 0:
+            raise RuntimeError("device error: %s" % pa.pa_strerror(rc))
+        total_ms = float(sum(a.elapsed_time(b) for a, b in zip(starts, ends)))
+        _, attn_ms, n_calls = pa.pa_timing(h, reset=True)
+    finally:
+        pa.pa_destroy(h)
+    ops = algorithmic_ops(wl)
+    attn_avg_ms = attn_ms / max(1, n_calls)
+    peak, peak_src = measured_peaks()
+    achieved = ops / (attn_avg_ms / 1e3) / 1e12
+    return {"metric": METRIC + ", output gate fused", "value": aggregate_tops(ops, args.steps, total_ms, 1),
+            "unit": UNIT, "ms_per_step": total_ms / args.steps, "steps": args.steps, "warmup": args.warmup,
+            "config": {"workload": wl.name, "gate": "out * sigmoid(q_gate), fused in the epilogue", "l2": L2_NOTE},
+            "clocks": clocks, "gpu_launches": 2 * args.steps,
+            "roofline": {"bound": "tensor", "kernel": "attention_kernel (gated epilogue)", "achieved": achieved,
+                         "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "launch_ms": attn_avg_ms}}
 
 
 def run_kv_append(args, wl):
