@@ -114,10 +114,20 @@ def measured_int8_peak():
     return best, "measured now: mma.sync.m16n8k32 s8 (no integer tcgen05 MMA on sm_103a), best of 1/2/4 blocks per SM"
 
 
-def kernel_source_hash():
+# The sources each profiled kernel is compiled from: its own file and the
+# device headers it includes (host-only files do not change the kernel).
+_DEVICE_HEADERS = ("pa_internal.h", "pa_ptx.cuh", "pa_tiles.cuh")
+KERNEL_SOURCES = {
+    "attention_kernel": ("pa_attention.cu",) + _DEVICE_HEADERS,
+    "decode_kernel": ("pa_decode.cu",) + _DEVICE_HEADERS,
+    "kv_append_kernel": ("pa_kernels.cu",) + _DEVICE_HEADERS,
+}
+
+
+def kernel_source_hash(kernel="attention_kernel"):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "windowed_prefill_attention_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -125,14 +135,14 @@ def kernel_source_hash():
 
 def profiled_traffic(config_name, kernel="attention_kernel"):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
-    was taken on the current kernel sources (else None)."""
+    was taken on the kernel's current sources (else None)."""
     path = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel, config_name))
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m_t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     m_h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
-    if not m_t or not m_h or m_h.group(1) != kernel_source_hash():
+    if not m_t or not m_h or m_h.group(1) != kernel_source_hash(kernel):
         return None
     return float(m_t.group(1))
 

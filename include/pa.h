@@ -214,6 +214,22 @@ int pa_decode(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const i
               const float* k_scale, const float* v_scale, const int32_t* block_table, int n_sink_blk, int n_win_blk,
               float sm_scale, void* out, void* stream);
 
+/* Host-only, no GPU needed: how pa_decode splits the work of one launch (the
+ * first min(n_seq, 512) sequences) when `slots` of its CTAs run at once (SMs x
+ * CTAs per SM; two per SM on a GB300).  The launch's (sequence, kv head)
+ * pairs, sequence-major, laid end to end give a list of *total_blocks visible
+ * 16-token blocks; CTA c computes the run from its first block to the next
+ * CTA's.  *listed = 1: one wave of runs of equal cost (blocks + 16 for every
+ * pair after a run's first), at most *per_cta (the budget, <= 128); 0: runs of
+ * *per_cta blocks over whole waves.  runs_out (may be NULL) receives *n_cta
+ * entries of int32[3] = {first block, its sequence, the CTA's partial slot in
+ * that block's pair (the CTAs before it in the pair)}; *max_slots = the most
+ * CTAs one pair's blocks meet.  PA_EINVAL for bad shapes, a sequence that is
+ * not a decode query (n_q == 1, q_start == n_ctx - 1), or cap < *n_cta. */
+int pa_decode_plan(int n_kv_heads, int slots, int n_seq, const pa_seq* seqs, int n_sink_blk, int n_win_blk,
+                   int32_t* runs_out, int cap, int* n_cta, int* per_cta, int* max_slots, int* listed,
+                   long long* total_blocks);
+
 /* Query rows per work unit: the G = n_q_heads / n_kv_heads q heads of one kv
  * head times PA_UNIT_ROWS / G consecutive tokens starting on a multiple of
  * PA_UNIT_ROWS / G.  One unit is one 256-row tensor-core tile computed by a

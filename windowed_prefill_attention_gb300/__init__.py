@@ -31,7 +31,8 @@ PA_P_F16, PA_P_U8 = 0, 1
 
 EXPORTED = ("pa_default_options", "pa_create", "pa_destroy", "pa_prefill", "pa_prefill_batch",
             "pa_prefill_batch_gated", "pa_prefill_host", "pa_kv_append", "pa_decode",
-            "pa_last_error", "pa_timing", "pa_strerror", "pa_plan", "pa_host_chunks", "pa_debug_gather",
+            "pa_last_error", "pa_timing", "pa_strerror", "pa_plan", "pa_host_chunks", "pa_decode_plan",
+            "pa_debug_gather",
             "pa_debug_maskset", "pa_debug_qcodes", "pa_debug_copy_streams_idle", "pa_prefill_noalloc")
 
 
@@ -63,6 +64,8 @@ _lib.pa_strerror.restype = C.c_char_p
 _lib.pa_plan.argtypes = [_i, _i, _i, C.POINTER(pa_seq), _i, _i, _vp, _i, C.POINTER(_i), C.POINTER(C.c_longlong),
                          C.POINTER(_i)]
 _lib.pa_host_chunks.argtypes = [_i, _i, _i, C.POINTER(pa_seq), _i, _vp, _i, C.POINTER(_i)]
+_lib.pa_decode_plan.argtypes = [_i, _i, _i, C.POINTER(pa_seq), _i, _i, _vp, _i, C.POINTER(_i), C.POINTER(_i),
+                                C.POINTER(_i), C.POINTER(_i), C.POINTER(C.c_longlong)]
 _lib.pa_debug_gather.argtypes = ([_vp, _i, C.POINTER(pa_seq)] + [_vp] * 5 + [_i, _i, _i] + [_vp] * 5
                                  + [_i, C.POINTER(_i), _vp])
 _lib.pa_debug_maskset.argtypes = [_vp, _i, C.POINTER(pa_seq), _i, _i, _vp, _vp, _i, _vp, _i, C.POINTER(_i), _vp]
@@ -258,6 +261,19 @@ def pa_host_chunks(n_q_heads, n_kv_heads, seqs, n_pairs):
     _check(_lib.pa_host_chunks(n_q_heads, n_kv_heads, len(s), s, n_pairs, ends.ctypes.data_as(C.c_void_p), n.value,
                                C.byref(n)), "pa_host_chunks")
     return ends
+
+
+def pa_decode_plan(n_kv_heads, slots, seqs, n_sink_blk, n_win_blk):
+    """Host-only: pa_decode's work split of one launch.  Returns (runs int32 [n_cta, 3] =
+    first block, sequence, partial slot; per_cta; max_slots; listed; total blocks)."""
+    s = _seqs(seqs)
+    n_cta, per_cta, max_slots, listed, total = C.c_int(), C.c_int(), C.c_int(), C.c_int(), C.c_longlong()
+    args = lambda buf, cap: (n_kv_heads, slots, len(s), s, n_sink_blk, n_win_blk, buf, cap, C.byref(n_cta),  # noqa: E731
+                             C.byref(per_cta), C.byref(max_slots), C.byref(listed), C.byref(total))
+    _check(_lib.pa_decode_plan(*args(None, 0)), "pa_decode_plan")
+    runs = np.zeros((n_cta.value, 3), dtype=np.int32)
+    _check(_lib.pa_decode_plan(*args(runs.ctypes.data_as(C.c_void_p), n_cta.value)), "pa_decode_plan")
+    return runs, per_cta.value, max_slots.value, bool(listed.value), total.value
 
 
 def pa_debug_gather(h, seqs, k_pool, v_pool, k_scale, v_scale, block_table, n_sink_blk, n_win_blk, seq, cap,

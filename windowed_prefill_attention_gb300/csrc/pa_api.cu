@@ -1021,7 +1021,117 @@ bool decode_pack(const std::vector<int>& len, int HKV, long long total, long lon
   }
   return true;
 }
+
+// Visible blocks of a decode query (the context's last token, t = n_ctx - 1)
+// under the prefill's block mask: sink blocks, then the window run up to t's block.
+int decode_n_vis(int n_ctx, int n_sink_blk, int n_win_blk) {
+  const int last = (n_ctx - 1) / kPage;
+  const int lo = n_win_blk > 0 ? std::max(0, last + 1 - n_win_blk) : 0;
+  const int n_sink = n_win_blk > 0 ? std::min(std::max(n_sink_blk, 0), lo) : 0;
+  return n_sink + (last - lo + 1);
+}
+
+// One decode launch (up to kDecParamSeqs sequences): the launch's pairs'
+// blocks end to end; one wave of cost-balanced runs listed in the parameters
+// when runs of at most 128 blocks fit in one wave, else whole waves of equal
+// runs of per_cta blocks.
+struct DecLaunch {
+  int s0 = 0, n = 0, total = 0, per_cta = 0, n_cta = 0, max_slots = 1;
+  bool listed = false;
+  DecRuns runs;
+};
+int decode_launch_plan(int HKV, long long slots, const int* n_vis, int s0, int n, DecLaunch& L) {
+  L = DecLaunch{};
+  L.s0 = s0;
+  L.n = n;
+  long long vis = 0;
+  int nv_max = 1;
+  std::vector<int> len;
+  for (int i = 0; i < n; ++i) {
+    vis += n_vis[i];
+    nv_max = std::max(nv_max, n_vis[i]);
+    for (int g = 0; g < HKV; ++g) len.push_back(n_vis[i]);
+  }
+  const long long total = vis * HKV;
+  if (total >= (1ll << 30) || slots < 1) return PA_EINVAL;
+  L.total = (int)total;
+  const long long wave = std::min<long long>(slots, kDecParamCtas);
+  if (total <= wave * kDecMaxCtaBlocks && decode_pack(len, HKV, total, kDecMaxCtaBlocks, wave, L.runs)) {
+    long long lo = std::max(1ll, (total + wave - 1) / wave), hi = kDecMaxCtaBlocks;
+    while (lo < hi) {  // the smallest budget that packs into one wave
+      const long long mid = (lo + hi) / 2;
+      if (decode_pack(len, HKV, total, mid, wave, L.runs)) hi = mid;
+      else lo = mid + 1;
+    }
+    (void)decode_pack(len, HKV, total, lo, wave, L.runs);
+    L.listed = true;
+    L.per_cta = (int)lo;
+    L.n_cta = (int)L.runs.x0.size();
+    L.max_slots = L.runs.max_slots;
+  } else {
+    const long long full = (total + kDecMaxCtaBlocks - 1) / kDecMaxCtaBlocks;
+    const long long waves = std::max(1ll, (full + slots - 1) / slots);
+    L.listed = false;
+    L.per_cta = (int)std::max(1ll, (total + waves * slots - 1) / (waves * slots));
+    L.n_cta = (int)((total + L.per_cta - 1) / L.per_cta);
+    L.max_slots = (nv_max - 1 + L.per_cta - 1) / L.per_cta + 1;  // CTA runs a pair's blocks can meet
+  }
+  return PA_OK;
+}
+
+// A decode query's checks: one token, the context's last, within the block table.
+bool decode_seq_ok(const pa_seq& q1, int max_pages) {
+  return q1.n_q == 1 && q1.q_off >= 0 && q1.n_ctx >= 1 && q1.q_start == q1.n_ctx - 1 &&
+         (q1.n_ctx + kPage - 1) / kPage <= max_pages;
+}
 }  // namespace
+
+int pa_decode_plan(int n_kv_heads, int slots, int n_seq, const pa_seq* seqs, int n_sink_blk, int n_win_blk,
+                   int32_t* runs_out, int cap, int* n_cta, int* per_cta, int* max_slots, int* listed,
+                   long long* total_blocks) {
+  if (n_kv_heads < 1 || n_kv_heads > 8 || slots < 1 || n_seq <= 0 || !seqs) return PA_EINVAL;
+  const int n = std::min(n_seq, kDecParamSeqs);
+  std::vector<int> n_vis((size_t)n);
+  for (int s = 0; s < n; ++s) {
+    if (!decode_seq_ok(seqs[s], INT32_MAX)) return PA_EINVAL;
+    n_vis[(size_t)s] = decode_n_vis(seqs[s].n_ctx, n_sink_blk, n_win_blk);
+  }
+  DecLaunch L;
+  const int rc = decode_launch_plan(n_kv_heads, slots, n_vis.data(), 0, n, L);
+  if (rc) return rc;
+  if (n_cta) *n_cta = L.n_cta;
+  if (per_cta) *per_cta = L.per_cta;
+  if (max_slots) *max_slots = L.max_slots;
+  if (listed) *listed = L.listed ? 1 : 0;
+  if (total_blocks) *total_blocks = L.total;
+  if (runs_out) {
+    if (cap < L.n_cta) return PA_EINVAL;
+    if (L.listed) {
+      for (int c = 0; c < L.n_cta; ++c) {
+        runs_out[3 * c] = L.runs.x0[(size_t)c];
+        runs_out[3 * c + 1] = L.runs.seq[(size_t)c];
+        runs_out[3 * c + 2] = L.runs.slot[(size_t)c];
+      }
+    } else {  // equal runs: CTA c starts at c per_cta; its slot counts the CTAs before it in that block's pair
+      long long pstart = 0;
+      int s = 0, g = 0;
+      for (int c = 0; c < L.n_cta; ++c) {
+        const long long x = (long long)c * L.per_cta;
+        while (x >= pstart + n_vis[(size_t)s]) {
+          pstart += n_vis[(size_t)s];
+          if (++g == n_kv_heads) {
+            g = 0;
+            ++s;
+          }
+        }
+        runs_out[3 * c] = (int)x;
+        runs_out[3 * c + 1] = s;
+        runs_out[3 * c + 2] = c - (int)(pstart / L.per_cta);
+      }
+    }
+  }
+  return PA_OK;
+}
 
 int pa_decode(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const int8_t* k_pool, const int8_t* v_pool,
               const float* k_scale, const float* v_scale, const int32_t* block_table, int n_sink_blk, int n_win_blk,
@@ -1031,64 +1141,17 @@ int pa_decode(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const i
   if (n_seq <= 0 || !seqs || h->G > 8 || !(sm_scale == sm_scale) || sm_scale < 0.f) return PA_EINVAL;
   std::vector<int> n_vis((size_t)n_seq);
   for (int s = 0; s < n_seq; ++s) {
-    const pa_seq& q1 = seqs[s];
-    if (q1.n_q != 1 || q1.q_off < 0 || q1.n_ctx < 1 || q1.q_start != q1.n_ctx - 1) return PA_EINVAL;
-    if ((q1.n_ctx + kPage - 1) / kPage > h->max_pages) return PA_EINVAL;
-    // the prefill's block mask for the query at t = n_ctx - 1: sink blocks, then the window run up to t's block
-    const int last = (q1.n_ctx - 1) / kPage;
-    const int lo = n_win_blk > 0 ? std::max(0, last + 1 - n_win_blk) : 0;
-    const int n_sink = n_win_blk > 0 ? std::min(std::max(n_sink_blk, 0), lo) : 0;
-    n_vis[(size_t)s] = n_sink + (last - lo + 1);
+    if (!decode_seq_ok(seqs[s], h->max_pages)) return PA_EINVAL;
+    n_vis[(size_t)s] = decode_n_vis(seqs[s].n_ctx, n_sink_blk, n_win_blk);
   }
-  // Launches of up to kDecParamSeqs sequences, their table in the launch's
-  // parameters.  Work split: the launch's pairs' blocks end to end; one wave
-  // of cost-balanced runs listed in the parameters when runs of at most 128
-  // blocks fit in one wave, else whole waves of equal runs of per_cta blocks.
-  struct Launch {
-    int s0, n, total, per_cta, n_cta, max_slots;
-    bool listed;
-    DecRuns runs;
-  };
-  std::vector<Launch> launches;
+  // launches of up to kDecParamSeqs sequences, their table in the launch's parameters
+  std::vector<DecLaunch> launches;
   const long long slots = (long long)h->n_sm * decode_ctas_per_sm(h->HKV);
-  const long long wave = std::min<long long>(slots, kDecParamCtas);
   size_t part_need = 0;
   for (int s0 = 0; s0 < n_seq; s0 += kDecParamSeqs) {
-    Launch L{};
-    L.s0 = s0;
-    L.n = std::min(kDecParamSeqs, n_seq - s0);
-    long long vis = 0;
-    int nv_max = 1;
-    std::vector<int> len;
-    for (int i = 0; i < L.n; ++i) {
-      const int nv = n_vis[(size_t)(s0 + i)];
-      vis += nv;
-      nv_max = std::max(nv_max, nv);
-      for (int g = 0; g < h->HKV; ++g) len.push_back(nv);
-    }
-    const long long total = vis * h->HKV;
-    if (total >= (1ll << 30)) return PA_EINVAL;
-    L.total = (int)total;
-    if (total <= wave * kDecMaxCtaBlocks && decode_pack(len, h->HKV, total, kDecMaxCtaBlocks, wave, L.runs)) {
-      long long lo = std::max(1ll, (total + wave - 1) / wave), hi = kDecMaxCtaBlocks;
-      while (lo < hi) {  // the smallest budget that packs into one wave
-        const long long mid = (lo + hi) / 2;
-        if (decode_pack(len, h->HKV, total, mid, wave, L.runs)) hi = mid;
-        else lo = mid + 1;
-      }
-      (void)decode_pack(len, h->HKV, total, lo, wave, L.runs);
-      L.listed = true;
-      L.per_cta = (int)lo;
-      L.n_cta = (int)L.runs.x0.size();
-      L.max_slots = L.runs.max_slots;
-    } else {
-      const long long full = (total + kDecMaxCtaBlocks - 1) / kDecMaxCtaBlocks;
-      const long long waves = std::max(1ll, (full + slots - 1) / slots);
-      L.listed = false;
-      L.per_cta = (int)std::max(1ll, (total + waves * slots - 1) / (waves * slots));
-      L.n_cta = (int)((total + L.per_cta - 1) / L.per_cta);
-      L.max_slots = (nv_max - 1 + L.per_cta - 1) / L.per_cta + 1;  // CTA runs a pair's blocks can meet
-    }
+    DecLaunch L;
+    if ((rc = decode_launch_plan(h->HKV, slots, n_vis.data() + s0, s0, std::min(kDecParamSeqs, n_seq - s0), L)))
+      return rc;
     part_need = std::max(part_need, (size_t)L.n * h->HKV * L.max_slots * h->G * kDecPartStride);
     launches.push_back(std::move(L));
   }
@@ -1134,7 +1197,7 @@ int pa_decode(pa_handle h, int n_seq, const pa_seq* seqs, const void* q, const i
   p.err = h->d_err;
   p.wait_ns = (unsigned long long)h->opt.wait_timeout_ms * 1000000ull;
   DecodeSeqs tab;
-  for (const Launch& L : launches) {
+  for (const DecLaunch& L : launches) {
     int vstart = 0;
     for (int i = 0; i < L.n; ++i) {
       const pa_seq& q1 = seqs[L.s0 + i];
