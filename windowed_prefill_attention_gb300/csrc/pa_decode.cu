@@ -34,14 +34,17 @@
 // 16-byte words of the swizzled rows instead of gathering bytes.
 //
 // Work split: the launch's (sequence, kv head) pairs laid end to end give one
-// list of visible blocks; CTA c takes blocks [c B, c B + B) of it, B chosen so
-// that the grid is one wave of equal CTAs (or whole waves of 128-block CTAs).
-// A CTA's run covers one or more segments (the part of a run that falls in
-// one pair).  Per segment its 4 warps take the blocks in turn, then combine in
-// shared memory: a segment that is a whole pair writes bf16 out directly;
-// otherwise it writes a partial (row max, row sum, unnormalised O per q head)
-// and adds its block count to the pair's ticket, and the CTA that completes
-// the count merges the pair's partials and writes bf16 out.
+// list of visible blocks; each CTA takes a run of it: runs of equal cost
+// (blocks, plus a fixed charge for every pair a run crosses into) listed by
+// the host in the launch parameters when one wave holds them, else equal runs
+// over whole waves.  A CTA's run covers one or more segments (the part of a
+// run that falls in one pair).  Per segment its 4 warps take the blocks in
+// turn, then combine in shared memory in a fixed order (a call's result does
+// not depend on scheduling): a segment that is a whole pair writes bf16 out
+// directly; otherwise it writes a partial (row max, row sum, unnormalised O
+// per q head) and adds its block count to the pair's ticket, and the CTA that
+// completes the count merges the pair's partials and writes bf16 out.  The
+// next segment's query rows are bulk-copied while the current one runs.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
