@@ -327,6 +327,15 @@ int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_pages, int max_
                        const int32_t* block_table, int q_start, int n_q, int n_ctx, int n_sink_blk, int n_win_blk,
                        float sm_scale, void* out, void* stream);
 
+/* Debug export (tests only; like pa_prefill_noalloc, the pages have no
+ * counterpart): copies the work list the last pa_prefill_noalloc call on the
+ * current device built in its scratch array into units_out (host int32
+ * [n_units][4] = {sequence (0), kv head, first token, key tiles}, the layout
+ * of pa_plan's units).  Synchronous on `stream`; call it after that call and
+ * before any other on the device.  PA_EINVAL for n_units outside (0, the
+ * array's work-list capacity] or a NULL pointer. */
+int pa_debug_noalloc_units(int n_units, int32_t* units_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

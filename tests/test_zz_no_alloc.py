@@ -62,6 +62,20 @@ def test_noalloc_matches_handle_entry_point_on_consecutive_calls():
             assert np.array_equal(got, ref), wl.name
 
 
+def test_noalloc_work_list_has_the_planner_order():
+    """The work list the ordering kernel builds on the device is pa_plan's, unit
+    for unit (longest first, ties by first token then kv head)."""
+    import windowed_prefill_attention_gb300 as pa
+    for wl, S, W in CASES:
+        inp = make_inputs(wl)
+        _, rc = call_noalloc(inp, S, W)
+        assert rc == 0
+        want, _, _ = pa.pa_plan(wl.n_q_heads, wl.n_kv_heads, inp.seq_desc, S, W)
+        got = pa.pa_debug_noalloc_units(len(want))
+        assert np.array_equal(got, want), wl.name
+        assert np.all(np.diff(got[:, 3]) <= 0)  # decreasing key tiles
+
+
 def test_noalloc_rejects_contexts_beyond_its_scratch():
     import windowed_prefill_attention_gb300 as pa
     inp = make_inputs(CONFIGS["tiny"])

@@ -33,7 +33,8 @@ EXPORTED = ("pa_default_options", "pa_create", "pa_destroy", "pa_prefill", "pa_p
             "pa_prefill_batch_gated", "pa_prefill_host", "pa_kv_append", "pa_decode",
             "pa_last_error", "pa_timing", "pa_strerror", "pa_plan", "pa_host_chunks", "pa_decode_plan",
             "pa_debug_gather",
-            "pa_debug_maskset", "pa_debug_qcodes", "pa_debug_copy_streams_idle", "pa_prefill_noalloc")
+            "pa_debug_maskset", "pa_debug_qcodes", "pa_debug_copy_streams_idle", "pa_prefill_noalloc",
+            "pa_debug_noalloc_units")
 
 
 class pa_options(C.Structure):
@@ -72,6 +73,7 @@ _lib.pa_debug_maskset.argtypes = [_vp, _i, C.POINTER(pa_seq), _i, _i, _vp, _vp, 
 _lib.pa_debug_qcodes.argtypes = [_vp, _i, _vp, _vp, _vp]
 _lib.pa_debug_copy_streams_idle.argtypes = [_vp]
 _lib.pa_prefill_noalloc.argtypes = [_i] * 4 + [_vp] * 6 + [_i] * 5 + [_f, _vp, _vp]
+_lib.pa_debug_noalloc_units.argtypes = [_i, _vp, _vp]
 
 
 class PAError(RuntimeError):
@@ -219,6 +221,14 @@ def pa_prefill_noalloc(n_q_heads, n_kv_heads, n_pool_pages, max_pages_per_seq, q
     _check(_lib.pa_prefill_noalloc(n_q_heads, n_kv_heads, n_pool_pages, max_pages_per_seq, *args, q_start, n_q, n_ctx,
                                    n_sink_blk, n_win_blk, float(sm_scale), _dev(out, torch.bfloat16, "out"),
                                    _stream(stream)), "pa_prefill_noalloc")
+
+
+def pa_debug_noalloc_units(n_units, stream=None):
+    """The work list (int32 [n_units, 4]) the last pa_prefill_noalloc call on the current device built."""
+    units = np.zeros((n_units, 4), dtype=np.int32)
+    _check(_lib.pa_debug_noalloc_units(n_units, units.ctypes.data_as(C.c_void_p), _stream(stream)),
+           "pa_debug_noalloc_units")
+    return units
 
 
 def pa_debug_copy_streams_idle(h) -> bool:

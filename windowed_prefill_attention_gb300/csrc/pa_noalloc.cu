@@ -294,3 +294,22 @@ extern "C" int pa_prefill_noalloc(int n_q_heads, int n_kv_heads, int n_pool_page
   if (e & DEV_ERR_BAD_PAGE) return PA_EBADPAGE;
   return e ? PA_ECUDA : PA_OK;
 }
+
+// Debug export (tests): the work list the last call on the current device
+// built, read back from the scratch array on `stream`.
+int pa_debug_noalloc_units(int n_units, int32_t* units_out, void* stream) {
+  if (n_units <= 0 || n_units > kMaxUnits || !units_out) return PA_EINVAL;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ECUDA;
+  DeviceSetup ds;
+  const int rc = device_setup(dev, &ds);
+  if (rc) return rc;
+  if (!ds.sm103) return PA_EARCH;
+  static_assert(sizeof(Unit) == 4 * sizeof(int32_t), "a unit is four int32");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(units_out, static_cast<unsigned char*>(ds.addr) + kHeaderBytes, (size_t)n_units * sizeof(Unit),
+                      cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return PA_ECUDA;
+  return PA_OK;
+}
