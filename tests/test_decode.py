@@ -123,3 +123,43 @@ def test_decode_repeated_calls_on_one_handle_are_identical():
             assert np.array_equal(out.float().cpu().numpy(), ref, equal_nan=True)
     finally:
         pa.pa_destroy(h)
+
+
+def test_decode_full_size_bench_configuration():
+    """The bench's decode step at full size, in its launch configuration: 64
+    sequences at a 32768-token context, 16 q / 2 kv heads, 1 sink block + a
+    256-block window (one wave of cost-balanced runs), every output row against
+    the fp64 definition.  Only the 257 visible pages of a sequence hold data
+    (random codes, scales in [1e-3, 2e-2]); its other block-table entries
+    point at a valid page that the mask never visits."""
+    from synth.workloads import Inputs
+    rng = np.random.default_rng(123)
+    n_seq, ctx, hq, hkv, S, W = 64, 32768, 16, 2, 1, 256
+    pages = ctx // 16
+    vis_blocks = [0] + list(range(pages - W, pages))
+    n_pool = n_seq * len(vis_blocks)
+    perm = rng.permutation(n_pool).astype(np.int32)
+    bt = np.zeros((n_seq, pages), dtype=np.int32)
+    bt[:, vis_blocks] = perm.reshape(n_seq, len(vis_blocks))
+    def codes():  # int8 codes in [-127, 127]: random 64-bit words as bytes, -128 raised to -127
+        n = n_pool * 16 * hkv * 256
+        c = rng.integers(0, 2**63, size=n // 8, dtype=np.uint64).view(np.int8).reshape(n_pool, 16, hkv, 256)
+        return np.maximum(c, np.int8(-127))
+    k_pool, v_pool = codes(), codes()
+    k_scale = (rng.random((n_pool, 16, hkv), dtype=np.float32) * 0.019 + 0.001).astype(np.float32)
+    v_scale = (rng.random((n_pool, 16, hkv), dtype=np.float32) * 0.019 + 0.001).astype(np.float32)
+    q32 = rng.standard_normal((n_seq, hq, 256), dtype=np.float32)
+    u = q32.view(np.uint32)
+    q = ((u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)).astype(np.uint16)
+    desc = np.array([(s, ctx - 1, 1, ctx) for s in range(n_seq)], dtype=np.int32)
+    wl = Workload("dec_bench", hq, hkv, tuple((ctx - 1, 1) for _ in range(n_seq)), S, W, seed=0)
+    inp = Inputs(wl, q, k_pool, v_pool, k_scale, v_scale, bt, desc)
+    out, rc = run_decode(inp)
+    assert rc == 0
+    rows = oracle.all_rows(inp)
+    ref = oracle.exact(oracle.Problem.from_inputs(inp), rows)
+    got = out[rows[:, 0], rows[:, 1]].astype(np.float64)
+    assert np.isfinite(got).all()
+    mx, mean = norm_errors(got, ref)
+    assert mx <= TOL_MAX and mean <= TOL_MEAN, (mx, mean)
+
