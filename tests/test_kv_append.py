@@ -177,3 +177,21 @@ def test_kv_append_scale_is_the_rounded_quotient_for_every_bf16_magnitude():
                             0, bits, bits)
     for got, ref in zip((kp, vp), want[:2]):
         assert np.array_equal(got.view(np.uint8), ref.view(np.uint8))
+
+
+def test_kv_append_full_size_bench_configuration():
+    """The bench's append at full size: every one of the 32k workload's 32768
+    tokens, 2 kv heads, quantised into its pool through its block table
+    (N(0,1) rows with 1 % of tokens x8, one all-zero row); every code and
+    scale of the pool equals the oracle's, every other slot unchanged."""
+    inp = make_inputs(CONFIGS["32k"])
+    hkv = inp.wl.n_kv_heads
+    q_off, q_start, n_q, n_ctx = inp.seq_desc[0].tolist()
+    kn, vn = _new_rows(n_q, hkv, 300), _new_rows(n_q, hkv, 301)
+    (kp, vp, ks, vs), rc = _append_gpu(inp, 0, q_start, kn, vn)
+    assert rc == 0
+    want = oracle.kv_append(inp.k_pool, inp.v_pool, inp.k_scale, inp.v_scale, inp.block_table[0], q_start, kn, vn)
+    for got, ref in zip((kp, vp, ks, vs), want):
+        bits = (lambda a: a.view(np.uint8)) if got.dtype == np.int8 else (lambda a: a.view(np.uint32))
+        assert np.array_equal(bits(got), bits(ref))
+
