@@ -200,8 +200,8 @@ int pa_kv_append(pa_handle h, const void* k_new, const void* v_new, int n_new, i
  * == n_ctx - 1: the token is the context's last; its row in q and out is
  * seqs[s].q_off; block_table row s holds its pages.  Layouts as pa_prefill_batch
  * (q, out bf16 [rows][n_q_heads][256]).  The visible 16-token blocks of all
- * (sequence, kv head) pairs are split into equal runs computed in parallel
- * and merged on the device; q, the pool and P' stay in exact or fp16
+ * (sequence, kv head) pairs are split into runs of equal cost (pa_decode_plan)
+ * computed in parallel and merged on the device; q, the pool and P' stay in exact or fp16
  * containers (the bf16 query scaled per row by a power of two, codes as exact
  * fp16, P' = p * v_scale in fp16, fp32 accumulation).  One launch per 512
  * sequences, the sequence table carried in its parameters (no host-to-device
