@@ -466,33 +466,47 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
       if (!(ok = oks)) break;
       // y = S * k_scale (masked: -inf), in place, and each row's maximum; the
       // products in fp32 pairs, the maximum three operands at a time
-      const bool full = !tg.needs_mask && tg.nb == kTileBlocks;  // every row sees every key
-      unsigned long long vis[2][2] = {{~0ull, ~0ull}, {~0ull, ~0ull}};  // [row][key half] >> tcol
-      if (!full) {
+      // A tile every row sees in full (most of them) takes a loop without the
+      // mask: with the mask's selects inside one loop under a condition, they
+      // were executed as predicated instructions on every tile.
+      const bool full = !tg.needs_mask && tg.nb == kTileBlocks;
+      float mx[2][2] = {{-INFINITY, -INFINITY}, {-INFINITY, -INFINITY}};
+      if (full) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float2 k2 = *reinterpret_cast<const float2*>(ksp + 8 * k);
+          const float2 a = mul2(make_float2(__uint_as_float(sv[4 * k]), __uint_as_float(sv[4 * k + 1])), k2);
+          const float2 b = mul2(make_float2(__uint_as_float(sv[4 * k + 2]), __uint_as_float(sv[4 * k + 3])), k2);
+          sv[4 * k] = __float_as_uint(a.x);
+          sv[4 * k + 1] = __float_as_uint(a.y);
+          sv[4 * k + 2] = __float_as_uint(b.x);
+          sv[4 * k + 3] = __float_as_uint(b.y);
+          mx[0][k & 1] = max3(mx[0][k & 1], a.x, a.y);
+          mx[1][k & 1] = max3(mx[1][k & 1], b.x, b.y);
+        }
+      } else {
+        unsigned long long vis[2][2];  // [row][key half] >> tcol
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) vis[i][hf] = visible_columns(tg, t_row[i], p.S, p.W, hf) >> tcol;
-      }
-      float mx[2][2] = {{-INFINITY, -INFINITY}, {-INFINITY, -INFINITY}};
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float2 k2 = *reinterpret_cast<const float2*>(ksp + 8 * k);
-        float2 a = mul2(make_float2(__uint_as_float(sv[4 * k]), __uint_as_float(sv[4 * k + 1])), k2);
-        float2 b = mul2(make_float2(__uint_as_float(sv[4 * k + 2]), __uint_as_float(sv[4 * k + 3])), k2);
-        if (!full) {
+        for (int k = 0; k < 16; ++k) {
+          const float2 k2 = *reinterpret_cast<const float2*>(ksp + 8 * k);
+          float2 a = mul2(make_float2(__uint_as_float(sv[4 * k]), __uint_as_float(sv[4 * k + 1])), k2);
+          float2 b = mul2(make_float2(__uint_as_float(sv[4 * k + 2]), __uint_as_float(sv[4 * k + 3])), k2);
           const int hf = k >> 3, sh = 8 * (k & 7);
           a.x = ((vis[0][hf] >> sh) & 1ull) ? a.x : -INFINITY;
           a.y = ((vis[0][hf] >> (sh + 1)) & 1ull) ? a.y : -INFINITY;
           b.x = ((vis[1][hf] >> sh) & 1ull) ? b.x : -INFINITY;
           b.y = ((vis[1][hf] >> (sh + 1)) & 1ull) ? b.y : -INFINITY;
+          sv[4 * k] = __float_as_uint(a.x);
+          sv[4 * k + 1] = __float_as_uint(a.y);
+          sv[4 * k + 2] = __float_as_uint(b.x);
+          sv[4 * k + 3] = __float_as_uint(b.y);
+          mx[0][k & 1] = max3(mx[0][k & 1], a.x, a.y);
+          mx[1][k & 1] = max3(mx[1][k & 1], b.x, b.y);
         }
-        sv[4 * k] = __float_as_uint(a.x);
-        sv[4 * k + 1] = __float_as_uint(a.y);
-        sv[4 * k + 2] = __float_as_uint(b.x);
-        sv[4 * k + 3] = __float_as_uint(b.y);
-        mx[0][k & 1] = max3(mx[0][k & 1], a.x, a.y);
-        mx[1][k & 1] = max3(mx[1][k & 1], b.x, b.y);
       }
       // the reference of a row moves only when its max grew by more than 2^kLazy
       float alpha[2] = {1.f, 1.f}, mref[2];
