@@ -326,76 +326,167 @@ __device__ __forceinline__ void role_producer_q(const AttnParams& p, const AttnM
 // ------------------------------------------------------------------ MMA issuer
 // One thread of the even CTA issues every MMA of the pair: 256 query rows
 // (128 in each CTA's TMEM lanes) against the tile's keys.
+//
+// This thread is the pipeline's critical path (clock64 stamps on GB300): each
+// tcgen05.mma costs it ~70-80 cycles to issue whatever its operands, and a
+// wait, a commit or a branch between MMA groups ~60-150, while the tensor pipe
+// runs a tile's 16 QK^T MMAs in ~1024 cycles and its 8 PV MMAs in ~1024.  So
+// the MMAs of a tile are issued from one asm block each and the rare arrivals
+// and commits are predicated or kept off the common path.
+
+// S(t) = Q K(t)^T for a tile: 16 MMAs, Q region r at qd + 1024 r and the K
+// slot's region r at kd + 512 r (start addresses in 16-byte units), k-step q
+// at + 2 q within the 128-byte swizzled rows; the first MMA overwrites D.
+__device__ __forceinline__ void mma_qk_tile(uint32_t d, uint64_t qd, uint64_t kd, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .b64 a, b;\n\t.reg .pred pf, pt;\n\t"
+      "setp.ne.b32 pf, %4, 0;\n\tsetp.eq.b32 pt, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+      "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 4;\n\tadd.s64 b, %2, 4;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 6;\n\tadd.s64 b, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 1024;\n\tadd.s64 b, %2, 512;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 1026;\n\tadd.s64 b, %2, 514;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 1028;\n\tadd.s64 b, %2, 516;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 1030;\n\tadd.s64 b, %2, 518;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 2048;\n\tadd.s64 b, %2, 1024;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 2050;\n\tadd.s64 b, %2, 1026;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 2052;\n\tadd.s64 b, %2, 1028;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 2054;\n\tadd.s64 b, %2, 1030;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 3072;\n\tadd.s64 b, %2, 1536;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 3074;\n\tadd.s64 b, %2, 1538;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 3076;\n\tadd.s64 b, %2, 1540;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 3078;\n\tadd.s64 b, %2, 1542;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "}" ::"r"(d), "l"(qd), "l"(kd), "r"(idesc), "r"(0u)
+      : "memory");
+}
+// O (+)= P' V for a full tile: 8 MMAs, P' of 64-key chunk ch at TMEM column
+// a + 64 ch + 8 ks, its V^T slot at vd0 / vd1 + 2 ks; the first MMA
+// accumulates iff acc0.
+__device__ __forceinline__ void mma_pv_tile(uint32_t d, uint32_t a, uint64_t vd0, uint64_t vd1, uint32_t idesc,
+                                            uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .b64 b;\n\t.reg .b32 ta;\n\t.reg .pred pa, pt;\n\t"
+      "setp.ne.b32 pa, %5, 0;\n\tsetp.eq.b32 pt, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %4, pa;\n\t"
+      "add.u32 ta, %1, 8;\n\tadd.s64 b, %2, 2;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+      "add.u32 ta, %1, 16;\n\tadd.s64 b, %2, 4;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+      "add.u32 ta, %1, 24;\n\tadd.s64 b, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+      "add.u32 ta, %1, 64;\n\tadd.s64 b, %3, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+      "add.u32 ta, %1, 72;\n\tadd.s64 b, %3, 2;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+      "add.u32 ta, %1, 80;\n\tadd.s64 b, %3, 4;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+      "add.u32 ta, %1, 88;\n\tadd.s64 b, %3, 6;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+      "}" ::"r"(d), "r"(a), "l"(vd0), "l"(vd1), "r"(idesc), "r"(acc0), "r"(0u)
+      : "memory");
+}
+// mma_commit_pair when `pred` holds, without a branch.
+__device__ __forceinline__ void mma_commit_pair_if(uint32_t bar, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+      "@q tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(bar),
+      "h"((uint16_t)3), "r"((uint32_t)pred)
+      : "memory");
+}
+
 __device__ __forceinline__ void role_mma(const AttnParams& p, const Ctx& c) {
   uint32_t tc = 0;  // global tile counter: K/V slots and S buffer by its parity
   int k_unit = 0;
   bool ok = true;
   const uint32_t id_pv = idesc_f16(kUnitRows, kHeadDim, false, false);
   const uint32_t qsoon_peer = cluster_addr(c.bar(B_QSOON), 1);
+  const uint64_t qd = sdesc_k_sw128(c.sbase + kSmQ);
+  // K slots and V^T slots by tile parity (selected, not indexed: kept in registers)
+  const uint64_t kd0 = sdesc_k_sw128(c.sbase + kSmK), kd1 = sdesc_k_sw128(c.sbase + kSmK + 4 * kKSlotBytes);
+  const uint64_t vd00 = sdesc_k_sw128(c.sbase + kSmV), vd01 = sdesc_k_sw128(c.sbase + kSmV + kVSlotBytes);
+  const uint64_t vd10 = sdesc_k_sw128(c.sbase + kSmV + 2 * kVSlotBytes);
+  const uint64_t vd11 = sdesc_k_sw128(c.sbase + kSmV + 3 * kVSlotBytes);
   for (int u = c.pair; u < p.n_units && ok; u += c.n_pairs, ++k_unit) {
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
     const UnitGeom ug = unit_geom(un.t0, 2 * p.TQ, sg, p.S, p.W);
     const int n = ug.n_tiles;
+    const int jsoon = imax(0, n - kQSoon);  // its QK^T lets the next unit's Q rows be prefetched
     const int qbar = p.debug_stall ? B_STALL : (p.q_mode == 1 ? B_QREADY2 : B_QFULL);
     if (!(ok = (qbar == B_QREADY2 ? c.wait_cluster(qbar, k_unit & 1, 20) : c.wait(qbar, k_unit & 1, 20)))) break;
-    for (int j = 0; j <= n; ++j) {
-      if (j < n) {  // S(j) = Q K(j)^T, region by region
-        const uint32_t t = tc + j;
-        const uint32_t d = c.tb + kTmS + (t & 1) * kTileKeys;
-        const uint32_t id = idesc_f16(kUnitRows, tile_width(ug, j) * kPage, true, true);  // bf16 Q, bf16 K codes
-        if (!(ok = c.wait(B_KFULL + (t & 1), (t >> 1) & 1, 21))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          // Q region r and K slot (t & 1, r): SW128 K-major, k-step q at +32 q bytes
-          const uint64_t qd = sdesc_k_sw128(c.sbase + kSmQ + r * kRegionBytes);
-          const uint64_t kd = sdesc_k_sw128(c.sbase + kSmK + ((int)(t & 1) * 4 + r) * kKSlotBytes);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) mma_ss_pair(d, qd + 2 * q, kd + 2 * q, id, (r | q) != 0 ? 1u : 0u);
-        }
-        mma_commit_pair(c.bar(B_SFULL + (t & 1)));  // S(t) ready; tile t's K slots free
-        if (j == n - 1) mma_commit_pair(c.bar(B_QEMPTY));
-        if (j == imax(0, n - kQSoon)) {
-          mbar_arrive(c.bar(B_QSOON));
-          mbar_arrive_cluster(qsoon_peer);
+    // S(j) = Q K(j)^T, then the unit's rare arrivals: Q free after its last
+    // QK^T, the prefetch of the next unit's Q rows a few tiles before
+    auto qk = [&](int j) {
+      const uint32_t t = tc + j;
+      const uint32_t d = c.tb + kTmS + (t & 1) * kTileKeys;
+      const uint32_t id = idesc_f16(kUnitRows, tile_width(ug, j) * kPage, true, true);  // bf16 Q, bf16 K codes
+      if (!c.wait(B_KFULL + (t & 1), (t >> 1) & 1, 21)) return false;
+      tc_fence_after();
+      mma_qk_tile(d, qd, (t & 1) ? kd1 : kd0, id);
+      mma_commit_pair(c.bar(B_SFULL + (t & 1)));  // S(t) ready; tile t's K slots free
+      mma_commit_pair_if(c.bar(B_QEMPTY), j == n - 1);
+      if (__builtin_expect(j == jsoon, 0)) {
+        // a timing hint, no data: the CTA-scope arrive (a cluster-scope
+        // release would wait for this thread's MMAs in flight)
+        mbar_arrive(c.bar(B_QSOON));
+        mbar_arrive_remote(qsoon_peer);
+      }
+      return true;
+    };
+    // O (+)= P(j) V(j), then O's release to the epilogue after the unit's last
+    auto pv = [&](int j) {
+      const uint32_t t = tc + j;
+      if (!c.wait(B_VFULL + (t & 1), (t >> 1) & 1, 23)) return false;
+      if (!c.wait(B_PFULL + (t & 1), (t >> 1) & 1, 22)) return false;
+      // the previous unit's O was read by the epilogue of both CTAs
+      if (__builtin_expect(j == 0 && k_unit > 0, 0) && !c.wait(B_OEMPTY, (k_unit - 1) & 1, 24)) return false;
+      const uint32_t a = c.tb + kTmS + (t & 1) * kTileKeys;
+      const int nb = tile_width(ug, j);
+      const uint32_t acc0 = j > 0 ? 1u : 0u;
+      const uint64_t vd0 = (t & 1) ? vd10 : vd00, vd1 = (t & 1) ? vd11 : vd01;
+      tc_fence_after();
+      // k-step ks of chunk ch covers keys [64 ch + 16 ks, +16); P' of chunk ch
+      // sits at S columns [64 ch, 64 ch + 32)
+      if (__builtin_expect(nb == kTileBlocks, 1)) {
+        mma_pv_tile(c.tb + kTmO, a, vd0, vd1, id_pv, acc0);
+      } else {
+        for (int ch = 0; ch < n_chunks(nb); ++ch) {
+          const int nks = imin(4, nb - 4 * ch);
+          for (int ks = 0; ks < nks; ++ks)
+            mma_ts_pair(c.tb + kTmO, a + 64 * ch + 8 * ks, (ch ? vd1 : vd0) + (uint64_t)(2 * ks), id_pv,
+                        (ch > 0 || ks > 0) ? 1u : acc0);
         }
       }
-      if (j >= 1) {  // O (+)= P(j-1) V(j-1), chunk by chunk
-        const int jj = j - 1;
-        const uint32_t t = tc + jj;
-        if (!(ok = c.wait(B_PFULL + (t & 1), (t >> 1) & 1, 22))) break;
-        if (jj == 0 && k_unit > 0 && !(ok = c.wait(B_OEMPTY, (k_unit - 1) & 1, 24))) break;
-        const uint32_t a = c.tb + kTmS + (t & 1) * kTileKeys;
-        const int nb = tile_width(ug, jj);
-        if (!(ok = c.wait(B_VFULL + (t & 1), (t >> 1) & 1, 23))) break;
-        tc_fence_after();
-        // k-step ks of chunk ch covers keys [64 ch + 16 ks, +16); P of chunk ch
-        // sits at S columns [64 ch, 64 ch + 32).  A full tile's eight MMAs are
-        // issued straight-line: a loop with a data-dependent trip count between
-        // MMAs leaves the tensor pipe idle for most of each instruction.
-        const uint64_t vd0 = sdesc_k_sw128(c.sbase + kSmV + (int)(t & 1) * 2 * kVSlotBytes);
-        const uint64_t vd1 = sdesc_k_sw128(c.sbase + kSmV + ((int)(t & 1) * 2 + 1) * kVSlotBytes);
-        const uint32_t acc0 = jj > 0 ? 1u : 0u;
-        if (nb == kTileBlocks) {
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_ts_pair(c.tb + kTmO, a + 8 * ks, vd0 + (uint64_t)(2 * ks), id_pv, ks > 0 ? 1u : acc0);
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) mma_ts_pair(c.tb + kTmO, a + 64 + 8 * ks, vd1 + (uint64_t)(2 * ks), id_pv, 1u);
-        } else {
-          for (int ch = 0; ch < n_chunks(nb); ++ch) {
-            const int nks = imin(4, nb - 4 * ch);
-            for (int ks = 0; ks < nks; ++ks)
-              mma_ts_pair(c.tb + kTmO, a + 64 * ch + 8 * ks, (ch ? vd1 : vd0) + (uint64_t)(2 * ks), id_pv,
-                          (ch > 0 || ks > 0) ? 1u : acc0);
-          }
-        }
-        mma_commit_pair(c.bar(B_VEMPTY + (t & 1)));  // tile t's V^T slots free; O holds PV up to tile t
-        if (jj == n - 1) mma_commit_pair(c.bar(B_OFULL));
+      mma_commit_pair(c.bar(B_VEMPTY + (t & 1)));  // tile t's V^T slots free; O holds PV up to tile t
+      mma_commit_pair_if(c.bar(B_OFULL), j == n - 1);
+      return true;
+    };
+    // QK^T(j) before PV(j - 1): the tensor pipe computes the next scores
+    // while the softmax handles the current ones
+    if (!(ok = qk(0))) break;
+    for (int j = 1; j < n; ++j) {
+      if (__builtin_expect(!qk(j), 0) || __builtin_expect(!pv(j - 1), 0)) {
+        ok = false;
+        break;
       }
     }
-    if (!ok) break;
+    if (!ok || !(ok = pv(n - 1))) break;
     tc += n;
   }
   // every issued MMA completes before TMEM is freed (the odd CTA waits for

@@ -134,7 +134,8 @@ struct WaitCtl {
 // other thread has already recorded an error.  Never spins without bound.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& w,
                                           int site) {
-  if (mbar_try_wait(bar, parity)) return true;
+  // the phase is normally complete already: keep that path straight
+  if (__builtin_expect(mbar_try_wait(bar, parity), 1)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
@@ -150,7 +151,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 
 // As mbar_wait, with acquire at cluster scope.
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, const WaitCtl& w, int site) {
-  if (mbar_try_wait_cluster(bar, parity, 0u)) return true;
+  if (__builtin_expect(mbar_try_wait_cluster(bar, parity, 0u), 1)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait_cluster(bar, parity, 20000u)) return true;

@@ -136,11 +136,13 @@ PA_HD TileGeom tile_geom(const UnitGeom& u, int i, int S, int W) {
 }
 
 // Width in blocks of tile i, the same as tile_geom(u, i, S, W).nb: only the
-// last tile of each run can be narrower than kTileBlocks.
+// last tile of each run can be narrower than kTileBlocks.  Written as selects
+// (no branch): the MMA issuer evaluates it per tile on its critical path.
 PA_HD int tile_width(const UnitGeom& u, int i) {
-  if (i == u.n_tiles - 1) return (u.qb + 1 - u.ws) - (u.n_tiles - 1 - u.n_sink_tiles) * kTileBlocks;
-  if (i == u.n_sink_tiles - 1) return u.nsk - i * kTileBlocks;
-  return kTileBlocks;
+  int w = kTileBlocks;
+  w = i == u.n_sink_tiles - 1 ? u.nsk - i * kTileBlocks : w;
+  w = i == u.n_tiles - 1 ? (u.qb + 1 - u.ws) - (u.n_tiles - 1 - u.n_sink_tiles) * kTileBlocks : w;
+  return w;
 }
 
 // Bits [0, n) set, for n clamped to [0, 64].
