@@ -247,8 +247,9 @@ int pa_plan(int n_q_heads, int n_kv_heads, int n_seq, const pa_seq* seqs, int n_
 /* Host-only, no GPU needed: the chunks pa_prefill_host cuts the query rows of
  * a call into, when the attention kernel runs n_pairs CTA pairs at once (76 on
  * a 152-SM GB300).  The rows of the sequences laid end to end (seqs order) go
- * in chunks of two waves of work units (a wave: one unit per pair), the
- * remainder last; a boundary inside a sequence falls on a multiple of
+ * in chunks of work units counted in waves (a wave: one unit per pair): one
+ * wave first, one wave last (or less: the remainder), two waves in between;
+ * a boundary inside a sequence falls on a multiple of
  * PA_UNIT_ROWS / G tokens (absolute position), so every work unit lies in one
  * chunk.  chunk_end (may be NULL) receives up to cap increasing row counts,
  * the last = the total rows; *n_chunks the count.  PA_EINVAL for bad shapes

@@ -232,7 +232,8 @@ def _chunk_cases():
 def test_host_chunks_cut_on_unit_boundaries_and_keep_every_unit_whole(pa, case):
     """The host-buffer path's chunks (pa_host_chunks, the schedule pa_prefill_host
     uses): increasing, ending at the total rows, at most two waves of units
-    (+ one unit's rounding) each, a boundary inside a sequence on a multiple of
+    (+ one unit's rounding) each and one wave (+ the same) for the first and the
+    last, a boundary inside a sequence on a multiple of
     a unit's tokens, and no work unit of the call's plan split between chunks."""
     _, hq, hkv, seqs, pairs = case
     ends = pa.pa_host_chunks(hq, hkv, seqs, pairs)
@@ -242,7 +243,9 @@ def test_host_chunks_cut_on_unit_boundaries_and_keep_every_unit_whole(pa, case):
     ut = pa.UNIT_ROWS // (hq // hkv)
     wave = max(ut, pairs * ut // hkv)
     assert ends[-1] == total and np.all(np.diff(ends) > 0)
-    assert np.all(np.diff(np.concatenate([[0], ends])) <= 2 * wave + ut)
+    sizes = np.diff(np.concatenate([[0], ends]))
+    assert np.all(sizes <= 2 * wave + ut)
+    assert sizes[0] <= wave + ut and sizes[-1] <= wave + ut
     for e in ends[:-1]:
         s = int(np.searchsorted(base, e, side="right")) - 1
         if base[s] < e < base[s + 1]:
