@@ -237,12 +237,24 @@ int pa_decode_plan(int n_kv_heads, int slots, int n_seq, const pa_seq* seqs, int
  * tiles visit: the union of the visible key blocks of the unit's query blocks. */
 #define PA_UNIT_ROWS 256
 
-/* Host-only planning, no GPU needed: the work units of a call in launch order
- * (longest first).  units_out (may be NULL) receives up to cap entries of
- * int32[4] = {sequence, kv head, first token, key tiles}.  Outputs: unit
- * count, total key tiles, widened rows. */
+/* Host-only planning, no GPU needed: the work units of a call, longest first
+ * (the launch then hands them to the kernel's SM pairs: pa_plan_pairs).
+ * units_out (may be NULL) receives up to cap entries of int32[4] = {sequence,
+ * kv head, first token, key tiles}.  Outputs: unit count, total key tiles,
+ * widened rows. */
 int pa_plan(int n_q_heads, int n_kv_heads, int n_seq, const pa_seq* seqs, int n_sink_blk, int n_win_blk,
             int32_t* units_out, int cap, int* n_units, long long* n_tiles, int* n_widened_rows);
+
+/* Host-only, no GPU needed: pa_plan's units as a launch hands them to n_pairs
+ * SM pairs (the attention kernel runs min(units, 76) pairs on a 152-SM
+ * GB300): longest first, each to the pair whose work so far (key tiles, plus
+ * two for each unit change) is least, ties to the lowest pair; then laid out
+ * pair by pair.  units_out (int32 [n_units][4], as pa_plan; may be NULL when
+ * cap is 0) receives them in that layout, pair_off (int32 [n_pairs + 1]) each
+ * pair's first unit and, last, the count.  PA_EINVAL for bad shapes,
+ * n_pairs < 1, or cap < the unit count when units_out is given. */
+int pa_plan_pairs(int n_q_heads, int n_kv_heads, int n_seq, const pa_seq* seqs, int n_sink_blk, int n_win_blk,
+                  int n_pairs, int32_t* units_out, int cap, int32_t* pair_off, int* n_units);
 
 /* Host-only, no GPU needed: the chunks pa_prefill_host cuts the query rows of
  * a call into, when the attention kernel runs n_pairs CTA pairs at once (76 on

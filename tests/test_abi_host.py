@@ -263,3 +263,49 @@ def test_host_chunks_rejects_bad_shapes(pa):
     for args in ((16, 3, seqs, 76), (16, 2, seqs, 0)):
         with pytest.raises(pa.PAError):
             pa.pa_host_chunks(*args)
+
+
+PAIR_CASES = [
+    ("4k", 16, 2, [(0, 0, 4096, 4096)], 1, 256, 76),
+    ("chunked_ragged", 16, 2, [(0, 1024, 2048, 3072), (2048, 6144, 2048, 8192), (4096, 30720, 2048, 32768),
+                               (6144, 12005, 2048, 14053)], 1, 256, 76),
+    ("few_units", 16, 2, [(0, 0, 100, 100)], 1, 256, 76),
+    ("g1_causal", 2, 2, [(0, 5, 3000, 3005)], 1, 0, 7),
+]
+
+
+@pytest.mark.parametrize("case", PAIR_CASES, ids=[c[0] for c in PAIR_CASES])
+def test_pair_plan_is_a_greedy_longest_first_schedule(pa, case):
+    """pa_plan_pairs (how a launch hands pa_plan's units to the kernel's SM
+    pairs): the same units, each once, laid out pair by pair, each pair's run
+    longest first; replaying the greedy rule (each unit, longest first, to the
+    least-loaded pair, ties to the lowest pair; a unit weighs its tiles + 2)
+    gives the same assignment, and no pair carries more than the mean load
+    plus one unit."""
+    _, hq, hkv, seqs, S, W, n_pairs = case
+    units, _, _ = pa.pa_plan(hq, hkv, seqs, S, W)
+    by_pair, off = pa.pa_plan_pairs(hq, hkv, seqs, S, W, n_pairs)
+    n = len(units)
+    assert off[0] == 0 and off[-1] == n and np.all(np.diff(off) >= 0)
+    assert sorted(map(tuple, by_pair.tolist())) == sorted(map(tuple, units.tolist()))
+    load = np.zeros(n_pairs, np.int64)
+    want = [[] for _ in range(n_pairs)]
+    for u in units.tolist():
+        p = int(np.argmin(load))  # argmin: the lowest pair among the least loaded
+        want[p].append(tuple(u))
+        load[p] += u[3] + 2
+    for p in range(n_pairs):
+        got = [tuple(x) for x in by_pair[off[p]:off[p + 1]].tolist()]
+        assert got == want[p], p
+        tiles = [x[3] for x in got]
+        assert tiles == sorted(tiles, reverse=True)
+    w = units[:, 3].astype(np.int64) + 2
+    assert load.max() <= w.sum() / n_pairs + w.max()
+
+
+def test_pair_plan_rejects_bad_arguments(pa):
+    seqs = [(0, 0, 100, 100)]
+    with pytest.raises(pa.PAError):
+        pa.pa_plan_pairs(16, 2, seqs, 1, 256, 0)
+    with pytest.raises(pa.PAError):
+        pa.pa_plan_pairs(16, 3, seqs, 1, 256, 76)

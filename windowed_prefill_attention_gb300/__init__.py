@@ -31,7 +31,7 @@ PA_P_F16, PA_P_U8 = 0, 1
 
 EXPORTED = ("pa_default_options", "pa_create", "pa_destroy", "pa_prefill", "pa_prefill_batch",
             "pa_prefill_batch_gated", "pa_prefill_host", "pa_kv_append", "pa_decode",
-            "pa_last_error", "pa_timing", "pa_strerror", "pa_plan", "pa_host_chunks", "pa_decode_plan",
+            "pa_last_error", "pa_timing", "pa_strerror", "pa_plan", "pa_plan_pairs", "pa_host_chunks", "pa_decode_plan",
             "pa_debug_gather",
             "pa_debug_maskset", "pa_debug_qcodes", "pa_debug_copy_streams_idle", "pa_prefill_noalloc",
             "pa_debug_noalloc_units")
@@ -64,6 +64,7 @@ _lib.pa_strerror.argtypes = [_i]
 _lib.pa_strerror.restype = C.c_char_p
 _lib.pa_plan.argtypes = [_i, _i, _i, C.POINTER(pa_seq), _i, _i, _vp, _i, C.POINTER(_i), C.POINTER(C.c_longlong),
                          C.POINTER(_i)]
+_lib.pa_plan_pairs.argtypes = [_i, _i, _i, C.POINTER(pa_seq), _i, _i, _i, _vp, _i, _vp, C.POINTER(_i)]
 _lib.pa_host_chunks.argtypes = [_i, _i, _i, C.POINTER(pa_seq), _i, _vp, _i, C.POINTER(_i)]
 _lib.pa_decode_plan.argtypes = [_i, _i, _i, C.POINTER(pa_seq), _i, _i, _vp, _i, C.POINTER(_i), C.POINTER(_i),
                                 C.POINTER(_i), C.POINTER(_i), C.POINTER(C.c_longlong)]
@@ -260,6 +261,21 @@ def pa_plan(n_q_heads, n_kv_heads, seqs, n_sink_blk, n_win_blk):
     _check(_lib.pa_plan(n_q_heads, n_kv_heads, len(s), s, n_sink_blk, n_win_blk, units.ctypes.data_as(C.c_void_p),
                         n_units.value, C.byref(n_units), C.byref(n_tiles), C.byref(n_rows)), "pa_plan")
     return units, n_tiles.value, n_rows.value
+
+
+def pa_plan_pairs(n_q_heads, n_kv_heads, seqs, n_sink_blk, n_win_blk, n_pairs):
+    """Host-only: pa_plan's units as a launch hands them to n_pairs SM pairs.  Returns
+    (units int32 [n, 4] laid out pair by pair, pair_off int32 [n_pairs + 1])."""
+    s = _seqs(seqs)
+    n = C.c_int()
+    off = np.zeros(n_pairs + 1, dtype=np.int32)
+    _check(_lib.pa_plan_pairs(n_q_heads, n_kv_heads, len(s), s, n_sink_blk, n_win_blk, n_pairs, None, 0,
+                              off.ctypes.data_as(C.c_void_p), C.byref(n)), "pa_plan_pairs")
+    units = np.zeros((n.value, 4), dtype=np.int32)
+    _check(_lib.pa_plan_pairs(n_q_heads, n_kv_heads, len(s), s, n_sink_blk, n_win_blk, n_pairs,
+                              units.ctypes.data_as(C.c_void_p), n.value, off.ctypes.data_as(C.c_void_p),
+                              C.byref(n)), "pa_plan_pairs")
+    return units, off
 
 
 def pa_host_chunks(n_q_heads, n_kv_heads, seqs, n_pairs):

@@ -11,9 +11,10 @@
 // (tcgen05.mma kind::f16), which hold them exactly: K in bf16 against the bf16
 // query, V in fp16 against P' in fp16.
 //
-// Pairs of SMs (clusters of two CTAs, one per SM) walk the longest-first
-// unit list with stride = the number of pairs.  A unit is 256 query rows of
-// one kv head (pa_tiles.cuh), 128 in each CTA; one 256-row tcgen05 MMA
+// Pairs of SMs (clusters of two CTAs, one per SM) each take the units the
+// host handed them (longest first, each to the pair with the least work so
+// far), or walk the list with stride = the number of pairs.  A unit is 256
+// query rows of one kv head (pa_tiles.cuh), 128 in each CTA; one 256-row tcgen05 MMA
 // (cta_group::2, issued by the even CTA) covers both, with the B operand (K
 // keys for QK^T, V^T dims for PV) split between the two CTAs' shared memory,
 // so each SM stores and reads only half of every K/V tile.  Key tiles are
@@ -136,7 +137,8 @@ struct Ctx {
   uint32_t sbase;    // shared address of the aligned base
   uint32_t tb;       // TMEM base address (the same in both CTAs)
   uint32_t rank;     // 0: the even CTA of the pair (issues the MMAs), 1: the odd one
-  int pair, n_pairs; // this pair's index and the number of pairs (units are strided over pairs)
+  int pair, n_pairs; // this pair's index and the number of pairs
+  int u0, u1, ustep; // this pair's units: u0, u0 + ustep, ... below u1
   WaitCtl wc;
   __device__ uint32_t bar(int i) const { return sbase + kSmBars + 8 * i; }
   // Bounded wait.  Phases completed by the other CTA of the pair hand over
@@ -189,7 +191,7 @@ __device__ __forceinline__ void role_producer_k(const AttnParams& p, const AttnM
   const int r = s & 3, par = s >> 2;
   uint32_t uses = 0, tc = 0;  // tiles this slot held; tiles so far
   bool ok = true;
-  for (int u = c.pair; u < p.n_units && ok; u += c.n_pairs) {
+  for (int u = c.u0; u < c.u1 && ok; u += c.ustep) {
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
     const UnitGeom ug = unit_geom(un.t0, 2 * p.TQ, sg, p.S, p.W);
@@ -222,7 +224,7 @@ __device__ __forceinline__ void role_producer_v(const AttnParams& p, const AttnM
   const int ch = s & 1, par = s >> 1;
   uint32_t uses = 0, tc = 0;  // tiles of this parity so far; tiles so far
   bool ok = true;
-  for (int u = c.pair; u < p.n_units && ok; u += c.n_pairs) {
+  for (int u = c.u0; u < c.u1 && ok; u += c.ustep) {
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
     const UnitGeom ug = unit_geom(un.t0, 2 * p.TQ, sg, p.S, p.W);
@@ -275,8 +277,8 @@ __device__ __forceinline__ void role_producer_q(const AttnParams& p, const AttnM
   int prev_t0 = 0, prev_g = 0;
   SeqGeom prev_sg{};
   // rows still on their way in from another stream: wait for their flag
-  if (r < 4 && p.q_ready && c.pair < p.n_units) ok = flag_wait(p.q_ready, p.q_epoch, c.wc, 18);
-  for (int u = c.pair; u < p.n_units && ok; u += c.n_pairs) {
+  if (r < 4 && p.q_ready && c.u0 < c.u1) ok = flag_wait(p.q_ready, p.q_epoch, c.wc, 18);
+  for (int u = c.u0; u < c.u1 && ok; u += c.ustep) {
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
     const int t0 = un.t0 + (int)c.rank * p.TQ;  // this CTA's first token
@@ -422,7 +424,7 @@ __device__ __forceinline__ void role_mma(const AttnParams& p, const Ctx& c) {
   const uint64_t vd00 = sdesc_k_sw128(c.sbase + kSmV), vd01 = sdesc_k_sw128(c.sbase + kSmV + kVSlotBytes);
   const uint64_t vd10 = sdesc_k_sw128(c.sbase + kSmV + 2 * kVSlotBytes);
   const uint64_t vd11 = sdesc_k_sw128(c.sbase + kSmV + 3 * kVSlotBytes);
-  for (int u = c.pair; u < p.n_units && ok; u += c.n_pairs, ++k_unit) {
+  for (int u = c.u0; u < c.u1 && ok; u += c.ustep, ++k_unit) {
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
     const UnitGeom ug = unit_geom(un.t0, 2 * p.TQ, sg, p.S, p.W);
@@ -519,7 +521,7 @@ __device__ __forceinline__ void role_softmax(const AttnParams& p, const Ctx& c, 
   uint32_t tc = 0;
   int k_unit = 0;
   bool ok = true;
-  for (int u = c.pair; u < p.n_units && ok; u += c.n_pairs, ++k_unit) {
+  for (int u = c.u0; u < c.u1 && ok; u += c.ustep, ++k_unit) {
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
     const UnitGeom ug = unit_geom(un.t0, 2 * p.TQ, sg, p.S, p.W);
@@ -893,7 +895,7 @@ __device__ __forceinline__ void role_correction(const AttnParams& p, const Ctx& 
   bool ok = true;
   int prev_t0 = 0, prev_g = 0;
   SeqGeom prev_sg{};
-  for (int u = c.pair; u < p.n_units && ok; u += c.n_pairs, ++k_unit) {
+  for (int u = c.u0; u < c.u1 && ok; u += c.ustep, ++k_unit) {
     const Unit un = p.units[u];
     const SeqGeom sg = p.seqs[un.seq];
     if (p.q_mode == 1) {  // the unit's Q codes, in place, before the MMA may read Q
@@ -930,6 +932,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   c.rank = cluster_rank();
   c.pair = (int)(blockIdx.x >> 1);
   c.n_pairs = (int)(gridDim.x >> 1);
+  if (p.pair_off) {  // the host's assignment (longest units first, to the least-loaded pair)
+    c.u0 = p.pair_off[c.pair];
+    c.u1 = p.pair_off[c.pair + 1];
+    c.ustep = 1;
+  } else {
+    c.u0 = c.pair;
+    c.u1 = p.n_units;
+    c.ustep = c.n_pairs;
+  }
   c.wc = WaitCtl{p.err, p.wait_ns};
   // a launch queued behind this one that reads nothing this one writes may
   // start on each pair this one leaves
@@ -1072,8 +1083,9 @@ int attention_pairs(int n_sm) {
 cudaError_t launch_attention(const AttnParams& p, const AttnMaps& m, int n_sm, cudaStream_t st, bool overlap_prev) {
   cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
   if (e != cudaSuccess) return e;
-  // persistent grid: one CTA pair per co-resident cluster slot (or per unit)
-  const int pairs = imax(1, imin(p.n_units, attention_pairs(n_sm)));
+  // persistent grid: one CTA pair per co-resident cluster slot (or per unit),
+  // or the pairs the host assigned the units to
+  const int pairs = p.pair_off ? p.plan_pairs : imax(1, imin(p.n_units, attention_pairs(n_sm)));
   if (!overlap_prev) {
     attention_kernel<<<2 * pairs, kThreads, kAttnSmem, st>>>(p, m);
     return cudaGetLastError();

@@ -49,6 +49,11 @@ struct AttnParams {
   const SeqGeom* seqs;
   const Unit* units;
   int n_units;
+  // units assigned to SM pairs by the host: pair i runs units [pair_off[i],
+  // pair_off[i + 1]) on a grid of plan_pairs pairs; plan_pairs = 0: pair i runs
+  // units i, i + n_pairs, ... of the list
+  const int* pair_off;
+  int plan_pairs;
   const float* ks;
   const float* vs;
   const unsigned int* vsmax;
