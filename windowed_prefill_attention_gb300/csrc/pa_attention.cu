@@ -339,6 +339,7 @@ __device__ __forceinline__ void role_producer_q(const AttnParams& p, const AttnM
 // S(t) = Q K(t)^T for a tile: 16 MMAs, Q region r at qd + 1024 r and the K
 // slot's region r at kd + 512 r (start addresses in 16-byte units), k-step q
 // at + 2 q within the 128-byte swizzled rows; the first MMA overwrites D.
+static_assert(kRegionBytes / 16 == 1024 && kKSlotBytes / 16 == 512, "descriptor steps of mma_qk_tile");
 __device__ __forceinline__ void mma_qk_tile(uint32_t d, uint64_t qd, uint64_t kd, uint32_t idesc) {
   asm volatile(
       "{\n\t.reg .b64 a, b;\n\t.reg .pred pf, pt;\n\t"
@@ -380,6 +381,7 @@ __device__ __forceinline__ void mma_qk_tile(uint32_t d, uint64_t qd, uint64_t kd
 // O (+)= P' V for a full tile: 8 MMAs, P' of 64-key chunk ch at TMEM column
 // a + 64 ch + 8 ks, its V^T slot at vd0 / vd1 + 2 ks; the first MMA
 // accumulates iff acc0.
+static_assert(kChunkKeys == 64 && kTileKeys == 2 * kChunkKeys, "TMEM column steps of mma_pv_tile");
 __device__ __forceinline__ void mma_pv_tile(uint32_t d, uint32_t a, uint64_t vd0, uint64_t vd1, uint32_t idesc,
                                             uint32_t acc0) {
   asm volatile(
